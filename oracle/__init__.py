@@ -1,0 +1,334 @@
+"""CPU oracle for FP4 block-scaled quantize-and-multiply -- TEST INFRASTRUCTURE.
+
+A numpy-level wrapper around ``liboracle.so`` (plain C, see ``oracle.c``).
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg may import this package.  It never imports the CUDA library
+and the CUDA library never imports it.
+
+Inputs are float32 numpy arrays (BF16 tensors widened exactly).  Format ids
+are this module's own: UE5M3=0, NVFP4=1, MXFP4=2.
+
+Composition helpers (``quantize``, ``quantize_transpose``, ``amax_pair``)
+follow the method's steps in the pages' order: per-tensor scale from the held
+amax and T, then per-copy block scales and payloads; the transposed copy is
+the tensor transposed, optionally rotated by the fixed-sign Hadamard along
+its new rows, then quantised exactly like a row-wise copy.
+
+Functions whose result no page or closed form fixes say "parity unpinned" in
+their docstring.
+"""
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import build as _build
+
+UE5M3, NVFP4, MXFP4 = 0, 1, 2
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        i8p = ctypes.POINTER(ctypes.c_int8)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        i64, i32, u32, u64, f32 = (ctypes.c_int64, ctypes.c_int, ctypes.c_uint32,
+                                   ctypes.c_uint64, ctypes.c_float)
+        sig = {
+            "orc_block_size": (i32, [i32]),
+            "orc_e2m1_value": (ctypes.c_double, [i32]),
+            "orc_e2m1_rne": (i32, [f32]),
+            "orc_ue5m3_value": (ctypes.c_double, [i32]),
+            "orc_ue5m3_rne_sat": (i32, [f32]),
+            "orc_e4m3_value": (ctypes.c_double, [i32]),
+            "orc_e4m3_rne_sat": (i32, [f32]),
+            "orc_e8m0_value": (ctypes.c_double, [i32]),
+            "orc_scale_value": (ctypes.c_double, [i32, i32]),
+            "orc_philox4x32_10": (None, [u32p, u32p, u32p]),
+            "orc_e2m1_sr": (i32, [f32, u32]),
+            "orc_hadamard": (None, [f32p, i32, u32]),
+            "orc_hadamard_rows": (None, [f32p, i64, i64, i32, u32]),
+            "orc_tensor_scale": (None, [i32, f32, f32, f32p, f32p]),
+            "orc_amax": (f32, [f32p, i64]),
+            "orc_quantize_rows": (None, [f32p, i64, i64, i32, f32, f32, i32, u64, u32,
+                                         u32, i64, u8p, u8p]),
+            "orc_quantize_2d": (None, [f32p, i64, i64, i32, f32, f32, u8p, u8p, u8p, u8p]),
+            "orc_sf_mma_bytes": (i64, [i64, i64]),
+            "orc_sf_to_mma": (None, [u8p, i64, i64, u8p]),
+            "orc_remap_ue5m3": (i32, [u8p, u8p, i64, i64, u8p, i8p]),
+            "orc_gemm_model": (None, [u8p, u8p, u8p, u8p, i32, i64, i64, i64, f32, f32, i32,
+                                      i64p, i64p, i64, f32p, f64p, f64p]),
+            "orc_canon1024": (f32, [f32]),
+            "orc_round_sum_f32": (f32, [f64p, i32, i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a, t):
+    return a.ctypes.data_as(ctypes.POINTER(t))
+
+
+def _threads():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+# ---------------------------------------------------------------- formats
+
+def block_size(fmt):
+    return lib().orc_block_size(fmt)
+
+
+def e2m1_value(code):
+    return lib().orc_e2m1_value(int(code))
+
+
+def e2m1_rne(v):
+    return lib().orc_e2m1_rne(float(v))
+
+
+def e2m1_sr(v, r16):
+    return lib().orc_e2m1_sr(float(v), int(r16))
+
+
+def ue5m3_value(code):
+    return lib().orc_ue5m3_value(int(code))
+
+
+def ue5m3_rne_sat(v):
+    return lib().orc_ue5m3_rne_sat(float(v))
+
+
+def e4m3_value(code):
+    return lib().orc_e4m3_value(int(code))
+
+
+def e4m3_rne_sat(v):
+    return lib().orc_e4m3_rne_sat(float(v))
+
+
+def e8m0_value(code):
+    return lib().orc_e8m0_value(int(code))
+
+
+def scale_value(fmt, code):
+    return lib().orc_scale_value(fmt, int(code))
+
+
+def philox4x32_10(ctr, key):
+    c = np.asarray(ctr, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c, ctypes.c_uint32), _p(k, ctypes.c_uint32),
+                            _p(out, ctypes.c_uint32))
+    return out
+
+
+def hadamard(x, n, signs=0):
+    y = np.ascontiguousarray(x, dtype=np.float32).copy()
+    lib().orc_hadamard(_p(y, ctypes.c_float), n, signs)
+    return y
+
+
+def hadamard_rows(x, n, signs=0):
+    y = np.ascontiguousarray(x, dtype=np.float32).copy()
+    R, C = y.shape
+    assert C % n == 0
+    lib().orc_hadamard_rows(_p(y, ctypes.c_float), R, C, n, signs)
+    return y
+
+
+def canon1024(c):
+    return lib().orc_canon1024(float(c))
+
+
+def round_sum_f32(terms, rtz):
+    t = np.ascontiguousarray(terms, dtype=np.float64)
+    return lib().orc_round_sum_f32(_p(t, ctypes.c_double), len(t), 1 if rtz else 0)
+
+
+# ----------------------------------------------------------------- scales
+
+def tensor_scale(fmt, T, amax):
+    se, sd = ctypes.c_float(), ctypes.c_float()
+    lib().orc_tensor_scale(fmt, float(T), float(amax), ctypes.byref(se), ctypes.byref(sd))
+    return se.value, sd.value
+
+
+def amax(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return lib().orc_amax(_p(x, ctypes.c_float), x.size)
+
+
+def amax_pair(x, hadamard_n=0, signs=0):
+    """(max|x|, max|y|) where y is the transposed view rotated by the fixed-sign
+    Hadamard along its rows (y = x^T when hadamard_n == 0)."""
+    a = amax(x)
+    if hadamard_n == 0:
+        return a, a
+    return a, amax(hadamard_rows(np.ascontiguousarray(x.T), hadamard_n, signs))
+
+
+# -------------------------------------------------------------- quantizers
+
+def quantize_rows(x, fmt, s_enc, s_dec, sr=False, seed=0, offset=0, copy_id=0,
+                  threads=None):
+    """One copy, blocks along rows.  Returns (q [R, C/2] u8, sf [R, C/B] u8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    B = block_size(fmt)
+    assert C % B == 0
+    q = np.zeros((R, C // 2), dtype=np.uint8)
+    sf = np.zeros((R, C // B), dtype=np.uint8)
+    nt = threads or _threads()
+    chunk = max(1, -(-R // nt))
+
+    def run(r0):
+        r1 = min(R, r0 + chunk)
+        if r1 <= r0:
+            return
+        lib().orc_quantize_rows(_p(x[r0:r1], ctypes.c_float), r1 - r0, C, fmt, s_enc, s_dec,
+                                1 if sr else 0, seed, offset, copy_id, r0,
+                                _p(q[r0:r1], ctypes.c_uint8), _p(sf[r0:r1], ctypes.c_uint8))
+
+    if nt == 1 or R <= chunk:
+        run(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(0, R, chunk)))
+    return q, sf
+
+
+def quantize_2d(x, fmt, s_enc, s_dec):
+    """B x B tiles shared by both copies.  Returns (q_row, sf_row, q_col, sf_col)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    B = block_size(fmt)
+    assert R % B == 0 and C % B == 0
+    q_row = np.zeros((R, C // 2), np.uint8)
+    sf_row = np.zeros((R, C // B), np.uint8)
+    q_col = np.zeros((C, R // 2), np.uint8)
+    sf_col = np.zeros((C, R // B), np.uint8)
+    lib().orc_quantize_2d(_p(x, ctypes.c_float), R, C, fmt, s_enc, s_dec,
+                          _p(q_row, ctypes.c_uint8), _p(sf_row, ctypes.c_uint8),
+                          _p(q_col, ctypes.c_uint8), _p(sf_col, ctypes.c_uint8))
+    return q_row, sf_row, q_col, sf_col
+
+
+def quantize(x, amax_held, fmt, T=448.0, block2d=False, sr=False, seed=0, offset=0):
+    """Row-wise copy of x (what the library's fp4_quantize emits).
+    Returns dict(q, sf, s_dec) with sf in the plain [R, C/B] layout."""
+    s_enc, s_dec = tensor_scale(fmt, T, amax_held)
+    if block2d:
+        q, sf, _, _ = quantize_2d(x, fmt, s_enc, s_dec)
+    else:
+        q, sf = quantize_rows(x, fmt, s_enc, s_dec, sr=sr, seed=seed, offset=offset,
+                              copy_id=0)
+    return dict(q=q, sf=sf, s_dec=s_dec)
+
+
+def quantize_transpose(x, amax_row, amax_col, fmt, T=448.0, block2d=False, sr_row=False,
+                       sr_col=False, seed=0, offset=0, hadamard_n=0, signs=0):
+    """Row-wise copy and transposed copy (what fp4_quantize_transpose emits).
+    The transposed copy quantises x^T (rotated by the fixed-sign Hadamard along
+    its rows when hadamard_n is 16 or 32) with its own held amax."""
+    s_enc_r, s_dec_r = tensor_scale(fmt, T, amax_row)
+    if block2d:
+        q_r, sf_r, q_c, sf_c = quantize_2d(x, fmt, s_enc_r, s_dec_r)
+        return (dict(q=q_r, sf=sf_r, s_dec=s_dec_r), dict(q=q_c, sf=sf_c, s_dec=s_dec_r))
+    q_r, sf_r = quantize_rows(x, fmt, s_enc_r, s_dec_r, sr=sr_row, seed=seed, offset=offset,
+                              copy_id=0)
+    xt = np.ascontiguousarray(np.asarray(x, dtype=np.float32).T)
+    if hadamard_n:
+        xt = hadamard_rows(xt, hadamard_n, signs)
+    s_enc_c, s_dec_c = tensor_scale(fmt, T, amax_col)
+    q_c, sf_c = quantize_rows(xt, fmt, s_enc_c, s_dec_c, sr=sr_col, seed=seed, offset=offset,
+                              copy_id=1)
+    return dict(q=q_r, sf=sf_r, s_dec=s_dec_r), dict(q=q_c, sf=sf_c, s_dec=s_dec_c)
+
+
+# ------------------------------------------------------- tensor-core scales
+
+def sf_mma_bytes(R, Cb):
+    return lib().orc_sf_mma_bytes(R, Cb)
+
+
+def sf_to_mma(sf):
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    R, Cb = sf.shape
+    out = np.zeros(sf_mma_bytes(R, Cb), np.uint8)
+    lib().orc_sf_to_mma(_p(sf, ctypes.c_uint8), R, Cb, _p(out, ctypes.c_uint8))
+    return out
+
+
+def remap_ue5m3(sf, q):
+    """UE5M3 -> (E4M3 codes, per-row shift, window failures); plain layout."""
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    R, Cb = sf.shape
+    out = np.zeros_like(sf)
+    shift = np.zeros(R, np.int8)
+    fails = lib().orc_remap_ue5m3(_p(sf, ctypes.c_uint8), _p(q, ctypes.c_uint8), R, Cb,
+                                  _p(out, ctypes.c_uint8), _p(shift, ctypes.c_int8))
+    return out, shift, fails
+
+
+# ------------------------------------------------------------------ GEMM
+
+def gemm_model(qa, sfa, qb, sfb, fmt, K, s_dec_a, s_dec_b, mi, ni, canon=False,
+               threads=None):
+    """Probe-matched model, exact decoded-operand reference and |p| magnitude
+    for outputs (mi[t], ni[t]) of D = A B^T.  Returns (y_model f32,
+    y_exact f64, s_abs f64)."""
+    qa = np.ascontiguousarray(qa, np.uint8)
+    qb = np.ascontiguousarray(qb, np.uint8)
+    sfa = np.ascontiguousarray(sfa, np.uint8)
+    sfb = np.ascontiguousarray(sfb, np.uint8)
+    mi = np.ascontiguousarray(mi, np.int64)
+    ni = np.ascontiguousarray(ni, np.int64)
+    n = len(mi)
+    y = np.zeros(n, np.float32)
+    ye = np.zeros(n, np.float64)
+    sa = np.zeros(n, np.float64)
+    M, N = qa.shape[0], qb.shape[0]
+    nt = threads or _threads()
+    chunk = max(1, -(-n // nt))
+
+    def run(t0):
+        t1 = min(n, t0 + chunk)
+        if t1 <= t0:
+            return
+        lib().orc_gemm_model(_p(qa, ctypes.c_uint8), _p(sfa, ctypes.c_uint8),
+                             _p(qb, ctypes.c_uint8), _p(sfb, ctypes.c_uint8), fmt, M, N, K,
+                             s_dec_a, s_dec_b, 1 if canon else 0,
+                             _p(mi[t0:t1], ctypes.c_int64), _p(ni[t0:t1], ctypes.c_int64),
+                             t1 - t0, _p(y[t0:t1], ctypes.c_float),
+                             _p(ye[t0:t1], ctypes.c_double), _p(sa[t0:t1], ctypes.c_double))
+
+    if nt == 1 or n <= chunk:
+        run(0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(run, range(0, n, chunk)))
+    return y, ye, sa
+
+
+def gemm_model_full(qa, sfa, qb, sfb, fmt, K, s_dec_a, s_dec_b, canon=False):
+    M, N = qa.shape[0], qb.shape[0]
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    y, ye, sa = gemm_model(qa, sfa, qb, sfb, fmt, K, s_dec_a, s_dec_b, mm.ravel(),
+                           nn.ravel(), canon=canon)
+    return y.reshape(M, N), ye.reshape(M, N), sa.reshape(M, N)
