@@ -1,0 +1,447 @@
+"""Benchmark of the FP4 block-scaled quantize-and-multiply hot path on GB300.
+
+One step = one refresh step (current amax, D = 1) of a linear layer's forward
+and backward pass through the FP4 path on the 8B MLP down_proj shapes:
+  amax(X), amax(W), amax(dY);
+  producers: X row + transposed (T=448), W 2D 16x16 row + transposed,
+             dY row + transposed with Philox stochastic rounding (seed 42);
+  UE5M3 scale remap onto the tensor core's E4M3 scale path (both copies);
+  GEMMs: fprop Y = X W^T (8192 x 4096 x 14336, BF16 out),
+         dgrad dX = dY W (8192 x 14336 x 4096, BF16 out),
+         wgrad dW = dY^T X (4096 x 14336 x 8192, FP32 out).
+Inputs are seeded synthetic tensors with the workload's distributions,
+resident in HBM when the timed region starts; L2 is flushed (256 MB write)
+before every timed step.
+
+`value` is the step's roofline-normalised throughput: the time the step's
+kernels would take at the roofline (quantizer and amax bytes at the measured
+HBM bandwidth, GEMM flops at the FP4 dense peak) divided by the measured step
+time, in % of one GB300, summed over GPUs (each rank runs its own replica).
+
+`--impl reference` times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload, extrapolated to a full step.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+M_TOK, K_FF, N_MODEL = 8192, 14336, 4096
+WORKLOAD = "8B MLP down_proj fwd+bwd (refresh step), UE5M3-b16"
+FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32"}
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor ratio on GB300
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+def work_model(fmt):
+    """Algorithmic bytes / flops of one step (what the method must move)."""
+    B = 32 if fmt == 2 else 16
+    per_copy = 0.5 + 1.0 / B
+    ex, ew, edy = M_TOK * K_FF, N_MODEL * K_FF, M_TOK * N_MODEL
+    amax_bytes = 2.0 * (ex + ew + edy)
+    quant_bytes = {
+        "X": ex * (2 + 2 * per_copy) + 8,
+        "W": ew * (2 + 2 * per_copy) + 8,
+        "dY": edy * (2 + 2 * per_copy) + 8,
+    }
+    gemms = {
+        "fprop": (M_TOK, N_MODEL, K_FF, 2),
+        "dgrad": (M_TOK, K_FF, N_MODEL, 2),
+        "wgrad": (N_MODEL, K_FF, M_TOK, 4),
+    }
+    flops = {k: 2.0 * m * n * k_ for k, (m, n, k_, _) in gemms.items()}
+    return amax_bytes, quant_bytes, gemms, flops
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Layer:
+    """All device buffers of one step, allocated once; `step()` enqueues the
+    whole hot path on the current stream through the C ABI."""
+
+    def __init__(self, fmt, seed, device):
+        import fp4_block_scaled_quantize_gb300 as fq
+        from fp4_block_scaled_quantize_gb300 import inputs
+        self.fq = fq
+        d = inputs.down_proj_8b(seed=seed)
+        self.host = {k: v.pin_memory() for k, v in d.items()}
+        self.X, self.W, self.dY = (self.host[k].to(device) for k in ("X", "W", "dY"))
+        self.fmt = fmt
+        mma = fq.FP4_SF_MMA
+        self.px = fq.params(format=fmt, T=448.0, sf_layout=mma)
+        self.pw = fq.params(format=fmt, T=448.0, block2d=True, sf_layout=mma)
+        self.pdy = fq.params(format=fmt, T=448.0, round_row=fq.FP4_ROUND_SR,
+                             round_col=fq.FP4_ROUND_SR, sr_seed=42, sf_layout=mma)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.amax = {k: (torch.zeros(1, **f32), torch.zeros(1, **f32)) for k in ("X", "W", "dY")}
+        for k, t in (("X", self.X), ("W", self.W), ("dY", self.dY)):
+            fq._check(fq.fp4_amax(t, 0, 0, *self.amax[k]), "amax")
+        self.xr, self.xc = fq.quantize_transpose(self.X, *self.amax["X"], self.px)
+        self.wr, self.wc = fq.quantize_transpose(self.W, *self.amax["W"], self.pw)
+        self.dyr, self.dyc = fq.quantize_transpose(self.dY, *self.amax["dY"], self.pdy)
+        self.Y = torch.empty((M_TOK, N_MODEL), dtype=torch.bfloat16, device=device)
+        self.dX = torch.empty((M_TOK, K_FF), dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty((N_MODEL, K_FF), dtype=torch.float32, device=device)
+        self.launches_per_step = 3 + 3 + 3 + (6 if fmt == 0 else 0)
+
+    def _qt(self, x, key, p, r, c):
+        fq = self.fq
+        a_r, a_c = self.amax[key]
+        fq._check(fq.fp4_quantize_transpose(x, a_r, a_c, p, r.q, r.sf, r.s_dec, r.row_shift,
+                                            c.q, c.sf, c.s_dec, c.row_shift), "qt " + key)
+
+    def step(self, events=None):
+        fq = self.fq
+        ev = events if events is not None else {}
+
+        def mark(name):
+            if name in ev:
+                ev[name].record()
+
+        mark("amax")
+        for k, t in (("X", self.X), ("W", self.W), ("dY", self.dY)):
+            fq._check(fq.fp4_amax(t, 0, 0, *self.amax[k]), "amax")
+        mark("quant_X")
+        self._qt(self.X, "X", self.px, self.xr, self.xc)
+        mark("quant_W")
+        self._qt(self.W, "W", self.pw, self.wr, self.wc)
+        mark("quant_dY")
+        self._qt(self.dY, "dY", self.pdy, self.dyr, self.dyc)
+        mark("fprop")
+        fq.gemm(self.xr, self.wr, out=self.Y)
+        mark("dgrad")
+        fq.gemm(self.dyr, self.wc, out=self.dX)
+        mark("wgrad")
+        fq.gemm(self.dyc, self.xc, out=self.dW)
+        mark("end")
+
+
+def run_gpu(args, world, rank, local):
+    import fp4_block_scaled_quantize_gb300 as fq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    layer = Layer(args.format, seed=args.seed + rank, device=dev)
+    amax_b, qbytes, gemms, flops = work_model(args.format)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    names = ["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad", "end"]
+
+    for _ in range(args.warmup):
+        layer.step()
+    st = fq.fp4_status_sync()
+    if st != fq.FP4_OK:
+        raise RuntimeError("device status after warm-up: " + fq.STATUS_NAMES[st])
+    torch.cuda.synchronize()
+    barrier(world)
+
+    per_kernel = {n: 0.0 for n in names[:-1]}
+    total_ms = 0.0
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
+            torch.cuda.synchronize()
+            layer.step(ev)
+            torch.cuda.synchronize()
+            for a, b in zip(names, names[1:]):
+                per_kernel[a] += ev[a].elapsed_time(ev[b])
+            total_ms += ev["amax"].elapsed_time(ev["end"])
+    barrier(world)
+    st = fq.fp4_status_sync()
+    if st != fq.FP4_OK:
+        raise RuntimeError("device status after timed steps: " + fq.STATUS_NAMES[st])
+    ms_step = reduce_max(total_ms / args.steps, world)
+
+    # roofline-ideal time of one step (seconds)
+    hbm = pk["hbm_gbs"] * 1e9
+    ideal = amax_b / hbm + sum(qbytes.values()) / hbm + sum(flops.values()) / (fp4_peak * 1e12)
+    value = 100.0 * ideal / (ms_step * 1e-3) * world
+    avg = {k: v / args.steps for k, v in per_kernel.items()}
+    q_ms = avg["quant_X"] + avg["quant_W"] + avg["quant_dY"]
+    g_ms = avg["fprop"] + avg["dgrad"] + avg["wgrad"]
+    quant_gbs = sum(qbytes.values()) / (q_ms * 1e-3) / 1e9
+    gemm_tflops = sum(flops.values()) / (g_ms * 1e-3) / 1e12
+    dominant = max(("fprop", "dgrad", "wgrad"), key=lambda k: avg[k])
+    dom_tflops = flops[dominant] / (avg[dominant] * 1e-3) / 1e12
+    traffic = load_traffic(dominant)
+
+    # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
+    e2e = run_e2e(layer, args, world, ideal)
+
+    clocks = clk.summary()
+    out = {
+        "metric": "quantize GB/s and FP4 block-scaled GEMM TFLOP/s, each as % of GB300 roofline",
+        "value": round(value, 3),
+        "unit": "% of one GB300 roofline (step ideal time / step time, summed over GPUs)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1 payload x fp32 accumulate (u8 codes)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "format": FMT_NAMES[args.format],
+                   "X": [M_TOK, K_FF], "W": [N_MODEL, K_FF], "dY": [M_TOK, N_MODEL],
+                   "amax": "current (D=1 refresh step)", "l2": "flushed before each step",
+                   "parallelism": f"replicas x{world}"},
+        "quantize": {"gbs": round(quant_gbs, 1), "frac": round(quant_gbs / pk["hbm_gbs"], 4),
+                     "ms": round(q_ms, 4)},
+        "amax": {"gbs": round(amax_b / (avg["amax"] * 1e-3) / 1e9, 1),
+                 "ms": round(avg["amax"], 4)},
+        "gemm": {"tflops": round(gemm_tflops, 1), "frac": round(gemm_tflops / fp4_peak, 4),
+                 "ms": {k: round(avg[k], 4) for k in ("fprop", "dgrad", "wgrad")}},
+        "roofline": {"kernel": "k_gemm (" + dominant + ")", "bound": "tensor",
+                     "achieved": round(dom_tflops, 1), "peak": round(fp4_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(dom_tflops / fp4_peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal "
+                                    "FP4/BF16 dense ratio)"},
+        "clocks": clocks,
+        "gpu_launches": layer.launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(args, ideal)
+        print(json.dumps(out))
+
+
+def run_e2e(layer, args, world, ideal):
+    """Same step with host inputs and outputs: pinned H2D copies of X, W, dY,
+    the step, and D2H of Y, dX, dW, all inside the timed region."""
+    fq = layer.fq
+    host_out = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for k, t in (("Y", layer.Y), ("dX", layer.dX), ("dW", layer.dW))}
+    h2d = sum(t.numel() * t.element_size() for t in layer.host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        layer.X.copy_(layer.host["X"], non_blocking=True)
+        layer.W.copy_(layer.host["W"], non_blocking=True)
+        layer.dY.copy_(layer.host["dY"], non_blocking=True)
+        layer.step()
+        host_out["Y"].copy_(layer.Y, non_blocking=True)
+        host_out["dX"].copy_(layer.dX, non_blocking=True)
+        host_out["dW"].copy_(layer.dW, non_blocking=True)
+    e.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e) / steps, world)
+    fq._check(fq.fp4_status_sync(), "e2e")
+    return {"value": round(100.0 * ideal / (ms * 1e-3) * world, 3),
+            "unit": "% of one GB300 roofline (summed over GPUs)", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def load_traffic(kernel):
+    """dram read+write bytes per launch of the dominant kernel from the
+    committed ncu summary (null when absent or stale)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    v = d.get(kernel)
+    return None if v is None else v.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------ CPU oracle arm
+
+def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
+    """Time the oracle on a bounded sample of one step and extrapolate.
+    Returns (seconds per full step, threads used, description)."""
+    import numpy as np
+
+    import oracle as orc
+    from fp4_block_scaled_quantize_gb300 import inputs
+    fmt = {0: orc.UE5M3, 1: orc.NVFP4, 2: orc.MXFP4}[args.format]
+    R = sample_rows
+    g = inputs.down_proj_8b(seed=args.seed, M=R * 2, K=K_FF, N=N_MODEL)
+    threads = os.cpu_count() or 1
+    t_quant = 0.0
+    elems_done = 0
+    for name, x in (("X", g["X"][:R]), ("W", g["W"][:R]), ("dY", g["dY"][:R])):
+        x32 = x.float().numpy()
+        t0 = time.perf_counter()
+        a = orc.amax(x32)
+        orc.quantize_transpose(x32, a, a, fmt, block2d=(name == "W"), sr_row=(name == "dY"),
+                               sr_col=(name == "dY"), seed=42)
+        t_quant += time.perf_counter() - t0
+        elems_done += x32.size
+    total_elems = M_TOK * K_FF + N_MODEL * K_FF + M_TOK * N_MODEL
+    quant_s = t_quant / elems_done * total_elems
+    gemm_s = 0.0
+    gemm_desc = []
+    for name, (M, N, K) in (("fprop", (M_TOK, N_MODEL, K_FF)), ("dgrad", (M_TOK, K_FF, N_MODEL)),
+                            ("wgrad", (N_MODEL, K_FF, M_TOK))):
+        rng = np.random.default_rng(1)
+        a = orc.quantize(rng.standard_normal((4, K)).astype(np.float32), 4.0, fmt)
+        b = orc.quantize(rng.standard_normal((4, K)).astype(np.float32), 4.0, fmt)
+        mi = np.arange(sample_outputs) % 4
+        ni = (np.arange(sample_outputs) // 4) % 4
+        t0 = time.perf_counter()
+        orc.gemm_model(a["q"], a["sf"], b["q"], b["sf"], fmt, K, a["s_dec"], b["s_dec"], mi, ni)
+        dt = time.perf_counter() - t0
+        gemm_s += dt / sample_outputs * M * N
+        gemm_desc.append(f"{name} {sample_outputs} outputs")
+    desc = (f"amax+producers on {R} rows of each of X, W, dY; probe-matched GEMM model on "
+            + ", ".join(gemm_desc) + "; extrapolated to the full step")
+    return quant_s + gemm_s, threads, desc
+
+
+def cpu_baseline(args, ideal):
+    secs, threads, desc = oracle_step_seconds(args)
+    return {"value": 100.0 * ideal / secs, "unit": "% of one GB300 roofline", "cores": threads,
+            "kind": "oracle", "sample": desc, "seconds_per_step_extrapolated": round(secs, 1)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    pk = peaks()
+    amax_b, qbytes, gemms, flops = work_model(args.format)
+    ideal = (amax_b / (pk["hbm_gbs"] * 1e9) + sum(qbytes.values()) / (pk["hbm_gbs"] * 1e9)
+             + sum(flops.values()) / (pk["bf16_tflops"] * FP4_OVER_BF16 * 1e12))
+    for _ in range(args.warmup):
+        oracle_step_seconds(args, sample_rows=32, sample_outputs=4)
+    times = []
+    for _ in range(args.steps):
+        s, threads, desc = oracle_step_seconds(args, sample_rows=32, sample_outputs=8)
+        times.append(s)
+    secs = statistics.mean(times)
+    value = 100.0 * ideal / secs
+    out = {"impl": "reference",
+           "metric": "quantize GB/s and FP4 block-scaled GEMM TFLOP/s, each as % of GB300 roofline",
+           "value": value, "unit": "% of one GB300 roofline", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "e2m1 payload x exact accumulate (u8 codes)", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "format": FMT_NAMES[args.format],
+                      "X": [M_TOK, K_FF], "W": [N_MODEL, K_FF], "dY": [M_TOK, N_MODEL]},
+           "cpu_baseline": {"value": value, "unit": "% of one GB300 roofline", "kind": "oracle",
+                            "cores": threads, "sample": desc},
+           "e2e": {"value": value, "unit": "% of one GB300 roofline", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--format", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,2 +1,226 @@
-"""GB300-native FP4 block-scaled quantize-and-multiply (placeholder; the
-binding to the CUDA library is added with the library)."""
+"""GB300-native FP4 block-scaled quantize-and-multiply.
+
+Thin ctypes binding of ``libfp4gb300.so`` (C ABI declared in include/fp4.h).
+Functions keep the C names and only marshal arguments: torch tensors supply
+device memory, ``torch.cuda.current_stream()`` the stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU fallback --
+importing this package raises if the library has not been built.
+
+Convenience allocators (``quantize``, ``quantize_transpose``, ``amax``,
+``gemm``) create the output tensors with torch and call the entry points.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import inputs  # noqa: F401  (seeded workload generators)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libfp4gb300.so")
+
+FP4_FMT_UE5M3_B16, FP4_FMT_NVFP4_B16, FP4_FMT_MXFP4_B32 = 0, 1, 2
+FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
+FP4_SF_PLAIN, FP4_SF_MMA = 0, 1
+FP4_OK = 0
+STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_ALIGNMENT", 3: "FP4_ERR_SHAPE",
+                4: "FP4_ERR_UNSUPPORTED", 5: "FP4_ERR_CUDA", 6: "FP4_ERR_TIMEOUT",
+                7: "FP4_ERR_NONFINITE", 8: "FP4_ERR_SCALE_WINDOW"}
+
+
+class fp4_quant_params(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("T", ctypes.c_float), ("block2d", ctypes.c_int32),
+                ("round_row", ctypes.c_int32), ("round_col", ctypes.c_int32),
+                ("sr_seed", ctypes.c_uint64), ("sr_offset", ctypes.c_uint32),
+                ("hadamard_n", ctypes.c_int32), ("hadamard_signs", ctypes.c_uint32),
+                ("sf_layout", ctypes.c_int32)]
+
+
+class fp4_operand(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("s_dec", ctypes.c_void_p),
+                ("row_shift", ctypes.c_void_p), ("format", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+class FP4Error(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+EXPORTS = ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_sf_bytes",
+           "fp4_block_size", "fp4_status_sync", "fp4_status_string")
+
+
+def lib():
+    """Load the CUDA library (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+        qp = ctypes.POINTER(fp4_quant_params)
+        op = ctypes.POINTER(fp4_operand)
+        L.fp4_amax.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp]
+        L.fp4_quantize.argtypes = [vp, i64, i64, vp, qp, vp, vp, vp, vp, vp]
+        L.fp4_quantize_transpose.argtypes = [vp, i64, i64, vp, vp, qp, vp, vp, vp, vp, vp, vp, vp,
+                                             vp, vp]
+        L.fp4_gemm.argtypes = [op, op, i64, i64, i64, vp, i32, i32, vp]
+        L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
+        L.fp4_sf_bytes.restype = i64
+        L.fp4_block_size.argtypes = [i32]
+        L.fp4_block_size.restype = i32
+        L.fp4_status_sync.argtypes = [vp]
+        L.fp4_status_string.argtypes = [i32]
+        L.fp4_status_string.restype = ctypes.c_char_p
+        for f in ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
+                  "fp4_status_sync"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code, where):
+    if code != FP4_OK:
+        raise FP4Error(code, where)
+    return code
+
+
+def params(format=FP4_FMT_UE5M3_B16, T=448.0, block2d=False, round_row=FP4_ROUND_RNE,
+           round_col=FP4_ROUND_RNE, sr_seed=0, sr_offset=0, hadamard_n=0, hadamard_signs=0,
+           sf_layout=FP4_SF_PLAIN):
+    return fp4_quant_params(int(format), float(T), int(bool(block2d)), int(round_row),
+                            int(round_col), int(sr_seed), int(sr_offset), int(hadamard_n),
+                            int(hadamard_signs), int(sf_layout))
+
+
+# ------------------------------------------------------------- raw entry points
+
+def fp4_amax(x, hadamard_n, hadamard_signs, amax_row, amax_col=None, stream=None):
+    rows, cols = x.shape
+    return lib().fp4_amax(_ptr(x), rows, cols, hadamard_n, hadamard_signs, _ptr(amax_row),
+                          _ptr(amax_col), _stream(stream))
+
+
+def fp4_quantize(x, amax, p, q, sf, s_dec, row_shift=None, stream=None):
+    rows, cols = x.shape
+    return lib().fp4_quantize(_ptr(x), rows, cols, _ptr(amax), ctypes.byref(p), _ptr(q), _ptr(sf),
+                              _ptr(s_dec), _ptr(row_shift), _stream(stream))
+
+
+def fp4_quantize_transpose(x, amax_row, amax_col, p, q_row, sf_row, s_dec_row, shift_row, q_col,
+                           sf_col, s_dec_col, shift_col, stream=None):
+    rows, cols = x.shape
+    return lib().fp4_quantize_transpose(
+        _ptr(x), rows, cols, _ptr(amax_row), _ptr(amax_col), ctypes.byref(p), _ptr(q_row),
+        _ptr(sf_row), _ptr(s_dec_row), _ptr(shift_row), _ptr(q_col), _ptr(sf_col),
+        _ptr(s_dec_col), _ptr(shift_col), _stream(stream))
+
+
+def fp4_gemm(A, B, M, N, K, D, d_is_bf16, canonicalize_1024=0, stream=None):
+    return lib().fp4_gemm(ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(D), int(d_is_bf16),
+                          int(canonicalize_1024), _stream(stream))
+
+
+def fp4_sf_bytes(format, rows, cols, layout):
+    return lib().fp4_sf_bytes(format, rows, cols, layout)
+
+
+def fp4_block_size(format):
+    return lib().fp4_block_size(format)
+
+
+def fp4_status_sync(stream=None):
+    return lib().fp4_status_sync(_stream(stream))
+
+
+def fp4_status_string(code):
+    return lib().fp4_status_string(code).decode()
+
+
+# ------------------------------------------------------ allocating conveniences
+
+class Quantized:
+    """One quantised copy held in torch tensors: payload q [rows, k/2] uint8,
+    scales sf (layout per `sf_layout`), s_dec (1-element float32) and, for a
+    UE5M3 copy in the tensor-core layout, row_shift [rows] int8."""
+
+    def __init__(self, q, sf, s_dec, row_shift, format, sf_layout):
+        self.q, self.sf, self.s_dec, self.row_shift = q, sf, s_dec, row_shift
+        self.format, self.sf_layout = format, sf_layout
+
+    @property
+    def rows(self):
+        return self.q.shape[0]
+
+    @property
+    def k(self):
+        return self.q.shape[1] * 2
+
+    def operand(self):
+        return fp4_operand(self.q.data_ptr(), self.sf.data_ptr(), self.s_dec.data_ptr(),
+                           self.row_shift.data_ptr() if self.row_shift is not None else None,
+                           self.format, self.rows, self.k)
+
+
+def _alloc_copy(rows, cols, p, device, with_shift):
+    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    nsf = fp4_sf_bytes(p.format, rows, cols, p.sf_layout)
+    sf = torch.empty(max(nsf, 16), dtype=torch.uint8, device=device)
+    s_dec = torch.empty(1, dtype=torch.float32, device=device)
+    shift = None
+    if with_shift:
+        shift = torch.empty(max(rows, 1), dtype=torch.int8, device=device)
+    return Quantized(q, sf[:nsf] if nsf else sf[:0], s_dec, shift, p.format, p.sf_layout)
+
+
+def _want_shift(p, remap):
+    return bool(remap) and p.format == FP4_FMT_UE5M3_B16 and p.sf_layout == FP4_SF_MMA
+
+
+def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
+    """(amax_row, amax_col) device float32 tensors of shape [1]."""
+    a = torch.empty(1, dtype=torch.float32, device=x.device)
+    b = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(fp4_amax(x, hadamard_n, hadamard_signs, a, b, stream), "fp4_amax")
+    return a, b
+
+
+def quantize(x, amax_dev, p, remap=True, stream=None):
+    rows, cols = x.shape
+    out = _alloc_copy(rows, cols, p, x.device, _want_shift(p, remap))
+    _check(fp4_quantize(x, amax_dev, p, out.q, out.sf, out.s_dec, out.row_shift, stream),
+           "fp4_quantize")
+    return out
+
+
+def quantize_transpose(x, amax_row, amax_col, p, remap=True, stream=None):
+    rows, cols = x.shape
+    ws = _want_shift(p, remap)
+    r = _alloc_copy(rows, cols, p, x.device, ws)
+    c = _alloc_copy(cols, rows, p, x.device, ws)
+    _check(fp4_quantize_transpose(x, amax_row, amax_col, p, r.q, r.sf, r.s_dec, r.row_shift,
+                                  c.q, c.sf, c.s_dec, c.row_shift, stream),
+           "fp4_quantize_transpose")
+    return r, c
+
+
+def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, stream=None):
+    """D = alpha * A B^T for two Quantized operands in the tensor-core layout."""
+    M, N, K = a.rows, b.rows, a.k
+    D = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.q.device)
+    _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
+                    canonicalize_1024, stream), "fp4_gemm")
+    return D

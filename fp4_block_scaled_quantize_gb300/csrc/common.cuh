@@ -1,0 +1,76 @@
+// common.cuh -- shared device/host plumbing of the FP4 library (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp4.h"
+
+namespace fp4 {
+
+// Bits of the per-device status word (reported by fp4_status_sync).
+enum : uint32_t {
+  kStatusTimeout = 1u << 0,
+  kStatusNonfinite = 1u << 1,
+  kStatusScaleWindow = 1u << 2,
+};
+
+// Device address of the status word on the current device (set up on first
+// use per device; nullptr if the CUDA runtime failed).
+uint32_t *status_word();
+
+__device__ __forceinline__ void raise_status(uint32_t *status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline int block_of(int32_t fmt) {
+  return fmt == FP4_FMT_MXFP4_B32 ? 32 : (fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_NVFP4_B16 ? 16 : -1);
+}
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Enqueue-only entry points launched by abi.cu.
+fp4_status launch_amax(const void *x, int64_t rows, int64_t cols, int had_n, uint32_t signs,
+                       float *amax_row, float *amax_col, cudaStream_t s);
+
+struct QuantJob {
+  const uint16_t *x;
+  int64_t R, C;
+  const float *amax_row, *amax_col;
+  float T;
+  int fmt, block2d, had_n;
+  uint32_t signs;
+  int sr_row, sr_col;
+  uint64_t seed;
+  uint32_t offset;
+  int sf_mma;
+  uint8_t *q_row, *sf_row;
+  float *s_dec_row;
+  int8_t *shift_row;
+  uint8_t *q_col, *sf_col;
+  float *s_dec_col;
+  int8_t *shift_col;
+};
+fp4_status launch_quantize(const QuantJob &j, cudaStream_t s);
+
+// UE5M3 -> E4M3 image of an MMA-layout scale buffer, in place, plus shifts.
+fp4_status launch_remap_ue5m3(uint8_t *sf_mma, const uint8_t *q, int64_t rows, int64_t cols,
+                              int8_t *shift, cudaStream_t s);
+
+struct GemmJob {
+  const uint8_t *qa, *sfa, *qb, *sfb;
+  const float *sda, *sdb;
+  const int8_t *sha, *shb;
+  int fmt;
+  int64_t M, N, K;
+  void *D;
+  int d_bf16, canon;
+};
+fp4_status launch_gemm(const GemmJob &j, cudaStream_t s);
+
+}  // namespace fp4

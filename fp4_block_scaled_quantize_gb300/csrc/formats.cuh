@@ -1,0 +1,210 @@
+// formats.cuh -- device encoders/decoders of the FP4 number formats.
+//
+// E2M1 payload, UE5M3 / E4M3 / E8M0 block scales ("UE5M3 FP4 Block Scaling
+// for Stable Language Model Pretraining", Approach: E2M1 payload with a
+// UE5M3 block scale whose largest value is 61,440; "Practical FP4 Training
+// for Large-Scale MoE Models on Hopper GPUs", Method: MXFP4 = E2M1 with a
+// power-of-two scale per 32 values).  Every function is exact or a single
+// IEEE binary32 rounding; none depends on FMA contraction or flush-to-zero.
+#pragma once
+#include <stdint.h>
+
+namespace fp4 {
+
+enum { kUE5M3 = 0, kNVFP4 = 1, kMXFP4 = 2 };
+
+template <int FMT>
+struct Fmt {
+  static constexpr int B = (FMT == kMXFP4) ? 32 : 16;
+};
+
+// ---------------------------------------------------------------- BF16
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------- E2M1
+// Nearest-even onto {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating: the code is the
+// number of rounding thresholds |v| passes; a threshold at a midpoint is
+// passed with ">" when the lower neighbour has the even code and with ">="
+// when the upper one has.  Sign bit copied from v (so -0 gives 8).
+__device__ __forceinline__ uint32_t e2m1_rne(float v) {
+  float a = fabsf(v);
+  uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+               (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+               (uint32_t)(a > 5.0f);
+  return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Hardware conversion of two values (hi -> upper nibble).  Used only where
+// the self-check kernel has shown it equal to e2m1_rne on every input class.
+__device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Stochastic rounding with 16 random bits r16: between the neighbouring
+// codebook values lo <= |v| < hi, round up iff r16 < 65536 (|v|-lo)/(hi-lo).
+// For |v| in [1, 6) the value sits in a binade with one kept mantissa bit,
+// so (|v|-lo)/(hi-lo) is the dropped 22-bit mantissa tail over 2^22 and the
+// test is the integer comparison r16 * 64 < tail.  Below 1 the codebook step
+// is 0.5: t = 2|v|, and the fraction is t - floor(t), exact.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
+  float a = fabsf(v);
+  uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
+  uint32_t code;
+  if (a >= 6.0f) {
+    code = 7u;
+  } else if (a >= 1.0f) {
+    uint32_t u = __float_as_uint(a);
+    uint32_t e = (u >> 23) - 127u;  // 0, 1 or 2
+    code = 2u + 2u * e + ((u >> 22) & 1u) + (uint32_t)((r16 << 6) < (u & 0x3FFFFFu));
+  } else {
+    float t = __fmul_rn(a, 2.0f);
+    float c = (t >= 1.0f) ? 1.0f : 0.0f;
+    float f = __fmul_rn(__fsub_rn(t, c), 65536.0f);
+    code = (uint32_t)c + (uint32_t)(__uint2float_rn(r16) < f);
+  }
+  return code | sign;
+}
+
+// --------------------------------------------------------------- UE5M3
+// Unsigned E5M3, bias 15, exponent 31 reserved: normal (8+m) 2^(e-18),
+// subnormal m 2^-17, largest 0xF7 = 61,440.
+__device__ __forceinline__ float ue5m3_dec(uint32_t code) {
+  uint32_t e = code >> 3, m = code & 7u;
+  if (e == 0) return __fmul_rn(__uint2float_rn(m), 0x1p-17f);
+  return __uint_as_float(((e + 112u) << 23) | (m << 20));
+}
+
+// Nearest-even, saturating at 0xF7; f >= 0.
+__device__ __forceinline__ uint32_t ue5m3_rne_sat(float f) {
+  if (!(f >= 0x1p-14f)) {
+    // subnormal range: f * 2^17 is exact; its nearest-even integer (0..8) is
+    // the code, 8 being the smallest normal 2^-14.
+    return __float2uint_rn(__fmul_rn(f, 131072.0f));
+  }
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFFu + ((u >> 20) & 1u);  // round the mantissa to 3 bits, ties even
+  int e = (int)(u >> 23) - 127;
+  if (e > 15) return 0xF7u;
+  uint32_t code = ((uint32_t)(e + 15) << 3) | ((u >> 20) & 7u);
+  return code > 0xF7u ? 0xF7u : code;
+}
+
+// ---------------------------------------------------------------- E4M3
+// E4M3 "FN": bias 7, 0x7F NaN, largest 0x7E = 448, subnormal m 2^-9.
+__device__ __forceinline__ float e4m3_dec(uint32_t code) {
+  uint32_t e = (code >> 3) & 15u, m = code & 7u;
+  if (e == 0) return __fmul_rn(__uint2float_rn(m), 0x1p-9f);
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+__device__ __forceinline__ uint32_t e4m3_rne_sat(float f) {
+  if (!(f >= 0x1p-6f)) return __float2uint_rn(__fmul_rn(f, 512.0f));
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFFu + ((u >> 20) & 1u);
+  int e = (int)(u >> 23) - 127;
+  if (e > 8) return 0x7Eu;
+  uint32_t code = ((uint32_t)(e + 7) << 3) | ((u >> 20) & 7u);
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// ---------------------------------------------------------------- E8M0
+// MX shared exponent E = floor(log2 b) - 2 (2 = largest E2M1 exponent),
+// clamped to [-127, 127]; b == 0 gives 0.
+__device__ __forceinline__ int mx_exponent(float b) {
+  if (b == 0.0f) return 0;
+  uint32_t u = __float_as_uint(b);
+  int ex = (int)(u >> 23);
+  int fl = ex ? ex - 127 : (31 - __clz(u & 0x7FFFFFu)) - 149;
+  int E = fl - 2;
+  return E < -127 ? -127 : (E > 127 ? 127 : E);
+}
+
+// 2^-E as binary32, E in [-127, 125].
+__device__ __forceinline__ float pow2_neg(int E) { return __uint_as_float((uint32_t)(127 - E) << 23); }
+
+// ----------------------------------------------------- block scale rule
+// Block scale code and element multiplier for a block whose max |x| is b:
+//  UE5M3/NVFP4: code = enc(RN32(RN32(b/6) * s_enc)), 0 -> code of 1.0,
+//               mult = RN32(1 / RN32(dec(code) * s_dec)); zero payload if
+//               that product is 0;
+//  MXFP4:       code = E + 127, mult = 2^-E.
+template <int FMT>
+__device__ __forceinline__ uint32_t block_scale(float b, float s_enc, float s_dec, float &mult,
+                                                bool &zero_payload) {
+  if (FMT == kMXFP4) {
+    int E = mx_exponent(b);
+    mult = pow2_neg(E);
+    zero_payload = false;
+    return (uint32_t)(E + 127);
+  } else {
+    float raw = __fmul_rn(__fdiv_rn(b, 6.0f), s_enc);
+    uint32_t code = (FMT == kUE5M3) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
+    if (code == 0) code = (FMT == kUE5M3) ? 0x78u : 0x38u;
+    float dec = (FMT == kUE5M3) ? ue5m3_dec(code) : e4m3_dec(code);
+    float sd = __fmul_rn(dec, s_dec);
+    zero_payload = (sd == 0.0f);
+    mult = __fdiv_rn(1.0f, sd);
+    return code;
+  }
+}
+
+// Per-tensor scale: s_enc = RN32(RN32(6 T) / amax) (1 for amax 0 or
+// non-finite, FLT_MAX on overflow), s_dec = RN32(1 / s_enc); MX: 1, 1.
+template <int FMT>
+__device__ __forceinline__ void tensor_scale(float amax, float T, float &s_enc, float &s_dec) {
+  if (FMT == kMXFP4) {
+    s_enc = 1.0f;
+    s_dec = 1.0f;
+    return;
+  }
+  float e;
+  if (!(amax > 0.0f) || isinf(amax)) {
+    e = 1.0f;
+  } else {
+    e = __fdiv_rn(__fmul_rn(6.0f, T), amax);
+    if (isinf(e)) e = 3.402823466e38f;
+  }
+  s_enc = e;
+  s_dec = __fdiv_rn(1.0f, e);
+}
+
+// v = x * mult, with 0 * inf read as 0 (keeps the sign of x).
+__device__ __forceinline__ float scale_elem(float x, float mult) {
+  return (x == 0.0f) ? x : __fmul_rn(x, mult);
+}
+
+// --------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies and xors with the key, the key advanced by the Weyl
+// constants after every round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Random bits for the 8-element group g of copy `copy`: element j of the
+// group uses bits [16 (j&1), +16) of word j>>1.
+__device__ __forceinline__ uint4 sr_group_bits(uint64_t seed, uint32_t offset, uint32_t copy,
+                                               uint64_t g) {
+  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), copy, offset), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t sr_r16(const uint4 &w, int j) {
+  uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+  return (word >> (16 * (j & 1))) & 0xFFFFu;
+}
+
+}  // namespace fp4

@@ -1,0 +1,497 @@
+// gemm.cu -- block-scaled FP4 GEMM on the sm_103a tensor cores (tcgen05).
+//
+// D[M][N] = alpha * sum_k A[m][k] B[n][k], A and B K-major E2M1 payloads with
+// one scale per 16 (E4M3) or 32 (E8M0) elements ("UE5M3 FP4 Block Scaling for
+// Stable Language Model Pretraining", Approach: fprop Y = X W^T, dgrad
+// dX = dY W, wgrad dW = dY^T X, all "TN" once the producers supply the
+// transposed copies).  UE5M3 operands arrive remapped onto E4M3 scales with a
+// per-row power-of-two shift (Limitations: UE5M3 is not native); the
+// epilogue multiplies by 2^(shift_a[m] + shift_b[n]).  The tensor core adds
+// K in steps of one 64-element MMA into a binary32 accumulator in tensor
+// memory, the grouping the page's probe-matched model describes.
+//
+// Kernel (one persistent CTA per SM, 192 threads):
+//   warp 0  TMA producer: per 256-element K step, A [128 x 128 B] and
+//           B [256 x 128 B] payload tiles (128-byte swizzle) by tensor TMA,
+//           plus the matching 512-byte scale tiles by bulk copy;
+//   warp 1  MMA issuer: tcgen05.cp of the scale tiles into tensor memory,
+//           four tcgen05.mma.kind::mxf4nvf4 (M128 N256 K64) per stage,
+//           tcgen05.commit to release the stage / publish the accumulator;
+//   warps 2-5 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator,
+//           shift / canonicalise / alpha, BF16 or binary32 stores.
+// Every mbarrier wait is bounded (about one second): on expiry the CTA
+// raises the timeout status bit, drains its own copies and MMAs (again
+// bounded), frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "formats.cuh"
+
+namespace fp4 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256;
+constexpr int BK_BYTES = 128;  // 256 FP4 elements per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK_BYTES;          // 16 KB
+constexpr int B_BYTES = BN * BK_BYTES;          // 32 KB
+constexpr int SFA_BYTES = 4 * 512;              // up to 4 scale tiles (block 16)
+constexpr int SFB_BYTES = 2 * 4 * 512;          // two 128-row groups
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 54 KB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;    // 256 binary32 columns
+constexpr uint32_t SFA_COL = 256;  // 4 k-steps x 4 columns
+constexpr uint32_t SFB_COL = 272;  // 4 k-steps x 8 columns
+constexpr unsigned long long kTimeoutNs = 1000000000ull;
+
+struct Params {
+  const uint8_t *sfa, *sfb;
+  const float *sda, *sdb;
+  const int8_t *sha, *shb;
+  void *D;
+  int64_t M, N, K;
+  int m_tiles, n_tiles, k_tiles, k_steps;
+  int64_t cp4;     // scale tiles per 128-row group (both operands)
+  int64_t ngrp_b;  // 128-row groups of B
+  int d_bf16, canon;
+  uint32_t *status;
+};
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the CTA is aborting or the wait ran out (which then
+// starts the abort and raises the timeout status bit).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       uint32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        raise_status(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait used while draining after an abort (no abort check).
+__device__ __noinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kTimeoutNs / 4) return;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+template <int FMT>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  if (FMT == kMXFP4) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  }
+}
+__device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
+      "15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major, 128-byte
+// swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Descriptor of one 512-byte scale tile: 32 rows of 16 bytes, no swizzle.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) |
+         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, K-major A and B,
+// M = 128, N = 256; scale type E4M3 (block 16) or E8M0 (block 32).
+template <int FMT>
+__device__ __forceinline__ uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
+  uint32_t d = 0;
+  d |= (b_sf_id & 3u) << 4;
+  d |= 1u << 7;   // A: E2M1
+  d |= 1u << 10;  // B: E2M1
+  d |= (uint32_t)(BN >> 3) << 17;
+  d |= (FMT == kMXFP4 ? 1u : 0u) << 23;
+  d |= (uint32_t)(BM >> 4) << 24;
+  d |= (a_sf_id & 3u) << 29;
+  return d;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+           const Params p) {
+  constexpr int APK = (FMT == kMXFP4) ? 2 : 4;  // scale tiles per stage per 128 rows
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, drain
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * STAGES + 3);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
+  const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------- TMA producer
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tma_b)) : "memory");
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t *st = smem + stage * STAGE_BYTES;
+        const int64_t atoms = min((int64_t)APK, p.cp4 - (int64_t)kt * APK);
+        uint32_t bytes = A_BYTES + B_BYTES + (uint32_t)atoms * 512u;
+        const bool g1 = (2 * (int64_t)nt + 1) < p.ngrp_b;
+        if (g1) bytes += (uint32_t)atoms * 512u;
+        bytes += (uint32_t)atoms * 512u;  // group 0 of B always exists
+        const uint32_t fb = full_bar(stage);
+        mbar_expect_tx(fb, bytes);
+        tma_load_2d(smem_u32(st), &tma_a, fb, kt * BK_BYTES, mt * BM);
+        tma_load_2d(smem_u32(st + A_BYTES), &tma_b, fb, kt * BK_BYTES, nt * BN);
+        const uint8_t *sfa = p.sfa + ((int64_t)mt * p.cp4 + (int64_t)kt * APK) * 512;
+        bulk_load(smem_u32(st + A_BYTES + B_BYTES), sfa, (uint32_t)atoms * 512u, fb);
+        const uint8_t *sfb0 = p.sfb + ((2 * (int64_t)nt) * p.cp4 + (int64_t)kt * APK) * 512;
+        bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES), sfb0, (uint32_t)atoms * 512u, fb);
+        if (g1) {
+          const uint8_t *sfb1 = p.sfb + ((2 * (int64_t)nt + 1) * p.cp4 + (int64_t)kt * APK) * 512;
+          bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES + 4 * 512), sfb1,
+                    (uint32_t)atoms * 512u, fb);
+        }
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // make sure no copy into this CTA's shared memory is still in flight
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (issued_parity >> s) & 1u);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, any = false;
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+      tc_fence_after();
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t sfa_s = st + A_BYTES + B_BYTES, sfb_s = sfa_s + SFA_BYTES;
+        const int nks = min(4, p.k_steps - 4 * kt);
+        const int natoms = (FMT == kMXFP4) ? (nks + 1) / 2 : nks;
+        for (int a = 0; a < natoms; ++a) {
+          tc_cp_sf(tmem + SFA_COL + 4 * a, desc_sf(sfa_s + 512 * a));
+          tc_cp_sf(tmem + SFB_COL + 8 * a, desc_sf(sfb_s + 512 * a));
+          tc_cp_sf(tmem + SFB_COL + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
+        }
+        const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
+        for (int kk = 0; kk < nks; ++kk) {
+          const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
+          const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
+          tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id),
+                      tmem + SFA_COL + 4 * a, tmem + SFB_COL + 8 * a, (kt | kk) != 0);
+          any = true;
+        }
+        tc_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(acc_full);
+      acc_phase ^= 1u;
+    }
+    if (any) {  // all of this thread's tcgen05 operations have completed
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else if (warp >= 2) {
+    // --------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // tensor-memory lane quadrant this warp may read
+    const int row_in_tile = quad * 32 + lane;
+    const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)mt * BM + row_in_tile;
+      const int sa = p.sha && m < p.M ? (int)__ldg(p.sha + m) : 0;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tc_ld_32cols(tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + c0, r);
+        const int64_t n0 = (int64_t)nt * BN + c0;
+        if (m >= p.M || n0 >= p.N) continue;
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float v = __uint_as_float(r[j]);
+          if (p.shb) {
+            const int64_t n = n0 + j < p.N ? n0 + j : p.N - 1;
+            const int s = sa + (int)__ldg(p.shb + n);
+            v = __fmul_rn(v, __uint_as_float((uint32_t)(127 + s) << 23));
+          }
+          if (p.canon) v = __fmul_rn(rintf(__fmul_rn(v, 1024.0f)), 0x1p-10f);
+          y[j] = __fmul_rn(v, alpha);
+        }
+        if (p.d_bf16) {
+          __nv_bfloat16 *drow = reinterpret_cast<__nv_bfloat16 *>(p.D) + m * p.N + n0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            if (n0 + j >= p.N) break;
+            uint4 w;
+            w.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 1])) << 16);
+            w.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 2])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 3])) << 16);
+            w.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 4])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 5])) << 16);
+            w.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 6])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 7])) << 16);
+            *reinterpret_cast<uint4 *>(drow + j) = w;
+          }
+        } else {
+          float *drow = reinterpret_cast<float *>(p.D) + m * p.N + n0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            if (n0 + j >= p.N) break;
+            *reinterpret_cast<float4 *>(drow + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS));
+  }
+}
+
+// ------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int FMT>
+fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int grid,
+                      cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_gemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
+  k_gemm<FMT><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+}  // namespace
+
+fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
+  const size_t elt = j.d_bf16 ? 2 : 4;
+  if (j.K == 0) {
+    return cudaMemsetAsync(j.D, 0, (size_t)j.M * j.N * elt, s) == cudaSuccess ? FP4_OK
+                                                                             : FP4_ERR_CUDA;
+  }
+  uint32_t *status = status_word();
+  if (!status) return FP4_ERR_CUDA;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, j.qa, j.M, j.K / 2, BM) || !make_map(&mb, j.qb, j.N, j.K / 2, BN))
+    return FP4_ERR_CUDA;
+  Params p{};
+  p.sfa = j.sfa;
+  p.sfb = j.sfb;
+  p.sda = j.sda;
+  p.sdb = j.sdb;
+  p.sha = j.sha;
+  p.shb = j.shb;
+  p.D = j.D;
+  p.M = j.M;
+  p.N = j.N;
+  p.K = j.K;
+  p.m_tiles = (int)ceil_div(j.M, BM);
+  p.n_tiles = (int)ceil_div(j.N, BN);
+  p.k_steps = (int)(j.K / 64);
+  p.k_tiles = (int)ceil_div(j.K, 256);
+  const int blk = (j.fmt == kMXFP4) ? 32 : 16;
+  p.cp4 = ceil_div(j.K / blk, 4);
+  p.ngrp_b = ceil_div(j.N, 128);
+  p.d_bf16 = j.d_bf16;
+  p.canon = j.canon;
+  p.status = status;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  if (j.fmt == kMXFP4) return launch_fmt<kMXFP4>(ma, mb, p, grid, s);
+  return launch_fmt<kNVFP4>(ma, mb, p, grid, s);
+}
+
+}  // namespace fp4

@@ -1,0 +1,434 @@
+// quantize.cu -- FP4 block-scaled quantization producers (sm_103a).
+//
+// "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining", Approach:
+// BF16 -> E2M1 payload with one scale per 16 contiguous elements, per-tensor
+// scale from the held amax and the target T, nearest-even (stochastic on dY
+// only), zero-scale rule, 2D 16x16 weight tiles.  "Format-Aware Fusion for
+// Fast FP4 Pretraining", Abstract: the producer builds the consumer's layout
+// (row-wise and transposed copies, tensor-core scale tiles) in the same pass.
+// "Technical summary: LLM pretraining with MXFP4", Findings: deterministic
+// H16 / H32 rotation on the weight-gradient (transposed) copy.
+//
+// Design (one CTA of 256 threads per 128 x 128 BF16 tile, HBM-bound):
+//  * loads: 16 B per lane; warp w owns tile rows 16w..16w+15, two rows per
+//    load instruction (16 lanes x 16 B = one 256 B row), so each lane holds
+//    one half of a 16-element row block -- the row-wise copy is computed
+//    straight from registers (block max = one shuffle).
+//  * the transposed copy reads the tile back from shared memory column-wise:
+//    each lane owns 64 values (4 columns x 16 rows, or 2 x 32 with a 32-row
+//    rotation / block); 8-byte row-contiguous reads are conflict-free.
+//  * transposed payload bytes are staged in shared memory so every column
+//    segment leaves as contiguous 8-byte stores; scales leave as whole
+//    512-byte tensor-core tiles (or plain rows).
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "formats.cuh"
+
+#ifndef FP4_HW_E2M1
+#define FP4_HW_E2M1 0
+#endif
+
+namespace fp4 {
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 256;
+
+struct Params {
+  const uint16_t *x;
+  int64_t R, C;
+  int64_t tiles_c;
+  const float *amax_row, *amax_col;
+  float T;
+  uint8_t *q_row, *sf_row;
+  float *s_dec_row;
+  uint8_t *q_col, *sf_col;
+  float *s_dec_col;
+  int do_row, do_col, sr_row, sr_col, sf_mma;
+  uint64_t seed;
+  uint32_t offset, signs;
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Encode 8 values (already multiplied by the block multiplier) to 8 nibbles,
+// element j in bits [4j, 4j+4).
+__device__ __forceinline__ uint32_t encode8_rne(const float *v) {
+#if FP4_HW_E2M1
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) w |= e2m1x2_hw(v[j + 1], v[j]) << (4 * j);
+  return w;
+#else
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w |= e2m1_rne(v[j]) << (4 * j);
+  return w;
+#endif
+}
+
+__device__ __forceinline__ uint32_t encode8_sr(const float *v, const uint4 &bits) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w |= e2m1_sr(v[j], sr_r16(bits, j)) << (4 * j);
+  return w;
+}
+
+// Scale a block of 8 values by mult (0 * inf read as 0; zero payload -> 0).
+__device__ __forceinline__ void scale8(float *v, float mult, bool zero_payload) {
+  if (zero_payload) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+  } else if (isinf(mult)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = scale_elem(v[j], mult);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], mult);
+  }
+}
+
+// Write one copy's scales for this tile.  sfs[r][j] holds the codes of tile
+// row r (copy rows r0 + r) and scale columns c0b + j; `rows_valid` and
+// `cols_valid` bound the real part (the rest is padding, written as 0 in the
+// tensor-core layout and not written in the plain layout).
+template <int NSC>
+__device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *sf, int64_t copy_rows,
+                                             int64_t copy_cb, int64_t r0, int64_t c0b, int sf_mma) {
+  const int t = threadIdx.x;
+  const int64_t rows_valid = copy_rows - r0;
+  const int64_t cols_valid = copy_cb - c0b;
+  if (sf_mma) {
+    // NSC / 4 tiles of 128 x 4 codes; 32-bit word i of a tile holds the 4
+    // codes of row (i / 4) + 32 (i % 4).
+    const int64_t cp4 = (copy_cb + 3) / 4;  // tiles per tile-row
+    for (int idx = t; idx < 128 * (NSC / 4); idx += kThreads) {
+      int atom = idx / 128, i = idx % 128;
+      int64_t atom_col = c0b / 4 + atom;
+      if (atom_col >= cp4) continue;
+      int r = (i >> 2) + 32 * (i & 3);
+      uint32_t w = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        int j = atom * 4 + c;
+        uint32_t code = (r < rows_valid && j < cols_valid) ? sfs[r][j] : 0u;
+        w |= code << (8 * c);
+      }
+      int64_t base = ((r0 / 128) * cp4 + atom_col) * 512;
+      reinterpret_cast<uint32_t *>(sf + base)[i] = w;
+    }
+  } else {
+    for (int idx = t; idx < 128 * NSC; idx += kThreads) {
+      int r = idx / NSC, j = idx % NSC;
+      if (r < rows_valid && j < cols_valid) sf[(r0 + r) * copy_cb + c0b + j] = sfs[r][j];
+    }
+  }
+}
+
+template <int FMT, int HAD, bool TWO_D>
+__global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
+  constexpr int B = Fmt<FMT>::B;
+  constexpr int NSC = kTile / B;                    // scale columns per tile
+  constexpr int RU = (HAD > B) ? HAD : B;           // rows per column unit
+  constexpr int CPL = 64 / RU;                      // columns per lane
+  constexpr int NCG = RU / 16;                      // column groups per tile
+  constexpr int LANES_PER_BLOCK = B / 8;            // lanes per row block
+
+  __shared__ __align__(16) uint16_t xs[kTile][kTile];  // 32 KB BF16 tile
+  __shared__ __align__(16) uint8_t colq[kTile][kTile / 2];
+  __shared__ __align__(16) uint8_t sfr[kTile][8];
+  __shared__ __align__(16) uint8_t sfc[kTile][8];
+  __shared__ float tmax[8][8];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tr = blockIdx.x / p.tiles_c, tc = blockIdx.x % p.tiles_c;
+  const int64_t R0 = tr * kTile, C0 = tc * kTile;
+  const int64_t R = p.R, C = p.C;
+  const bool need_smem = p.do_col || TWO_D;
+
+  float se_r, sd_r, se_c = 1.0f, sd_c = 1.0f;
+  tensor_scale<FMT>(__ldg(p.amax_row), p.T, se_r, sd_r);
+  if (p.do_col && !TWO_D) tensor_scale<FMT>(__ldg(p.amax_col), p.T, se_c, sd_c);
+  if (TWO_D) {
+    se_c = se_r;
+    sd_c = sd_r;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (p.do_row) *p.s_dec_row = sd_r;
+    if (p.do_col) *p.s_dec_col = sd_c;
+  }
+
+  // ---- load: lane holds 8 BF16 of row 16w + 2i + (lane >> 4)
+  const int chunk = lane & 15;
+  const int64_t gc = C0 + 8 * chunk;
+  uint4 raw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    int r = 16 * warp + 2 * i + (lane >> 4);
+    int64_t gr = R0 + r;
+    if (gr < R && gc < C)
+      raw[i] = ldg_stream(p.x + gr * C + gc);
+    else
+      raw[i] = make_uint4(0, 0, 0, 0);
+    if (need_smem) *reinterpret_cast<uint4 *>(&xs[r][8 * chunk]) = raw[i];
+  }
+
+  // ---- row-wise copy (1 x B blocks along C) from registers
+  auto row_pass = [&](int i, const uint4 &w) {
+    int r = 16 * warp + 2 * i + (lane >> 4);
+    int64_t gr = R0 + r;
+    float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    float b;
+    if (TWO_D) {
+      b = tmax[r / B][chunk / LANES_PER_BLOCK];
+    } else {
+      b = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(v[j]));
+#pragma unroll
+      for (int o = 1; o < LANES_PER_BLOCK; o <<= 1)
+        b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
+    }
+    float mult;
+    bool zp;
+    uint32_t code = block_scale<FMT>(b, se_r, sd_r, mult, zp);
+    scale8(v, mult, zp);
+    uint32_t word;
+    if (p.sr_row) {
+      uint64_t g = ((uint64_t)gr * (uint64_t)C + (uint64_t)gc) >> 3;
+      word = encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u, g));
+    } else {
+      word = encode8_rne(v);
+    }
+    if (gr < R && gc < C) {
+      *reinterpret_cast<uint32_t *>(p.q_row + gr * (C / 2) + gc / 2) = word;
+    }
+    if ((chunk % LANES_PER_BLOCK) == 0) sfr[r][chunk / LANES_PER_BLOCK] = (uint8_t)code;
+  };
+
+  if (p.do_row && !TWO_D) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) row_pass(i, raw[i]);
+  }
+  if (need_smem) __syncthreads();
+
+  // ---- transposed copy: unit = RU rows x (32 * CPL) columns per warp
+  if (need_smem) {
+    const int rg = warp / NCG, cg = warp % NCG;
+    const int row0 = rg * RU;
+    const int col0 = cg * (32 * CPL) + lane * CPL;
+    float v[CPL][RU];
+#pragma unroll
+    for (int r = 0; r < RU; ++r) {
+      if (CPL == 4) {
+        uint2 w = *reinterpret_cast<const uint2 *>(&xs[row0 + r][col0]);
+        v[0][r] = bf16_lo(w.x);
+        v[1 % CPL][r] = bf16_hi(w.x);
+        v[2 % CPL][r] = bf16_lo(w.y);
+        v[3 % CPL][r] = bf16_hi(w.y);
+      } else {
+        uint32_t w = *reinterpret_cast<const uint32_t *>(&xs[row0 + r][col0]);
+        v[0][r] = bf16_lo(w);
+        v[1 % CPL][r] = bf16_hi(w);
+      }
+    }
+    if (HAD > 0) {
+      const float cn = (HAD == 16) ? 0.25f : 0x1.6a09e6p-3f;  // RN32(1/sqrt(HAD))
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+#pragma unroll
+        for (int g0 = 0; g0 < RU; g0 += (HAD > 0 ? HAD : RU)) {
+#pragma unroll
+          for (int j = 0; j < (HAD > 0 ? HAD : 1); ++j)
+            if ((p.signs >> j) & 1u) v[c][g0 + j] = -v[c][g0 + j];
+#pragma unroll
+          for (int h = 1; h < (HAD > 0 ? HAD : 1); h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < (HAD > 0 ? HAD : 1); ++i) {
+              if ((i & h) == 0) {
+                float a = v[c][g0 + i], bb = v[c][g0 + i + h];
+                v[c][g0 + i] = __fadd_rn(a, bb);
+                v[c][g0 + i + h] = __fsub_rn(a, bb);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < (HAD > 0 ? HAD : 1); ++j) v[c][g0 + j] = __fmul_rn(v[c][g0 + j], cn);
+        }
+      }
+    }
+#pragma unroll
+    for (int blk = 0; blk < RU / B; ++blk) {
+      float bmax[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        float m = 0.0f;
+#pragma unroll
+        for (int r = 0; r < B; ++r) m = fmaxf(m, fabsf(v[c][blk * B + r]));
+        bmax[c] = m;
+      }
+      if (TWO_D) {
+        // B x B tile max: this lane's CPL columns, then the B / CPL lanes of
+        // the tile.
+        float m = bmax[0];
+#pragma unroll
+        for (int c = 1; c < CPL; ++c) m = fmaxf(m, bmax[c]);
+#pragma unroll
+        for (int o = 1; o < B / CPL; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) bmax[c] = m;
+        if ((lane % (B / CPL)) == 0) tmax[(row0 / B) + blk][col0 / B] = m;
+      }
+      if (p.do_col) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          float mult;
+          bool zp;
+          uint32_t code = block_scale<FMT>(bmax[c], se_c, sd_c, mult, zp);
+          const int tcol = col0 + c;
+          const int64_t gcol = C0 + tcol;
+#pragma unroll
+          for (int h8 = 0; h8 < B / 8; ++h8) {
+            float e[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = v[c][blk * B + 8 * h8 + j];
+            scale8(e, mult, zp);
+            uint32_t word;
+            const int trow = row0 + blk * B + 8 * h8;
+            if (p.sr_col) {
+              uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
+              word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
+            } else {
+              word = encode8_rne(e);
+            }
+            *reinterpret_cast<uint32_t *>(&colq[tcol][trow / 2]) = word;
+          }
+          sfc[tcol][(row0 / B) + blk] = (uint8_t)code;
+        }
+      }
+    }
+  }
+
+  if (TWO_D) {
+    __syncthreads();
+    if (p.do_row) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) row_pass(i, raw[i]);
+    }
+  }
+  __syncthreads();
+
+  // ---- transposed payload: column segments of 64 B leave as 8 B stores
+  if (p.do_col) {
+    for (int idx = threadIdx.x; idx < kTile * 8; idx += kThreads) {
+      int col = idx >> 3, part = idx & 7;
+      int64_t gcol = C0 + col, grow = R0 + 16 * part;
+      if (gcol < C && grow < R) {
+        *reinterpret_cast<uint2 *>(p.q_col + gcol * (R / 2) + grow / 2) =
+            *reinterpret_cast<const uint2 *>(&colq[col][8 * part]);
+      }
+    }
+  }
+  // ---- scales
+  if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
+  if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
+}
+
+// s_dec only (empty tensors).
+template <int FMT>
+__global__ void k_scale_only(const float *amax_row, const float *amax_col, float T, float *sd_row,
+                             float *sd_col) {
+  float se, sd;
+  if (sd_row) {
+    tensor_scale<FMT>(*amax_row, T, se, sd);
+    *sd_row = sd;
+  }
+  if (sd_col) {
+    tensor_scale<FMT>(amax_col ? *amax_col : *amax_row, T, se, sd);
+    *sd_col = sd;
+  }
+}
+
+template <int FMT, int HAD, bool TWO_D>
+fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
+  k_quantize<FMT, HAD, TWO_D><<<(unsigned)tiles, kThreads, 0, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+template <int FMT>
+fp4_status launch_fmt(const Params &p, int64_t tiles, int had, bool two_d, cudaStream_t s) {
+  if (two_d) return launch_t<FMT, 0, true>(p, tiles, s);
+  if (had == 16) return launch_t<FMT, 16, false>(p, tiles, s);
+  if (had == 32) return launch_t<FMT, 32, false>(p, tiles, s);
+  return launch_t<FMT, 0, false>(p, tiles, s);
+}
+
+}  // namespace
+
+fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
+  Params p{};
+  p.x = j.x;
+  p.R = j.R;
+  p.C = j.C;
+  p.amax_row = j.amax_row;
+  p.amax_col = j.amax_col ? j.amax_col : j.amax_row;
+  p.T = j.T;
+  p.q_row = j.q_row;
+  p.sf_row = j.sf_row;
+  p.s_dec_row = j.s_dec_row;
+  p.q_col = j.q_col;
+  p.sf_col = j.sf_col;
+  p.s_dec_col = j.s_dec_col;
+  p.do_row = j.q_row != nullptr;
+  p.do_col = j.q_col != nullptr;
+  p.sr_row = j.sr_row;
+  p.sr_col = j.sr_col;
+  p.sf_mma = j.sf_mma;
+  p.seed = j.seed;
+  p.offset = j.offset;
+  p.signs = j.signs;
+  if (j.R == 0 || j.C == 0) {
+    float *sdr = p.do_row ? p.s_dec_row : nullptr;
+    float *sdc = p.do_col ? p.s_dec_col : nullptr;
+    switch (j.fmt) {
+      case kUE5M3: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
+      case kNVFP4: k_scale_only<kNVFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
+      default: k_scale_only<kMXFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+  }
+  const int64_t tiles_r = ceil_div(j.R, kTile);
+  p.tiles_c = ceil_div(j.C, kTile);
+  const int64_t tiles = tiles_r * p.tiles_c;
+  const bool two_d = j.block2d != 0;
+  const int had = p.do_col ? j.had_n : 0;
+  fp4_status st;
+  switch (j.fmt) {
+    case kUE5M3: st = launch_fmt<kUE5M3>(p, tiles, had, two_d, s); break;
+    case kNVFP4: st = launch_fmt<kNVFP4>(p, tiles, had, two_d, s); break;
+    default: st = launch_fmt<kMXFP4>(p, tiles, had, two_d, s); break;
+  }
+  if (st != FP4_OK) return st;
+  if (j.fmt == kUE5M3 && j.sf_mma) {
+    if (p.do_row && j.shift_row) {
+      st = launch_remap_ue5m3(j.sf_row, j.q_row, j.R, j.C, j.shift_row, s);
+      if (st != FP4_OK) return st;
+    }
+    if (p.do_col && j.shift_col) {
+      st = launch_remap_ue5m3(j.sf_col, j.q_col, j.C, j.R, j.shift_col, s);
+      if (st != FP4_OK) return st;
+    }
+  }
+  return FP4_OK;
+}
+
+}  // namespace fp4

@@ -1,0 +1,197 @@
+/*
+ * fp4.h -- C ABI of the GB300 (sm_103a) FP4 block-scaled quantize-and-multiply
+ * library (libfp4gb300.so).
+ *
+ * What it computes -- sources, cited by page title and section:
+ *   [UE5M3] "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining"
+ *           Approach (E2M1 payload, UE5M3 block scale, block 16, per-operand
+ *           amax cache with sample-and-hold every D steps, target T, RNE,
+ *           SR on dY only, zero-scale rule, 2D weight scaling, probe-matched
+ *           GEMM model), Contributions (61,440 / T headroom), Limitations
+ *           (UE5M3 scales are not native on the tensor cores).
+ *   [MXH]   "Technical summary: LLM pretraining with MXFP4" (gist.science,
+ *           arXiv 2605.09825) Method and Findings (deterministic H16 / H32
+ *           rotation of the weight-gradient operands).
+ *   [FAF]   "Format-Aware Fusion for Fast FP4 Pretraining" Abstract
+ *           (producers co-designed with the consumer's scale layout;
+ *           MXFP4 with row-gradient SR and fixed-sign 32-point Hadamard).
+ *   [HOP]   "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"
+ *           Method (MXFP4: E2M1 payload with a power-of-two scale per 32).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership: the caller allocates every buffer; no entry point allocates
+ *   device memory.  Pointers named *_dev and every tensor pointer are device
+ *   pointers; parameter structs are read from host memory during the call.
+ * Streams: work is enqueued on `stream` (a cudaStream_t passed as void*; NULL
+ *   is the legacy default stream) and the call returns without waiting.
+ * Errors: argument, shape and alignment errors are returned before anything
+ *   is launched.  Conditions found on the device (a bounded wait that ran
+ *   out, a non-finite amax, a UE5M3 scale outside the tensor core's window)
+ *   set bits of a per-device status word; fp4_status_sync() reports them.
+ *   No entry point traps, exits or throws.
+ * Layouts: tensors are row-major.  A "copy" is one quantised view: the
+ *   row-wise copy blocks each row of x along its columns; the transposed copy
+ *   is x^T blocked along x's rows.  Payload q holds two E2M1 codes per byte,
+ *   element 2j in the low nibble of byte j, rows of cols/2 bytes.
+ */
+#ifndef FP4_GB300_H
+#define FP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP4_OK = 0,
+  FP4_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum      */
+  FP4_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned                */
+  FP4_ERR_SHAPE = 3,        /* size not a multiple the layout needs       */
+  FP4_ERR_UNSUPPORTED = 4,  /* valid but unsupported option combination   */
+  FP4_ERR_CUDA = 5,         /* a CUDA runtime call failed                 */
+  FP4_ERR_TIMEOUT = 6,      /* a bounded device wait ran out              */
+  FP4_ERR_NONFINITE = 7,    /* amax saw Inf or NaN                        */
+  FP4_ERR_SCALE_WINDOW = 8  /* a UE5M3 row spans more than E4M3 can hold  */
+} fp4_status;
+
+/* Payload is always E2M1.  Block scale and block size per format:
+ *   UE5M3_B16: unsigned E5M3 (bias 15, largest value 61,440), 16 elements
+ *              -- the primary recipe of [UE5M3] Approach;
+ *   NVFP4_B16: E4M3 (bias 7, largest value 448), 16 elements;
+ *   MXFP4_B32: E8M0 (2^(code-127)), 32 elements, no per-tensor scale. */
+typedef enum {
+  FP4_FMT_UE5M3_B16 = 0,
+  FP4_FMT_NVFP4_B16 = 1,
+  FP4_FMT_MXFP4_B32 = 2
+} fp4_format;
+
+typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_rounding;
+
+/* Scale-factor layout.  PLAIN: [rows][cols/B] bytes.  MMA: the tiled layout
+ * the block-scaled tensor-core MMA reads -- rows padded to 128 and scale
+ * columns to 4, cut into 128 x 4 tiles of 512 bytes stored tile-row by
+ * tile-row, row r / column c of a tile at byte (r%32)*16 + (r/32)*4 + c;
+ * padding bytes are written as zero.  fp4_sf_bytes() gives the size. */
+typedef enum { FP4_SF_PLAIN = 0, FP4_SF_MMA = 1 } fp4_sf_layout;
+
+/* Producer options ([UE5M3] Approach; [FAF] Abstract; [MXH] Method). */
+typedef struct {
+  int32_t format;          /* fp4_format                                      */
+  float T;                 /* scale target, 1 <= T <= 61440 (ignored: MXFP4);
+                              448 default, 2048 for the dY override          */
+  int32_t block2d;         /* 1: one scale per B x B tile shared by both
+                              copies (weights); RNE only, no Hadamard        */
+  int32_t round_row;       /* fp4_rounding of the row-wise copy              */
+  int32_t round_col;       /* fp4_rounding of the transposed copy            */
+  uint64_t sr_seed;        /* Philox4x32-10 key (lo, hi words)               */
+  uint32_t sr_offset;      /* fourth Philox counter word, e.g. the step      */
+  int32_t hadamard_n;      /* 0, 16 or 32: rotation of the transposed copy   */
+  uint32_t hadamard_signs; /* bit j set: input lane j of each group negated  */
+  int32_t sf_layout;       /* fp4_sf_layout of every scale output            */
+} fp4_quant_params;
+
+/* One quantised GEMM operand: `rows` rows of `k` elements, K-major. */
+typedef struct {
+  const uint8_t *q;         /* [rows][k/2] payload                          */
+  const uint8_t *sf;        /* MMA-layout scales: E4M3 (NVFP4, and UE5M3
+                               after remap), E8M0 (MXFP4)                   */
+  const float *s_dec;       /* device: per-tensor decode scale (1 for MX)   */
+  const int8_t *row_shift;  /* device, UE5M3 only: [rows] power-of-two
+                               exponents from the remap; NULL otherwise     */
+  int32_t format;           /* fp4_format                                   */
+  int64_t rows, k;
+} fp4_operand;
+
+/* Amax of a BF16 tensor x[rows][cols] ([UE5M3] Approach: per-operand amax
+ * caches refreshed every D steps; the caller runs this on refresh steps and
+ * keeps the result on the device between them).
+ *   amax_row_dev: max |x| (exact, binary32).
+ *   amax_col_dev (nullable): the amax the transposed copy uses -- max |x|
+ *     again when hadamard_n == 0, else max |y| with y the transposed view
+ *     rotated by the fixed-sign Hadamard along its rows ([MXH] Findings).
+ *     hadamard_n in {0, 16, 32}; rows % hadamard_n == 0.
+ * Inf/NaN in x sets FP4_ERR_NONFINITE in the status word.
+ * Alignment: x 16-byte aligned, cols % 8 == 0; outputs 4-byte aligned. */
+fp4_status fp4_amax(const void *x_bf16, int64_t rows, int64_t cols,
+                    int32_t hadamard_n, uint32_t hadamard_signs,
+                    float *amax_row_dev, float *amax_col_dev, void *stream);
+
+/* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
+ * payload, RNE or SR, zero-scale rule, 2D weight tiles):
+ *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);
+ *   per block b = max|x|, sf = enc(RN32(RN32(b/6) * s_enc)) nearest-even,
+ *   saturating, 0 -> code of 1.0 (MX: E = floor(log2 b) - 2);
+ *   q = E2M1(x * RN32(1 / RN32(dec(sf) * s_dec)))  (MX: x * 2^-E).
+ * amax_dev: device binary32 held amax.  Outputs: q [rows][cols/2], sf
+ * (layout per p->sf_layout), s_dec_dev (one float).  row_shift (nullable):
+ * only with UE5M3 and the MMA layout -- then sf receives the E4M3 image of
+ * the UE5M3 scales for the tensor core and row_shift[rows] the per-row
+ * power-of-two exponents (a row spanning more binades than E4M3 holds sets
+ * FP4_ERR_SCALE_WINDOW); with row_shift NULL, sf holds UE5M3 codes.
+ * Shapes: cols % B == 0, and rows % B == 0 with block2d.  rows == 0 or
+ * cols == 0 writes only s_dec.  Alignment: x, q, sf 16 bytes. */
+fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols,
+                        const float *amax_dev, const fp4_quant_params *p,
+                        uint8_t *q, uint8_t *sf, float *s_dec_dev,
+                        int8_t *row_shift, void *stream);
+
+/* Row-wise and transposed copies in one pass over x ([UE5M3] Approach:
+ * dW = dY^T X needs both layouts; [FAF] Abstract: layout construction and
+ * saved backward state fused into the producer; [MXH] Findings: H16 / H32
+ * on the weight-gradient operand).  The transposed copy is x^T quantised
+ * exactly as a row-wise copy, with its own amax (amax_col_dev) and, when
+ * p->hadamard_n != 0, after the rotation y = RN32(1/sqrt(n)) H_n diag(s) x
+ * of every n consecutive elements of its rows (butterflies of span 1, 2, 4,
+ * ... in binary32, then the normaliser).  With block2d both copies share
+ * the B x B tile scales and the transposed payload is the nibble transpose.
+ * SR draws Philox4x32-10 with key sr_seed and counter (g_lo, g_hi, copy,
+ * sr_offset), g = (row * cols_of_copy + col) >> 3, copy 0 row-wise / 1
+ * transposed, 16 bits per element.
+ * Outputs: q_row [rows][cols/2], sf_row, s_dec_row, shift_row (as in
+ * fp4_quantize); q_col [cols][rows/2], sf_col, s_dec_col, shift_col.
+ * Shapes: rows % B == 0, cols % B == 0, rows % hadamard_n == 0. */
+fp4_status fp4_quantize_transpose(
+    const void *x_bf16, int64_t rows, int64_t cols, const float *amax_row_dev,
+    const float *amax_col_dev, const fp4_quant_params *p, uint8_t *q_row,
+    uint8_t *sf_row, float *s_dec_row, int8_t *shift_row, uint8_t *q_col,
+    uint8_t *sf_col, float *s_dec_col, int8_t *shift_col, void *stream);
+
+/* Block-scaled FP4 GEMM D[M][N] = alpha * A[M][K] * B[N][K]^T on the tcgen05
+ * tensor cores ([UE5M3] Approach: fprop Y = X W^T, dgrad dX = dY W, wgrad
+ * dW = dY^T X, all "TN" because the producers supply the transposes).
+ * alpha = RN32(s_dec_A * s_dec_B); for UE5M3 operands each output is first
+ * multiplied by 2^(shift_A[m] + shift_B[n]).  The tensor core adds K in
+ * 64-element MMA steps into a binary32 accumulator in tensor memory, the
+ * order the probe-matched model of [UE5M3] describes.  canonicalize_1024:
+ * acc <- RNE(1024 * acc) / 1024 before alpha.  D is binary32 (d_is_bf16 ==
+ * 0) or BF16 (nearest-even), row pitch N elements.
+ * Shapes: A->rows == M, B->rows == N, A->k == B->k == K, K % 64 == 0, same
+ * format on both sides, N % 8 == 0.  K == 0 writes zeros.  Alignment: q, sf,
+ * D 16 bytes. */
+fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M,
+                    int64_t N, int64_t K, void *D, int32_t d_is_bf16,
+                    int32_t canonicalize_1024, void *stream);
+
+/* Bytes of one scale-factor output for a copy with `rows` rows and `cols`
+ * elements per row; -1 for an invalid format/layout. */
+int64_t fp4_sf_bytes(int32_t format, int64_t rows, int64_t cols,
+                     int32_t layout);
+
+/* Block size (16 or 32) of a format; -1 if invalid. */
+int32_t fp4_block_size(int32_t format);
+
+/* Waits for `stream`, then returns and clears the device status word of the
+ * current device (FP4_OK if no device condition was raised).  Calls that
+ * overlap on the device share one status word. */
+fp4_status fp4_status_sync(void *stream);
+
+/* Static description of a status code. */
+const char *fp4_status_string(fp4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/fp4.h declares, with the struct layout the Python binding assumes.
+CPU only: no compute call is made."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import fp4_block_scaled_quantize_gb300 as fq
+from fp4_block_scaled_quantize_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fbuild.build()
+    return fq.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^[\w\s\*]*?\b(fp4_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 8, names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(fq.EXPORTS) <= set(names)
+
+
+def test_struct_layout_matches_header():
+    c = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "fp4.h"
+int main(void){
+  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(fp4_quant_params), offsetof(fp4_quant_params, sr_seed),
+         offsetof(fp4_quant_params, sf_layout), sizeof(fp4_operand), offsetof(fp4_operand, format),
+         offsetof(fp4_operand, k));
+  return 0; }
+"""
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(src, "w").write(c)
+        subprocess.run(["gcc", "-I" + os.path.dirname(HEADER), src, "-o", exe], check=True)
+        got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    P, O = fq.fp4_quant_params, fq.fp4_operand
+    assert got == [ctypes.sizeof(P), P.sr_seed.offset, P.sf_layout.offset, ctypes.sizeof(O),
+                   O.format.offset, O.k.offset]
+
+
+def test_host_helpers(L):
+    assert fq.fp4_block_size(fq.FP4_FMT_UE5M3_B16) == 16
+    assert fq.fp4_block_size(fq.FP4_FMT_MXFP4_B32) == 32
+    assert fq.fp4_block_size(9) == -1
+    assert fq.fp4_sf_bytes(0, 100, 64, fq.FP4_SF_PLAIN) == 400
+    assert fq.fp4_sf_bytes(0, 100, 64, fq.FP4_SF_MMA) == 128 * 4
+    assert fq.fp4_sf_bytes(2, 300, 96, fq.FP4_SF_MMA) == 384 * 4
+    assert fq.fp4_sf_bytes(1, 256, 4096, fq.FP4_SF_MMA) == 256 * 256
+    assert fq.fp4_status_string(0) == "ok"
+    assert "aligned" in fq.fp4_status_string(2)
+
+
+def test_invalid_arguments_rejected_before_any_launch(L):
+    # null params / null operands fail validation without touching the device
+    assert L.fp4_quantize(None, 4, 16, None, None, None, None, None, None, None) == 1
+    assert L.fp4_gemm(None, None, 1, 1, 64, None, 0, 0, None) == 1
+    A = fq.fp4_operand(None, None, None, None, 0, 4, 64)
+    B = fq.fp4_operand(None, None, None, None, 1, 8, 64)
+    assert fq.fp4_gemm(A, B, 4, 8, 64, None, 0, 0, stream=type("S", (), {"cuda_stream": 0})()) == 1

@@ -1,0 +1,190 @@
+"""GPU parity of the tcgen05 block-scaled GEMM against the oracle's
+probe-matched model and its exact decoded-operand reference.
+
+Tolerances (stated with the method): for every output (m, n), with
+S = alpha * sum_k |p_k| the magnitude of the dot product,
+    |y_gpu - y_model| <= 1e-6 S     and     |y_gpu - y_exact| <= 1e-3 S.
+GEMM operands are produced by the oracle's quantizer and uploaded, so the
+GEMM is checked on its own; the end-to-end tests run the whole GPU path
+against the whole oracle path on the same BF16 inputs."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_quantize_gb300 as fq
+from fp4_block_scaled_quantize_gb300 import inputs
+import oracle as orc
+from gpu_util import ORC_FMT, f32, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+UE, NV, MX = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+TOL_MODEL, TOL_EXACT = 1e-6, 1e-3
+
+
+def upload(oq, fmt):
+    """Oracle-quantised copy -> GPU operand in the tensor-core scale layout."""
+    q = torch.from_numpy(np.ascontiguousarray(oq["q"])).cuda()
+    shift = None
+    if fmt == UE:
+        e4, sh, fails = orc.remap_ue5m3(oq["sf"], oq["q"])
+        assert fails == 0
+        sf = orc.sf_to_mma(e4)
+        shift = torch.from_numpy(sh).cuda()
+    else:
+        sf = orc.sf_to_mma(oq["sf"])
+    sf_t = torch.from_numpy(sf).cuda()
+    sd = torch.tensor([oq["s_dec"]], dtype=torch.float32, device="cuda")
+    return fq.Quantized(q, sf_t, sd, shift, fmt, fq.FP4_SF_MMA)
+
+
+def oracle_operand(x_bf16, fmt, T=448.0, block2d=False, sr=False, seed=0):
+    x32 = f32(x_bf16)
+    return orc.quantize(x32, orc.amax(x32), ORC_FMT[fmt], T=T, block2d=block2d, sr=sr, seed=seed)
+
+
+def sample_indices(M, N, count, seed=0):
+    """Seeded (m, n) samples including every corner of every 128 x 256 tile
+    that fits in the budget, plus the matrix corners."""
+    rng = np.random.default_rng(seed)
+    pts = {(0, 0), (M - 1, N - 1), (0, N - 1), (M - 1, 0)}
+    for m0 in range(0, M, 128):
+        for n0 in range(0, N, 256):
+            for dm, dn in ((0, 0), (127, 255), (0, 255), (127, 0)):
+                if len(pts) < count // 2:
+                    pts.add((min(m0 + dm, M - 1), min(n0 + dn, N - 1)))
+    while len(pts) < count:
+        pts.add((int(rng.integers(M)), int(rng.integers(N))))
+    pts = sorted(pts)
+    return np.array([p[0] for p in pts]), np.array([p[1] for p in pts])
+
+
+def check(y_gpu, oa, ob, fmt, K, mi, ni, canon=False, bf16=False, name=""):
+    y_model, y_exact, s_abs = orc.gemm_model(oa["q"], oa["sf"], ob["q"], ob["sf"], ORC_FMT[fmt],
+                                             K, oa["s_dec"], ob["s_dec"], mi, ni, canon=canon)
+    g = y_gpu.float().cpu().numpy()[mi, ni].astype(np.float64)
+    ym = y_model.astype(np.float64)
+    scale = np.maximum(s_abs, 1e-300)
+    if bf16:
+        ym_b = torch.from_numpy(y_model).to(torch.bfloat16).float().numpy().astype(np.float64)
+        tol = np.abs(ym) * 2.0 ** -8 + TOL_MODEL * s_abs
+        err = np.abs(g - ym_b)
+        assert np.all(err <= tol), f"{name}: bf16 max err {err.max()}"
+        return
+    rel_model = np.abs(g - ym) / scale
+    rel_exact = np.abs(g - y_exact) / scale
+    same = np.mean(g == ym)
+    print(f"{name}: max|gpu-model|/S={rel_model.max():.3e} max|gpu-exact|/S={rel_exact.max():.3e} "
+          f"bit-identical to model: {same * 100:.2f}%")
+    bad = np.argwhere(rel_model > TOL_MODEL)
+    assert len(bad) == 0, (f"{name}: {len(bad)} outputs off the model; first (m,n)="
+                           f"{(mi[bad[0][0]], ni[bad[0][0]])} gpu={g[bad[0][0]]} "
+                           f"model={ym[bad[0][0]]} S={s_abs[bad[0][0]]}")
+    assert np.all(rel_exact <= TOL_EXACT), f"{name}: exact-reference error {rel_exact.max()}"
+
+
+@pytest.mark.parametrize("fmt", [NV, UE, MX])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (200, 328, 320),
+                                   (384, 264, 1088)])
+def test_gemm_full_parity_small(fmt, M, N, K):
+    need_gpu()
+    d = inputs.sweep_operand(M + N, K, seed=M * 31 + N + K)
+    a = oracle_operand(d[:M], fmt)
+    b = oracle_operand(d[M:], fmt)
+    y = fq.gemm(upload(a, fmt), upload(b, fmt))
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    check(y, a, b, fmt, K, mm.ravel(), nn.ravel(), name=f"fmt{fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [NV, UE, MX])
+def test_gemm_many_tiles_persistent(fmt):
+    need_gpu()
+    M, N, K = 2304, 4352, 512  # 18 x 17 tiles > one wave of SMs
+    d = inputs.sweep_operand(M + N, K, seed=fmt + 5)
+    a = oracle_operand(d[:M], fmt)
+    b = oracle_operand(d[M:], fmt)
+    y = fq.gemm(upload(a, fmt), upload(b, fmt))
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    mi, ni = sample_indices(M, N, 6000, seed=fmt)
+    check(y, a, b, fmt, K, mi, ni, name=f"fmt{fmt} persistent")
+
+
+@pytest.mark.parametrize("fmt", [NV, UE])
+def test_gemm_bf16_output_and_canonicalisation(fmt):
+    need_gpu()
+    M, N, K = 256, 512, 768
+    d = inputs.sweep_operand(M + N, K, seed=99)
+    a = oracle_operand(d[:M], fmt)
+    b = oracle_operand(d[M:], fmt)
+    A, B = upload(a, fmt), upload(b, fmt)
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    yb = fq.gemm(A, B, out_dtype=torch.bfloat16)
+    check(yb, a, b, fmt, K, mm.ravel(), nn.ravel(), bf16=True, name="bf16")
+    yc = fq.gemm(A, B, canonicalize_1024=True)
+    check(yc, a, b, fmt, K, mm.ravel(), nn.ravel(), canon=True, name="canon")
+
+
+def test_gemm_k_zero_and_empty():
+    need_gpu()
+    A = fq.fp4_operand(None, None, None, None, NV, 64, 0)
+    B = fq.fp4_operand(None, None, None, None, NV, 32, 0)
+    D = torch.full((64, 32), 7.0, device="cuda")
+    assert fq.fp4_gemm(A, B, 64, 32, 0, D, 0) == fq.FP4_OK
+    torch.cuda.synchronize()
+    assert torch.all(D == 0)
+    assert fq.fp4_gemm(A, B, 64, 32, 32, D, 0) == 3  # K % 64 != 0
+
+
+def test_gemm_shape_errors():
+    need_gpu()
+    q = torch.zeros((128, 64), dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(128 * 8, dtype=torch.uint8, device="cuda")
+    sd = torch.ones(1, device="cuda")
+    A = fq.fp4_operand(q.data_ptr(), sf.data_ptr(), sd.data_ptr(), None, NV, 128, 128)
+    B = fq.fp4_operand(q.data_ptr(), sf.data_ptr(), sd.data_ptr(), None, MX, 128, 128)
+    D = torch.empty((128, 128), device="cuda")
+    assert fq.fp4_gemm(A, B, 128, 128, 128, D, 0) == 1  # mixed formats
+    A2 = fq.fp4_operand(q.data_ptr(), sf.data_ptr(), sd.data_ptr(), None, UE, 128, 128)
+    assert fq.fp4_gemm(A2, A2, 128, 128, 128, D, 0) == 1  # UE5M3 needs row shifts
+    assert fq.fp4_gemm(A, A, 128, 124, 128, D, 0) == 3  # N % 8
+
+
+@pytest.mark.parametrize("fmt", [UE, NV, MX])
+def test_end_to_end_layer_small(fmt):
+    """Whole GPU path (amax -> producers -> remap -> fprop / dgrad / wgrad)
+    against the whole oracle path, on the 8B down_proj distributions at a
+    small size."""
+    need_gpu()
+    M, K, N = 256, 384, 256
+    d = inputs.down_proj_8b(M=M, K=K, N=N)
+    X, W, dY = d["X"], d["W"], d["dY"]
+    of = ORC_FMT[fmt]
+    T_dy = 2048.0 if fmt == UE else 448.0
+    # GPU
+    P = lambda **kw: fq.params(format=fmt, sf_layout=fq.FP4_SF_MMA, **kw)
+    xg, wg, dyg = X.cuda(), W.cuda(), dY.cuda()
+    ax, _ = fq.amax(xg)
+    aw, _ = fq.amax(wg)
+    ady, _ = fq.amax(dyg)
+    x_r, x_c = fq.quantize_transpose(xg, ax, ax, P(T=448.0))
+    w_r, w_c = fq.quantize_transpose(wg, aw, aw, P(T=448.0, block2d=True))
+    dy_r, dy_c = fq.quantize_transpose(dyg, ady, ady, P(T=T_dy, round_row=1, round_col=1,
+                                                        sr_seed=42))
+    y = fq.gemm(x_r, w_r)       # fprop   [M, N]
+    dx = fq.gemm(dy_r, w_c)     # dgrad   [M, K]
+    dw = fq.gemm(dy_c, x_c)     # wgrad   [N, K]
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    # oracle
+    x32, w32, dy32 = f32(X), f32(W), f32(dY)
+    ox_r, ox_c = orc.quantize_transpose(x32, orc.amax(x32), orc.amax(x32), of)
+    ow_r, ow_c = orc.quantize_transpose(w32, orc.amax(w32), orc.amax(w32), of, block2d=True)
+    ody_r, ody_c = orc.quantize_transpose(dy32, orc.amax(dy32), orc.amax(dy32), of, T=T_dy,
+                                          sr_row=True, sr_col=True, seed=42)
+    for name, gq, oq in (("X.col", x_c, ox_c), ("dY.row", dy_r, ody_r), ("W.col", w_c, ow_c)):
+        assert np.array_equal(gq.q.cpu().numpy(), oq["q"]), name
+    for name, yg, oa, ob, kk in (("fprop", y, ox_r, ow_r, K), ("dgrad", dx, ody_r, ow_c, N),
+                                 ("wgrad", dw, ody_c, ox_c, M)):
+        Mo, No = yg.shape
+        mm, nn = np.meshgrid(np.arange(Mo), np.arange(No), indexing="ij")
+        check(yg, oa, ob, fmt, kk, mm.ravel(), nn.ravel(), name=f"{name} fmt{fmt}")

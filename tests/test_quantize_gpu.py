@@ -1,0 +1,224 @@
+"""GPU parity of the producers (amax, quantize, quantize_transpose, UE5M3 remap)
+against the CPU oracle: payloads, scales, s_dec and shifts bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_quantize_gb300 as fq
+from fp4_block_scaled_quantize_gb300 import inputs
+import oracle as orc
+from gpu_util import ORC_FMT, expect_sf, f32, mismatch_report, need_gpu, np_u8, set_device_scalar
+
+pytestmark = pytest.mark.gpu
+
+UE, NV, MX = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+
+
+def _edge_tensor(rows, cols, seed):
+    """N(0,1) with planted edge blocks: all-zero, -0.0, tiny (zero-scale rule),
+    huge (saturation), BF16 subnormals, exact E2M1 ties."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((rows, cols), generator=g)
+    if rows >= 32 and cols >= 64:
+        x[0:32, 0:32] = 0.0
+        x[1, 0:16] = -0.0
+        x[2:4, 32:64] = 1e-30
+        x[4, 32:48] = 3e4
+        x[5, 0:32] = torch.tensor([2.0 ** -130]).repeat(32)
+        x[6, 0:16] = torch.tensor([6, .25, .75, 1.25, 1.75, 2.5, 3.5, 5, -6, -.25, -.75, -1.25,
+                                   -1.75, -2.5, -3.5, -5.0])
+    return x.to(torch.bfloat16)
+
+
+def _oracle_copies(x32, fmt, T, amax_r, amax_c, block2d, sr_r, sr_c, seed, offset, had, signs):
+    return orc.quantize_transpose(x32, amax_r, amax_c, ORC_FMT[fmt], T=T, block2d=block2d,
+                                  sr_row=sr_r, sr_col=sr_c, seed=seed, offset=offset,
+                                  hadamard_n=had, signs=signs)
+
+
+def _check_copy(name, got, want, fmt, layout, remap):
+    mismatch_report(np_u8(got.q), want["q"], name + ".q")
+    esf, eshift = expect_sf(fmt, want["sf"], want["q"], layout, remap)
+    mismatch_report(np_u8(got.sf), esf, name + ".sf")
+    assert float(got.s_dec.item()) == want["s_dec"], (name, got.s_dec.item(), want["s_dec"])
+    if eshift is not None:
+        mismatch_report(got.row_shift.cpu().numpy()[:len(eshift)], eshift, name + ".shift")
+
+
+CASES = [
+    # rows, cols, fmt, block2d, sr, had, signs, layout
+    (256, 256, UE, False, False, 0, 0, fq.FP4_SF_PLAIN),
+    (384, 640, UE, False, False, 0, 0, fq.FP4_SF_MMA),
+    (208, 336, UE, False, False, 0, 0, fq.FP4_SF_MMA),
+    (208, 336, NV, False, False, 0, 0, fq.FP4_SF_PLAIN),
+    (256, 384, NV, False, False, 0, 0, fq.FP4_SF_MMA),
+    (256, 384, MX, False, False, 0, 0, fq.FP4_SF_PLAIN),
+    (224, 352, MX, False, False, 0, 0, fq.FP4_SF_MMA),
+    (256, 256, UE, True, False, 0, 0, fq.FP4_SF_MMA),
+    (208, 336, NV, True, False, 0, 0, fq.FP4_SF_PLAIN),
+    (256, 384, MX, True, False, 0, 0, fq.FP4_SF_MMA),
+    (256, 512, UE, False, True, 0, 0, fq.FP4_SF_PLAIN),
+    (208, 336, UE, False, True, 0, 0, fq.FP4_SF_MMA),
+    (256, 256, MX, False, True, 0, 0, fq.FP4_SF_PLAIN),
+    (256, 256, UE, False, False, 16, 0, fq.FP4_SF_PLAIN),
+    (256, 256, UE, False, True, 16, 0xB00F, fq.FP4_SF_MMA),
+    (384, 256, UE, False, False, 32, 0, fq.FP4_SF_MMA),
+    (256, 256, MX, False, True, 32, 0x9A3C5F01, fq.FP4_SF_PLAIN),
+    (288, 160, MX, False, False, 16, 0x1234, fq.FP4_SF_MMA),
+    (16, 16, UE, False, False, 0, 0, fq.FP4_SF_MMA),
+    (32, 32, MX, False, False, 0, 0, fq.FP4_SF_PLAIN),
+]
+
+
+@pytest.mark.parametrize("rows,cols,fmt,block2d,sr,had,signs,layout", CASES)
+def test_quantize_transpose_parity(rows, cols, fmt, block2d, sr, had, signs, layout):
+    need_gpu()
+    x = _edge_tensor(rows, cols, seed=rows * 7 + cols)
+    xg = x.cuda()
+    a_r, a_c = fq.amax(xg, had, signs)
+    x32 = f32(x)
+    ea_r, ea_c = orc.amax_pair(x32, had, signs)
+    assert a_r.item() == ea_r and a_c.item() == ea_c
+    T = 2048.0 if sr else 448.0
+    p = fq.params(format=fmt, T=T, block2d=block2d, round_row=int(sr), round_col=int(sr),
+                  sr_seed=42, sr_offset=7, hadamard_n=had, hadamard_signs=signs,
+                  sf_layout=layout)
+    r, c = fq.quantize_transpose(xg, a_r, a_c, p)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    er, ec = _oracle_copies(x32, fmt, T, ea_r, ea_c, block2d, sr, sr, 42, 7, had, signs)
+    _check_copy("row", r, er, fmt, layout, True)
+    _check_copy("col", c, ec, fmt, layout, True)
+
+
+@pytest.mark.parametrize("fmt,layout,block2d,sr", [
+    (UE, fq.FP4_SF_PLAIN, False, False), (UE, fq.FP4_SF_MMA, False, True),
+    (NV, fq.FP4_SF_MMA, True, False), (MX, fq.FP4_SF_PLAIN, False, True),
+    (MX, fq.FP4_SF_MMA, True, False)])
+def test_quantize_rowwise_parity(fmt, layout, block2d, sr):
+    need_gpu()
+    rows, cols = (160, 416) if fmt != MX else (160, 416 - 32)
+    x = _edge_tensor(rows, cols, seed=3)
+    xg = x.cuda()
+    a, _ = fq.amax(xg)
+    x32 = f32(x)
+    p = fq.params(format=fmt, T=448.0, block2d=block2d, round_row=int(sr), sr_seed=5,
+                  sr_offset=1, sf_layout=layout)
+    out = fq.quantize(xg, a, p)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    want = orc.quantize(x32, orc.amax(x32), ORC_FMT[fmt], T=448.0, block2d=block2d, sr=sr,
+                        seed=5, offset=1)
+    _check_copy("row", out, want, fmt, layout, True)
+
+
+def test_ue5m3_mma_without_remap_keeps_ue5m3_codes():
+    need_gpu()
+    x = inputs.tiny()["X"]
+    xg = x.cuda()
+    a, _ = fq.amax(xg)
+    p = fq.params(format=UE, sf_layout=fq.FP4_SF_MMA)
+    out = fq.quantize(xg, a, p, remap=False)
+    want = orc.quantize(f32(x), a.item(), orc.UE5M3)
+    mismatch_report(np_u8(out.sf), orc.sf_to_mma(want["sf"]), "sf")
+
+
+@pytest.mark.parametrize("workload", ["tiny", "backward_sr", "forward_layer", "down_proj_8b"])
+def test_workload_distributions_small(workload):
+    """The pages' workload distributions at small sizes, all three formats."""
+    need_gpu()
+    gen = getattr(inputs, workload)
+    kw = {} if workload == "tiny" else dict(M=256, K=384, N=128)
+    data = gen(**kw)
+    for name, x in data.items():
+        xg = x.cuda()
+        x32 = f32(x)
+        for fmt in (UE, NV, MX):
+            sr = name == "dY"
+            stale = 0.5 if (workload == "backward_sr" and name == "dY") else 1.0
+            T = 2048.0 if (sr and fmt == UE) else 448.0
+            a_r, a_c = fq.amax(xg)
+            a_r.mul_(stale)
+            a_c.mul_(stale)
+            block2d = name == "W"
+            p = fq.params(format=fmt, T=T, block2d=block2d, round_row=int(sr),
+                          round_col=int(sr), sr_seed=42, sf_layout=fq.FP4_SF_MMA)
+            r, c = fq.quantize_transpose(xg, a_r, a_c, p)
+            st = fq.fp4_status_sync()
+            assert st == fq.FP4_OK, fq.STATUS_NAMES[st]
+            am = orc.amax(x32) * stale
+            er, ec = _oracle_copies(x32, fmt, T, am, am, block2d, sr, sr, 42, 0, 0, 0)
+            _check_copy(f"{workload}.{name}.row", r, er, fmt, fq.FP4_SF_MMA, True)
+            _check_copy(f"{workload}.{name}.col", c, ec, fmt, fq.FP4_SF_MMA, True)
+
+
+def test_stale_amax_tiny_and_degenerate_scales():
+    need_gpu()
+    x = _edge_tensor(128, 128, seed=11)
+    xg = x.cuda()
+    x32 = f32(x)
+    for amax_v in (0.0, 1e-38, 2.0 ** -133, 1e30, float(orc.amax(x32)) * 0.01):
+        for fmt in (UE, NV):
+            a = set_device_scalar(amax_v)
+            p = fq.params(format=fmt, T=448.0)
+            out = fq.quantize(xg, a, p)
+            want = orc.quantize(x32, np.float32(amax_v), ORC_FMT[fmt], T=448.0)
+            _check_copy(f"amax={amax_v}", out, want, fmt, fq.FP4_SF_PLAIN, False)
+
+
+def test_empty_inputs_write_s_dec_only():
+    need_gpu()
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    a = set_device_scalar(3.0)
+    p = fq.params(format=UE)
+    out = fq.quantize(x, a, p)
+    torch.cuda.synchronize()
+    assert out.s_dec.item() == orc.tensor_scale(orc.UE5M3, 448.0, 3.0)[1]
+    r, c = fq.quantize_transpose(x, a, a, p)
+    torch.cuda.synchronize()
+    assert r.s_dec.item() == c.s_dec.item() == out.s_dec.item()
+    ar, ac = fq.amax(x)
+    assert ar.item() == 0.0
+
+
+def test_nonfinite_amax_is_reported():
+    need_gpu()
+    x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    x[3, 5] = float("inf")
+    fq.amax(x)
+    assert fq.fp4_status_sync() == 7  # FP4_ERR_NONFINITE
+    assert fq.fp4_status_sync() == fq.FP4_OK  # cleared
+
+
+def test_scale_window_is_reported():
+    need_gpu()
+    # one row with blocks 2^28 apart: no per-row shift maps both onto E4M3
+    x = torch.full((128, 64), 1.0, dtype=torch.float32)
+    x[0, 0:16] = 2.0 ** 14
+    x[0, 16:32] = 2.0 ** -14
+    xg = x.to(torch.bfloat16).cuda()
+    a = set_device_scalar(2688.0)  # s_enc = 1
+    p = fq.params(format=UE, sf_layout=fq.FP4_SF_MMA)
+    out = fq.quantize(xg, a, p)
+    assert fq.fp4_status_sync() == 8  # FP4_ERR_SCALE_WINDOW
+    want = orc.quantize(f32(xg.cpu()), 2688.0, orc.UE5M3)
+    e4, shift, fails = orc.remap_ue5m3(want["sf"], want["q"])
+    assert fails == 1
+    mismatch_report(np_u8(out.sf), orc.sf_to_mma(e4), "sf")
+
+
+def test_argument_errors_are_synchronous():
+    need_gpu()
+    x = torch.zeros((64, 40), dtype=torch.bfloat16, device="cuda")  # 40 % 16 != 0
+    a = set_device_scalar(1.0)
+    p = fq.params(format=UE)
+    q = torch.empty((64, 20), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(64 * 3, dtype=torch.uint8, device="cuda")
+    sd = torch.empty(1, dtype=torch.float32, device="cuda")
+    assert fq.fp4_quantize(x, a, p, q, sf, sd) == 3  # FP4_ERR_SHAPE
+    x2 = torch.zeros((64, 48), dtype=torch.bfloat16, device="cuda")
+    bad = fq.params(format=7)
+    assert fq.fp4_quantize(x2, a, bad, q, sf, sd) == 1
+    p2d = fq.params(format=UE, block2d=True, round_row=fq.FP4_ROUND_SR)
+    assert fq.fp4_quantize(x2, a, p2d, q, sf, sd) == 4
+    big = torch.zeros(64 * 48 + 8, dtype=torch.bfloat16, device="cuda")
+    xs = big[1:1 + 64 * 48].view(64, 48)  # 2-byte offset: misaligned
+    assert fq.fp4_quantize(xs, a, p, q, sf, sd) == 2
