@@ -424,6 +424,28 @@ def run_reference(args, world, rank):
     print(json.dumps(out))
 
 
+def run_profile(args, local):
+    """Set up the step's buffers, then launch one kernel kind three times
+    (the workload of an ncu capture; prints nothing else)."""
+    torch.cuda.set_device(local)
+    layer = Layer(args.format, seed=args.seed, device=torch.device("cuda", local))
+    fq = layer.fq
+    ops = {
+        "amax": lambda: fq._check(fq.fp4_amax(layer.X, 0, 0, *layer.amax["X"]), "amax"),
+        "quant_X": lambda: layer._qt(layer.X, "X", layer.px, layer.xr, layer.xc),
+        "quant_W": lambda: layer._qt(layer.W, "W", layer.pw, layer.wr, layer.wc),
+        "quant_dY": lambda: layer._qt(layer.dY, "dY", layer.pdy, layer.dyr, layer.dyc),
+        "fprop": lambda: fq.gemm(layer.xr, layer.wr, out=layer.Y),
+        "dgrad": lambda: fq.gemm(layer.dyr, layer.wc, out=layer.dX),
+        "wgrad": lambda: fq.gemm(layer.dyc, layer.xc, out=layer.dW),
+    }
+    torch.cuda.synchronize()
+    for _ in range(3):
+        ops[args.profile]()
+    torch.cuda.synchronize()
+    fq._check(fq.fp4_status_sync(), "profile")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,9 +454,14 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--format", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--profile", default=None,
+                    choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad"],
+                    help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     world, rank, local = dist_init()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args, local)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_gpu(args, world, rank, local)

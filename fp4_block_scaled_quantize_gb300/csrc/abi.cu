@@ -159,11 +159,6 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   j.sf_col = sf_col;
   j.s_dec_col = s_dec_col;
   j.shift_col = shift_col;
-  if (empty) {
-    // keep both s_dec outputs defined
-    j.q_row = reinterpret_cast<uint8_t *>(1);
-    j.q_col = reinterpret_cast<uint8_t *>(1);
-  }
   return launch_quantize(j, as_stream(stream));
 }
 

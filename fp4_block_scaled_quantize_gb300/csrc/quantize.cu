@@ -20,13 +20,17 @@
 //  * transposed payload bytes are staged in shared memory so every column
 //    segment leaves as contiguous 8-byte stores; scales leave as whole
 //    512-byte tensor-core tiles (or plain rows).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 #include "formats.cuh"
 
+// The hardware conversion cvt.rn.satfinite.e2m1x2.f32 was checked against
+// e2m1_rne on every binary32 input (all 2^32 patterns, NaN excluded) and
+// found identical, sign of zero included; it replaces the software encoder.
 #ifndef FP4_HW_E2M1
-#define FP4_HW_E2M1 0
+#define FP4_HW_E2M1 1
 #endif
 
 namespace fp4 {
@@ -50,6 +54,15 @@ struct Params {
   uint64_t seed;
   uint32_t offset, signs;
 };
+
+constexpr uint32_t kMag2 = 0x7FFF7FFFu;  // clears the sign bits of two BF16
+
+// Per-half maximum of two pairs of non-negative BF16 (a selection: exact).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                             *reinterpret_cast<const __nv_bfloat162 *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   uint4 v;
@@ -191,9 +204,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     if (TWO_D) {
       b = tmax[r / B][chunk / LANES_PER_BLOCK];
     } else {
-      b = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) b = fmaxf(b, fabsf(v[j]));
+      const uint32_t m = bmax2(bmax2(w.x & kMag2, w.y & kMag2), bmax2(w.z & kMag2, w.w & kMag2));
+      b = fmaxf(bf16_lo(m), bf16_hi(m));
 #pragma unroll
       for (int o = 1; o < LANES_PER_BLOCK; o <<= 1)
         b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
@@ -226,6 +238,78 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     const int rg = warp / NCG, cg = warp % NCG;
     const int row0 = rg * RU;
     const int col0 = cg * (32 * CPL) + lane * CPL;
+    // Encode the B-row block starting at unit row rb of column c (tile
+    // column col0 + c) whose max |value| is bmax; value(r) gives unit row r.
+    auto emit_col = [&](int c, int rb, float bmax, auto value) {
+      float mult;
+      bool zp;
+      const uint32_t code = block_scale<FMT>(bmax, se_c, sd_c, mult, zp);
+      const int tcol = col0 + c;
+      const int64_t gcol = C0 + tcol;
+#pragma unroll
+      for (int h8 = 0; h8 < B / 8; ++h8) {
+        float e[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = value(rb + 8 * h8 + j);
+        scale8(e, mult, zp);
+        uint32_t word;
+        const int trow = row0 + rb + 8 * h8;
+        if (p.sr_col) {
+          uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
+          word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
+        } else {
+          word = encode8_rne(e);
+        }
+        *reinterpret_cast<uint32_t *>(&colq[tcol][trow / 2]) = word;
+      }
+      sfc[tcol][(row0 + rb) / B] = (uint8_t)code;
+    };
+    auto tile_max_2d = [&](float *bmax, int blk) {
+      // B x B tile max: this lane's CPL columns, then the B / CPL lanes of
+      // the tile.
+      float m = bmax[0];
+#pragma unroll
+      for (int c = 1; c < CPL; ++c) m = fmaxf(m, bmax[c]);
+#pragma unroll
+      for (int o = 1; o < B / CPL; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) bmax[c] = m;
+      if ((lane % (B / CPL)) == 0) tmax[(row0 / B) + blk][col0 / B] = m;
+    };
+    if constexpr (HAD == 0) {
+      // No rotation: RU == B.  Keep the BF16 pairs packed; the column maxima
+      // are per-half maxima of the magnitude bits.
+      constexpr int WPR = CPL / 2;  // 32-bit words per row
+      uint32_t w[RU][WPR];
+#pragma unroll
+      for (int r = 0; r < RU; ++r) {
+        if (WPR == 2) {
+          const uint2 t = *reinterpret_cast<const uint2 *>(&xs[row0 + r][col0]);
+          w[r][0] = t.x;
+          w[r][WPR - 1] = t.y;
+        } else {
+          w[r][0] = *reinterpret_cast<const uint32_t *>(&xs[row0 + r][col0]);
+        }
+      }
+      float bmax[CPL];
+#pragma unroll
+      for (int k = 0; k < WPR; ++k) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int r = 0; r < RU; ++r) m = bmax2(m, w[r][k] & kMag2);
+        bmax[2 * k] = bf16_lo(m);
+        bmax[2 * k + 1] = bf16_hi(m);
+      }
+      if (TWO_D) tile_max_2d(bmax, 0);
+      if (p.do_col) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+          emit_col(c, 0, bmax[c], [&](int r) {
+            const uint32_t x = w[r][c >> 1];
+            return (c & 1) ? bf16_hi(x) : bf16_lo(x);
+          });
+      }
+    } else {
     float v[CPL][RU];
 #pragma unroll
     for (int r = 0; r < RU; ++r) {
@@ -241,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
         v[1 % CPL][r] = bf16_hi(w);
       }
     }
-    if (HAD > 0) {
+    {
       const float cn = (HAD == 16) ? 0.25f : 0x1.6a09e6p-3f;  // RN32(1/sqrt(HAD))
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
@@ -276,45 +360,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
         for (int r = 0; r < B; ++r) m = fmaxf(m, fabsf(v[c][blk * B + r]));
         bmax[c] = m;
       }
-      if (TWO_D) {
-        // B x B tile max: this lane's CPL columns, then the B / CPL lanes of
-        // the tile.
-        float m = bmax[0];
-#pragma unroll
-        for (int c = 1; c < CPL; ++c) m = fmaxf(m, bmax[c]);
-#pragma unroll
-        for (int o = 1; o < B / CPL; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) bmax[c] = m;
-        if ((lane % (B / CPL)) == 0) tmax[(row0 / B) + blk][col0 / B] = m;
-      }
       if (p.do_col) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          float mult;
-          bool zp;
-          uint32_t code = block_scale<FMT>(bmax[c], se_c, sd_c, mult, zp);
-          const int tcol = col0 + c;
-          const int64_t gcol = C0 + tcol;
-#pragma unroll
-          for (int h8 = 0; h8 < B / 8; ++h8) {
-            float e[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = v[c][blk * B + 8 * h8 + j];
-            scale8(e, mult, zp);
-            uint32_t word;
-            const int trow = row0 + blk * B + 8 * h8;
-            if (p.sr_col) {
-              uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
-              word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
-            } else {
-              word = encode8_rne(e);
-            }
-            *reinterpret_cast<uint32_t *>(&colq[tcol][trow / 2]) = word;
-          }
-          sfc[tcol][(row0 / B) + blk] = (uint8_t)code;
-        }
+        for (int c = 0; c < CPL; ++c)
+          emit_col(c, blk * B, bmax[c], [&](int r) { return v[c][r]; });
       }
+    }
     }
   }
 
@@ -397,8 +448,8 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   p.offset = j.offset;
   p.signs = j.signs;
   if (j.R == 0 || j.C == 0) {
-    float *sdr = p.do_row ? p.s_dec_row : nullptr;
-    float *sdc = p.do_col ? p.s_dec_col : nullptr;
+    float *sdr = j.s_dec_row;
+    float *sdc = j.s_dec_col;
     switch (j.fmt) {
       case kUE5M3: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
       case kNVFP4: k_scale_only<kNVFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
