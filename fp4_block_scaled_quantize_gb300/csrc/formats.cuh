@@ -127,6 +127,23 @@ __device__ __forceinline__ int mx_exponent(float b) {
 // 2^-E as binary32, E in [-127, 125].
 __device__ __forceinline__ float pow2_neg(int E) { return __uint_as_float((uint32_t)(127 - E) << 23); }
 
+// ------------------------------------------------------- RN32(b / 6)
+// Correctly rounded division by 6 without the general divide: with
+// y = RN32(1/6), q0 = RN32(b y) is within one ulp of b/6, the residual
+// r = b - 6 q0 is exact in one FMA, and q1 = RN32(q0 + r y) is the
+// correctly rounded quotient (Markstein's theorem on division with a
+// correctly rounded reciprocal; J.-M. Muller et al., "Handbook of
+// Floating-Point Arithmetic", ch. 4).  The theorem needs the quotient to stay
+// in the normal range, so tiny inputs take the IEEE divide.  The result was
+// compared with __fdiv_rn(b, 6) on every non-negative binary32 input.
+__device__ __forceinline__ float div6_rn(float b) {
+  if (!(b >= 0x1p-100f && b < 0x1p120f)) return __fdiv_rn(b, 6.0f);  // tiny, huge, NaN
+  const float y = 0x1.555556p-3f;  // RN32(1/6)
+  const float q0 = __fmul_rn(b, y);
+  const float r = __fmaf_rn(-6.0f, q0, b);
+  return __fmaf_rn(r, y, q0);
+}
+
 // ----------------------------------------------------- block scale rule
 // Block scale code and element multiplier for a block whose max |x| is b:
 //  UE5M3/NVFP4: code = enc(RN32(RN32(b/6) * s_enc)), 0 -> code of 1.0,
@@ -149,6 +166,36 @@ __device__ __forceinline__ uint32_t block_scale(float b, float s_enc, float s_de
     float sd = __fmul_rn(dec, s_dec);
     zero_payload = (sd == 0.0f);
     mult = __fdiv_rn(1.0f, sd);
+    return code;
+  }
+}
+
+// Element multiplier of every scale code for one tensor: tab[code] =
+// RN32(1 / RN32(dec(code) * s_dec)), or 0 where that product is 0 (zero
+// payload).  Built once per CTA; unused for MX.
+template <int FMT>
+__device__ __forceinline__ float mult_of_code(uint32_t code, float s_dec) {
+  const float dec = (FMT == kUE5M3) ? ue5m3_dec(code) : e4m3_dec(code);
+  const float sd = __fmul_rn(dec, s_dec);
+  return sd == 0.0f ? 0.0f : __fdiv_rn(1.0f, sd);
+}
+
+// The block-scale rule above with the two divisions replaced by div6_rn and
+// the per-tensor multiplier table (identical results).
+template <int FMT>
+__device__ __forceinline__ uint32_t block_scale_tab(float b, float s_enc, const float *tab,
+                                                    float &mult, bool &zero_payload) {
+  if (FMT == kMXFP4) {
+    int E = mx_exponent(b);
+    mult = pow2_neg(E);
+    zero_payload = false;
+    return (uint32_t)(E + 127);
+  } else {
+    const float raw = __fmul_rn(div6_rn(b), s_enc);
+    uint32_t code = (FMT == kUE5M3) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
+    if (code == 0) code = (FMT == kUE5M3) ? 0x78u : 0x38u;
+    mult = tab[code];
+    zero_payload = (mult == 0.0f);
     return code;
   }
 }

@@ -45,11 +45,16 @@ constexpr int SFA_BYTES = 4 * 512;              // up to 4 scale tiles (block 16
 constexpr int SFB_BYTES = 2 * 4 * 512;          // two 128-row groups
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 54 KB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quadrant
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;    // 256 binary32 columns
-constexpr uint32_t SFA_COL = 256;  // 4 k-steps x 4 columns
-constexpr uint32_t SFB_COL = 272;  // 4 k-steps x 8 columns
+constexpr uint32_t ACC_COL = 0;      // 256 binary32 columns
+// Scale factors get their own tensor-memory slot per pipeline stage, so the
+// tcgen05.cp of one stage never overwrites scales an earlier stage's MMAs
+// may still be reading: slot = 16 columns of A scales (4 k-steps x 4) then
+// 32 columns of B scales (4 k-steps x 8).
+constexpr uint32_t SF_COL0 = 256;
+constexpr uint32_t SF_SLOT = 48;     // 256 + 4 x 48 = 448 <= 512
 constexpr unsigned long long kTimeoutNs = 1000000000ull;
 
 struct Params {
@@ -169,6 +174,21 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         : "memory");
   }
 }
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 32 consecutive binary32 columns of this thread's tensor-memory lane (no wait).
+__device__ __forceinline__ void tc_ld_32cols_nw(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
+      "15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, 32 * EPI_WARPS);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -314,17 +334,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sfa_s = st + A_BYTES + B_BYTES, sfb_s = sfa_s + SFA_BYTES;
         const int nks = min(4, p.k_steps - 4 * kt);
         const int natoms = (FMT == kMXFP4) ? (nks + 1) / 2 : nks;
+        const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
+        const uint32_t sfb_t = sfa_t + 16;
         for (int a = 0; a < natoms; ++a) {
-          tc_cp_sf(tmem + SFA_COL + 4 * a, desc_sf(sfa_s + 512 * a));
-          tc_cp_sf(tmem + SFB_COL + 8 * a, desc_sf(sfb_s + 512 * a));
-          tc_cp_sf(tmem + SFB_COL + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
+          tc_cp_sf(sfa_t + 4 * a, desc_sf(sfa_s + 512 * a));
+          tc_cp_sf(sfb_t + 8 * a, desc_sf(sfb_s + 512 * a));
+          tc_cp_sf(sfb_t + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
         }
         const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
         for (int kk = 0; kk < nks; ++kk) {
           const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
           const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
-          tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id),
-                      tmem + SFA_COL + 4 * a, tmem + SFB_COL + 8 * a, (kt | kk) != 0);
+          tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id), sfa_t + 4 * a,
+                      sfb_t + 8 * a, (kt | kk) != 0);
           any = true;
         }
         tc_commit(empty_bar(stage));
@@ -343,7 +365,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 2) {
     // --------------------------------------------------------------- epilogue
-    const int quad = warp & 3;  // tensor-memory lane quadrant this warp may read
+    // Each warp reads its lane quadrant (warp % 4) and one half of the 256
+    // accumulator columns into registers, releases the accumulator to the
+    // MMA warp, and only then scales, converts and stores -- the stores of
+    // tile t overlap the MMAs of tile t + 1.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     uint32_t acc_phase = 0;
@@ -351,13 +378,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
       if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
+      uint32_t acc[4][32];
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
       const int64_t m = (int64_t)mt * BM + row_in_tile;
-      const int sa = p.sha && m < p.M ? (int)__ldg(p.sha + m) : 0;
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tc_ld_32cols(tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + c0, r);
-        const int64_t n0 = (int64_t)nt * BN + c0;
-        if (m >= p.M || n0 >= p.N) continue;
+      if (m >= p.M) continue;
+      const int sa = p.sha ? (int)__ldg(p.sha + m) : 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t(&r)[32] = acc[q];
+        const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
+        if (n0 >= p.N) break;
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -395,9 +431,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
     }
   }
   tc_fence_before();

@@ -178,6 +178,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     if (p.do_row) *p.s_dec_row = sd_r;
     if (p.do_col) *p.s_dec_col = sd_c;
   }
+  __shared__ float mtab_r[256], mtab_c[256];  // element multiplier per scale code
+  if (FMT != kMXFP4) {
+    mtab_r[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_r);
+    mtab_c[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_c);
+    __syncthreads();
+  }
 
   // ---- load: lane holds 8 BF16 of row 16w + 2i + (lane >> 4)
   const int chunk = lane & 15;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     }
     float mult;
     bool zp;
-    uint32_t code = block_scale<FMT>(b, se_r, sd_r, mult, zp);
+    uint32_t code = block_scale_tab<FMT>(b, se_r, mtab_r, mult, zp);
     scale8(v, mult, zp);
     uint32_t word;
     if (p.sr_row) {
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     auto emit_col = [&](int c, int rb, float bmax, auto value) {
       float mult;
       bool zp;
-      const uint32_t code = block_scale<FMT>(bmax, se_c, sd_c, mult, zp);
+      const uint32_t code = block_scale_tab<FMT>(bmax, se_c, mtab_c, mult, zp);
       const int tcol = col0 + c;
       const int64_t gcol = C0 + tcol;
 #pragma unroll
