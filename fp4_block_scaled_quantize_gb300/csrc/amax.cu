@@ -55,8 +55,18 @@ __global__ void __launch_bounds__(kThreads) k_amax_plain(const uint4 *__restrict
                                                          float *out_a, float *out_b,
                                                          uint32_t *status) {
   uint32_t m = 0;
-  int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n16; i += stride) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      m = max(m, max(max(mag2(v[u].x), mag2(v[u].y)), max(mag2(v[u].z), mag2(v[u].w))));
+  }
+  for (; i < n16; i += stride) {
     uint4 v = __ldg(x + i);
     m = max(m, max(max(mag2(v.x), mag2(v.y)), max(mag2(v.z), mag2(v.w))));
   }
@@ -118,7 +128,7 @@ int grid_for(int64_t work) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t want = ceil_div(work, kThreads);
-  int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread CTAs per SM
+  int64_t cap = (int64_t)sms * 4;  // 4 resident 256-thread CTAs per SM, 4 loads each
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 

@@ -52,21 +52,19 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
 // test is the integer comparison r16 * 64 < tail.  Below 1 the codebook step
 // is 0.5: t = 2|v|, and the fraction is t - floor(t), exact.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-  float a = fabsf(v);
-  uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-  uint32_t code;
-  if (a >= 6.0f) {
-    code = 7u;
-  } else if (a >= 1.0f) {
-    uint32_t u = __float_as_uint(a);
-    uint32_t e = (u >> 23) - 127u;  // 0, 1 or 2
-    code = 2u + 2u * e + ((u >> 22) & 1u) + (uint32_t)((r16 << 6) < (u & 0x3FFFFFu));
-  } else {
-    float t = __fmul_rn(a, 2.0f);
-    float c = (t >= 1.0f) ? 1.0f : 0.0f;
-    float f = __fmul_rn(__fsub_rn(t, c), 65536.0f);
-    code = (uint32_t)c + (uint32_t)(__uint2float_rn(r16) < f);
-  }
+  const float a = fabsf(v);
+  const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
+  // [1, 6): adding 2^22 - 1 - 64 r16 to the bit pattern carries into the kept
+  // mantissa bit exactly when tail > 64 r16; the code is then the pattern's
+  // top bits (1.0 = 0x3F800000 -> 254 -> code 2).
+  const uint32_t u = __float_as_uint(a) + (0x3FFFFFu - (r16 << 6));
+  const uint32_t c_hi = (u >> 22) - 252u;
+  // [0, 1): step 0.5, t = 2|v|, fraction t - floor(t) exact.
+  const float t = __fmul_rn(a, 2.0f);
+  const float c = (t >= 1.0f) ? 1.0f : 0.0f;
+  const float f = __fmul_rn(__fsub_rn(t, c), 65536.0f);
+  const uint32_t c_lo = (uint32_t)c + (uint32_t)(__uint2float_rn(r16) < f);
+  const uint32_t code = (a >= 6.0f) ? 7u : ((a >= 1.0f) ? c_hi : c_lo);
   return code | sign;
 }
 

@@ -39,6 +39,8 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
+constexpr int kXsPad = 8;                      // BF16 elements (16 bytes)
+constexpr int kColqPitch = kTile * 8 + 32;     // bytes per 16-row plane
 
 struct Params {
   const uint16_t *x;
@@ -147,7 +149,7 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
 }
 
 template <int FMT, int HAD, bool TWO_D>
-__global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
+__global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   constexpr int B = Fmt<FMT>::B;
   constexpr int NSC = kTile / B;                    // scale columns per tile
   constexpr int RU = (HAD > B) ? HAD : B;           // rows per column unit
@@ -155,8 +157,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
   constexpr int NCG = RU / 16;                      // column groups per tile
   constexpr int LANES_PER_BLOCK = B / 8;            // lanes per row block
 
-  __shared__ __align__(16) uint16_t xs[kTile][kTile];  // 32 KB BF16 tile
-  __shared__ __align__(16) uint8_t colq[kTile][kTile / 2];
+  // BF16 tile; rows padded by 16 bytes so the two rows of one 16-byte store
+  // instruction land in different banks.
+  __shared__ __align__(16) uint16_t xs[kTile][kTile + kXsPad];
+  // Transposed payload staged per 16-row plane: colq[plane][col][8 bytes];
+  // planes padded by 32 bytes so the store loop's 8-byte reads are <= 2-way.
+  __shared__ __align__(16) uint8_t colq[kTile / 16][kColqPitch];
   __shared__ __align__(16) uint8_t sfr[kTile][8];
   __shared__ __align__(16) uint8_t sfc[kTile][8];
   __shared__ float tmax[8][8];
@@ -237,6 +243,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) row_pass(i, raw[i]);
   }
+  // the 2D path re-reads its rows from shared memory after the tile maxima
+  // are known instead of keeping them in registers
   if (need_smem) __syncthreads();
 
   // ---- transposed copy: unit = RU rows x (32 * CPL) columns per warp
@@ -244,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     const int rg = warp / NCG, cg = warp % NCG;
     const int row0 = rg * RU;
     const int col0 = cg * (32 * CPL) + lane * CPL;
+    // cw[c][k]: payload word (8 nibbles) of unit rows 8k..8k+7 of column c.
+    uint32_t cw[CPL][RU / 8];
     // Encode the B-row block starting at unit row rb of column c (tile
     // column col0 + c) whose max |value| is bmax; value(r) gives unit row r.
     auto emit_col = [&](int c, int rb, float bmax, auto value) {
@@ -266,9 +276,27 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
         } else {
           word = encode8_rne(e);
         }
-        *reinterpret_cast<uint32_t *>(&colq[tcol][trow / 2]) = word;
+        cw[c][(rb >> 3) + h8] = word;
       }
       sfc[tcol][(row0 + rb) / B] = (uint8_t)code;
+    };
+    // The lane's columns are consecutive, so per 16-row plane it owns
+    // CPL x 8 contiguous bytes of colq: one or two 16-byte stores.
+    auto flush_colq = [&]() {
+#pragma unroll
+      for (int pl = 0; pl < RU / 16; ++pl) {
+        uint8_t *dst = &colq[row0 / 16 + pl][col0 * 8];
+        if (CPL == 4) {
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(cw[0][2 * pl], cw[0][2 * pl + 1],
+                                                       cw[1 % CPL][2 * pl], cw[1 % CPL][2 * pl + 1]);
+          *reinterpret_cast<uint4 *>(dst + 16) =
+              make_uint4(cw[2 % CPL][2 * pl], cw[2 % CPL][2 * pl + 1], cw[3 % CPL][2 * pl],
+                         cw[3 % CPL][2 * pl + 1]);
+        } else {
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(cw[0][2 * pl], cw[0][2 * pl + 1],
+                                                       cw[1 % CPL][2 * pl], cw[1 % CPL][2 * pl + 1]);
+        }
+      }
     };
     auto tile_max_2d = [&](float *bmax, int blk) {
       // B x B tile max: this lane's CPL columns, then the B / CPL lanes of
@@ -314,6 +342,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
             const uint32_t x = w[r][c >> 1];
             return (c & 1) ? bf16_hi(x) : bf16_lo(x);
           });
+        flush_colq();
       }
     } else {
     float v[CPL][RU];
@@ -372,6 +401,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
           emit_col(c, blk * B, bmax[c], [&](int r) { return v[c][r]; });
       }
     }
+    if (p.do_col) flush_colq();
     }
   }
 
@@ -379,19 +409,23 @@ __global__ void __launch_bounds__(kThreads) k_quantize(Params p) {
     __syncthreads();
     if (p.do_row) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) row_pass(i, raw[i]);
+      for (int i = 0; i < 8; ++i) {
+        const int r = 16 * warp + 2 * i + (lane >> 4);
+        row_pass(i, *reinterpret_cast<const uint4 *>(&xs[r][8 * chunk]));
+      }
     }
   }
   __syncthreads();
 
-  // ---- transposed payload: column segments of 64 B leave as 8 B stores
+  // ---- transposed payload: each column's 64 bytes (8 planes x 8 bytes)
+  // leave as 8 consecutive 8-byte stores
   if (p.do_col) {
     for (int idx = threadIdx.x; idx < kTile * 8; idx += kThreads) {
       int col = idx >> 3, part = idx & 7;
       int64_t gcol = C0 + col, grow = R0 + 16 * part;
       if (gcol < C && grow < R) {
         *reinterpret_cast<uint2 *>(p.q_col + gcol * (R / 2) + grow / 2) =
-            *reinterpret_cast<const uint2 *>(&colq[col][8 * part]);
+            *reinterpret_cast<const uint2 *>(&colq[part][8 * col]);
       }
     }
   }

@@ -426,6 +426,8 @@ void orc_sf_to_mma(const uint8_t *sf, int64_t R, int64_t Cb, uint8_t *out) {
 int orc_remap_ue5m3(const uint8_t *sf, const uint8_t *q, int64_t R,
                     int64_t Cb, uint8_t *sf_e4m3, int8_t *shift) {
   int fails = 0;
+  double e4m3_vals[0x7F];
+  for (int k = 0; k <= 0x7E; ++k) e4m3_vals[k] = orc_e4m3_value(k);
   for (int64_t r = 0; r < R; ++r) {
     double vmax = 0.0;
     for (int64_t c = 0; c < Cb; ++c) {
@@ -440,7 +442,7 @@ int orc_remap_ue5m3(const uint8_t *sf, const uint8_t *q, int64_t R,
       double t = ldexp(orc_ue5m3_value(sf[r * Cb + c]), -sh);
       int found = -1;
       for (int k = 0; k <= 0x7E; ++k)
-        if (orc_e4m3_value(k) == t) {
+        if (e4m3_vals[k] == t) {
           found = k;
           break;
         }
