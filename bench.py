@@ -231,21 +231,43 @@ def run_gpu(args, world, rank, local):
     if st != fq.FP4_OK:
         raise RuntimeError("device status after warm-up: " + fq.STATUS_NAMES[st])
     torch.cuda.synchronize()
+    # the whole step captured once as a CUDA graph and replayed
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.step()
+        graph.replay()
+        torch.cuda.synchronize()
     barrier(world)
 
-    per_kernel = {n: 0.0 for n in names[:-1]}
     total_ms = 0.0
     with Clocks(local) as clk:
         for _ in range(args.steps):
             flush.fill_(1)
-            ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
+            s_ev = torch.cuda.Event(enable_timing=True)
+            e_ev = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
-            layer.step(ev)
+            s_ev.record()
+            if graph is not None:
+                graph.replay()
+            else:
+                layer.step()
+            e_ev.record()
             torch.cuda.synchronize()
-            for a, b in zip(names, names[1:]):
-                per_kernel[a] += ev[a].elapsed_time(ev[b])
-            total_ms += ev["amax"].elapsed_time(ev["end"])
+            total_ms += s_ev.elapsed_time(e_ev)
     barrier(world)
+    # per-kernel breakdown: the same steps launched one kernel at a time,
+    # each bracketed by events on the launching stream
+    per_kernel = {n: 0.0 for n in names[:-1]}
+    for _ in range(args.steps):
+        flush.fill_(1)
+        ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
+        torch.cuda.synchronize()
+        layer.step(ev)
+        torch.cuda.synchronize()
+        for a, b in zip(names, names[1:]):
+            per_kernel[a] += ev[a].elapsed_time(ev[b])
     st = fq.fp4_status_sync()
     if st != fq.FP4_OK:
         raise RuntimeError("device status after timed steps: " + fq.STATUS_NAMES[st])
@@ -265,7 +287,7 @@ def run_gpu(args, world, rank, local):
     traffic = load_traffic(dominant)
 
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
-    e2e = run_e2e(layer, args, world, ideal)
+    e2e = run_e2e(layer, args, world, ideal, graph)
 
     clocks = clk.summary()
     out = {
@@ -279,6 +301,7 @@ def run_gpu(args, world, rank, local):
         "config": {"workload": WORKLOAD, "format": FMT_NAMES[args.format],
                    "X": [M_TOK, K_FF], "W": [N_MODEL, K_FF], "dY": [M_TOK, N_MODEL],
                    "amax": "current (D=1 refresh step)", "l2": "flushed before each step",
+                   "launch": "CUDA graph of the whole step" if graph is not None else "eager",
                    "parallelism": f"replicas x{world}"},
         "quantize": {"gbs": round(quant_gbs, 1), "frac": round(quant_gbs / pk["hbm_gbs"], 4),
                      "ms": round(q_ms, 4)},
@@ -301,7 +324,7 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(out))
 
 
-def run_e2e(layer, args, world, ideal):
+def run_e2e(layer, args, world, ideal, graph=None):
     """Same step with host inputs and outputs: pinned H2D copies of X, W, dY,
     the step, and D2H of Y, dX, dW, all inside the timed region."""
     fq = layer.fq
@@ -319,7 +342,10 @@ def run_e2e(layer, args, world, ideal):
         layer.X.copy_(layer.host["X"], non_blocking=True)
         layer.W.copy_(layer.host["W"], non_blocking=True)
         layer.dY.copy_(layer.host["dY"], non_blocking=True)
-        layer.step()
+        if graph is not None:
+            graph.replay()
+        else:
+            layer.step()
         host_out["Y"].copy_(layer.Y, non_blocking=True)
         host_out["dX"].copy_(layer.dX, non_blocking=True)
         host_out["dW"].copy_(layer.dW, non_blocking=True)
@@ -454,6 +480,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--format", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", default=None,
                     choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")

@@ -45,6 +45,38 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
   return r;
 }
 
+// Eight values -> eight nibbles (value j in bits 4j..4j+3) with the same
+// hardware conversion, four conversions packed by one register move.
+__device__ __forceinline__ uint32_t e2m1x8_hw(const float *v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Two independent binary32 products, each rounded to nearest-even
+// (Blackwell packed FP32 multiply); x.lo * m.lo and x.hi * m.hi.
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t x, uint64_t m) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(m));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+// BF16 pair (lo in bits 0..15) widened to a binary32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return ((uint64_t)(w & 0xFFFF0000u) << 32) | (uint64_t)(w << 16);
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
+__device__ __forceinline__ float f32x2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
+
 // Stochastic rounding with 16 random bits r16: between the neighbouring
 // codebook values lo <= |v| < hi, round up iff r16 < 65536 (|v|-lo)/(hi-lo).
 // For |v| in [1, 6) the value sits in a binade with one kept mantissa bit,

@@ -10,15 +10,17 @@
 // K in steps of one 64-element MMA into a binary32 accumulator in tensor
 // memory, the grouping the page's probe-matched model describes.
 //
-// Kernel (one persistent CTA per SM, 192 threads):
+// Kernel (one persistent CTA per SM, 320 threads):
 //   warp 0  TMA producer: per 256-element K step, A [128 x 128 B] and
 //           B [256 x 128 B] payload tiles (128-byte swizzle) by tensor TMA,
 //           plus the matching 512-byte scale tiles by bulk copy;
-//   warp 1  MMA issuer: tcgen05.cp of the scale tiles into tensor memory,
-//           four tcgen05.mma.kind::mxf4nvf4 (M128 N256 K64) per stage,
-//           tcgen05.commit to release the stage / publish the accumulator;
-//   warps 2-5 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator,
-//           shift / canonicalise / alpha, BF16 or binary32 stores.
+//   warp 1  MMA issuer: tcgen05.cp of the scale tiles into a per-stage
+//           tensor-memory slot, four tcgen05.mma.kind::mxf4nvf4 (M128 N256
+//           K64) per stage, tcgen05.commit to release the stage / publish
+//           the accumulator;
+//   warps 2-9 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
+//           (two warps per lane quadrant), release, then shift /
+//           canonicalise / alpha and BF16 or binary32 stores.
 // Every mbarrier wait is bounded (about one second): on expiry the CTA
 // raises the timeout status bit, drains its own copies and MMAs (again
 // bounded), frees its tensor memory and returns.
@@ -27,6 +29,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -67,6 +70,7 @@ struct Params {
   int64_t cp4;     // scale tiles per 128-row group (both operands)
   int64_t ngrp_b;  // 128-row groups of B
   int d_bf16, canon;
+  int stall_producer;  // test switch: the producer never arrives (waits run out)
   uint32_t *status;
 };
 
@@ -108,6 +112,36 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        raise_status(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the MMA-issuing thread.  It polls with the non-blocking
+// test_wait: measured on this part, a potentially blocking try_wait in the
+// thread that issues tcgen05.mma slows the tensor pipe by ~1.7x however
+// rarely it runs, while a test_wait poll costs a few percent.
+__device__ __noinline__ bool mbar_wait_issuer(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag, uint32_t *status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > kTimeoutNs) {
         *abort_flag = 1;
@@ -278,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
-    bool ok = true;
+    bool ok = !p.stall_producer;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
       for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -322,10 +356,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, any = false;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+      if (!mbar_wait_issuer(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
       tc_fence_after();
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+        if (!mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -518,6 +552,11 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   p.d_bf16 = j.d_bf16;
   p.canon = j.canon;
   p.status = status;
+  // Failure-detection test switch: with FP4_TEST_STALL_PRODUCER=1 in the
+  // environment the TMA producer issues nothing, every consumer wait runs
+  // out after about a second, and fp4_status_sync reports FP4_ERR_TIMEOUT.
+  const char *stall = std::getenv("FP4_TEST_STALL_PRODUCER");
+  p.stall_producer = (stall && stall[0] == '1') ? 1 : 0;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

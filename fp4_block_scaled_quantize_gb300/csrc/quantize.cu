@@ -26,12 +26,10 @@
 #include "common.cuh"
 #include "formats.cuh"
 
-// The hardware conversion cvt.rn.satfinite.e2m1x2.f32 was checked against
-// e2m1_rne on every binary32 input (all 2^32 patterns, NaN excluded) and
-// found identical, sign of zero included; it replaces the software encoder.
-#ifndef FP4_HW_E2M1
-#define FP4_HW_E2M1 1
-#endif
+// Nearest-even E2M1 uses the hardware conversion cvt.rn.satfinite.e2m1x2.f32
+// (e2m1x8_hw); it was checked against the threshold encoder e2m1_rne on every
+// binary32 input (all 2^32 patterns, NaN excluded) and found identical, sign
+// of zero included.
 
 namespace fp4 {
 
@@ -72,22 +70,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-// Encode 8 values (already multiplied by the block multiplier) to 8 nibbles,
-// element j in bits [4j, 4j+4).
-__device__ __forceinline__ uint32_t encode8_rne(const float *v) {
-#if FP4_HW_E2M1
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 8; j += 2) w |= e2m1x2_hw(v[j + 1], v[j]) << (4 * j);
-  return w;
-#else
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) w |= e2m1_rne(v[j]) << (4 * j);
-  return w;
-#endif
 }
 
 __device__ __forceinline__ uint32_t encode8_sr(const float *v, const uint4 &bits) {
@@ -225,13 +207,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     float mult;
     bool zp;
     uint32_t code = block_scale_tab<FMT>(b, se_r, mtab_r, mult, zp);
-    scale8(v, mult, zp);
+    if (!zp && !isinf(mult)) {
+      // v = RN32(x * mult), two products per packed multiply
+      const uint64_t mm = pack_f32x2(mult, mult);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(ws[k]), mm);
+        v[2 * k] = f32x2_lo(r2);
+        v[2 * k + 1] = f32x2_hi(r2);
+      }
+    } else {
+      scale8(v, mult, zp);
+    }
     uint32_t word;
     if (p.sr_row) {
       uint64_t g = ((uint64_t)gr * (uint64_t)C + (uint64_t)gc) >> 3;
       word = encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u, g));
     } else {
-      word = encode8_rne(v);
+      word = e2m1x8_hw(v);
     }
     if (gr < R && gc < C) {
       *reinterpret_cast<uint32_t *>(p.q_row + gr * (C / 2) + gc / 2) = word;
@@ -274,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
           uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
           word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
         } else {
-          word = encode8_rne(e);
+          word = e2m1x8_hw(e);
         }
         cw[c][(rb >> 3) + h8] = word;
       }
@@ -336,12 +330,45 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
       }
       if (TWO_D) tile_max_2d(bmax, 0);
       if (p.do_col) {
+        // Column pair (2k, 2k+1) shares each packed word: one f32x2 multiply
+        // scales both columns, each by its own block multiplier.
 #pragma unroll
-        for (int c = 0; c < CPL; ++c)
-          emit_col(c, 0, bmax[c], [&](int r) {
-            const uint32_t x = w[r][c >> 1];
-            return (c & 1) ? bf16_hi(x) : bf16_lo(x);
-          });
+        for (int k = 0; k < WPR; ++k) {
+          float m0, m1;
+          bool z0, z1;
+          const uint32_t code0 = block_scale_tab<FMT>(bmax[2 * k], se_c, mtab_c, m0, z0);
+          const uint32_t code1 = block_scale_tab<FMT>(bmax[2 * k + 1], se_c, mtab_c, m1, z1);
+          const bool fast = !z0 && !z1 && !isinf(m0) && !isinf(m1);
+          const uint64_t mm = pack_f32x2(m0, m1);
+#pragma unroll
+          for (int h8 = 0; h8 < B / 8; ++h8) {
+            float v0[8], v1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t x = w[8 * h8 + j][k];
+              if (fast) {
+                const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(x), mm);
+                v0[j] = f32x2_lo(r2);
+                v1[j] = f32x2_hi(r2);
+              } else {
+                v0[j] = z0 ? 0.0f : scale_elem(bf16_lo(x), m0);
+                v1[j] = z1 ? 0.0f : scale_elem(bf16_hi(x), m1);
+              }
+            }
+            const int trow = row0 + 8 * h8;
+            if (p.sr_col) {
+              const uint64_t g0 = ((uint64_t)(C0 + col0 + 2 * k) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
+              const uint64_t g1 = ((uint64_t)(C0 + col0 + 2 * k + 1) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
+              cw[2 * k][h8] = encode8_sr(v0, sr_group_bits(p.seed, p.offset, 1u, g0));
+              cw[2 * k + 1][h8] = encode8_sr(v1, sr_group_bits(p.seed, p.offset, 1u, g1));
+            } else {
+              cw[2 * k][h8] = e2m1x8_hw(v0);
+              cw[2 * k + 1][h8] = e2m1x8_hw(v1);
+            }
+          }
+          sfc[col0 + 2 * k][row0 / B] = (uint8_t)code0;
+          sfc[col0 + 2 * k + 1][row0 / B] = (uint8_t)code1;
+        }
         flush_colq();
       }
     } else {

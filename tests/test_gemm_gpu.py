@@ -136,6 +136,28 @@ def test_gemm_k_zero_and_empty():
     assert fq.fp4_gemm(A, B, 64, 32, 32, D, 0) == 3  # K % 64 != 0
 
 
+def test_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
+    """Failure detection without a GPU fault: with the producer stalled by the
+    test switch, the MMA and epilogue waits run out after about a second, the
+    kernel returns, fp4_status_sync reports FP4_ERR_TIMEOUT, and the next
+    GEMM on the same context is correct."""
+    need_gpu()
+    M, N, K = 128, 256, 256
+    d = inputs.sweep_operand(M + N, K, seed=1)
+    a = oracle_operand(d[:M], NV)
+    b = oracle_operand(d[M:], NV)
+    A, B = upload(a, NV), upload(b, NV)
+    monkeypatch.setenv("FP4_TEST_STALL_PRODUCER", "1")
+    fq.gemm(A, B)
+    assert fq.fp4_status_sync() == 6  # FP4_ERR_TIMEOUT
+    monkeypatch.delenv("FP4_TEST_STALL_PRODUCER")
+    assert fq.fp4_status_sync() == fq.FP4_OK  # cleared
+    y = fq.gemm(A, B)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    check(y, a, b, NV, K, mm.ravel(), nn.ravel(), name="after timeout")
+
+
 def test_gemm_shape_errors():
     need_gpu()
     q = torch.zeros((128, 64), dtype=torch.uint8, device="cuda")
