@@ -1,0 +1,118 @@
+"""FP4 linear layer: the recipe's forward and backward through the library.
+
+"UE5M3 FP4 Block Scaling for Stable Language Model Pretraining", Approach and
+Developer view:
+  * one held-amax cache per operand (activation X, weight W, gradient dY),
+    refreshed by sample-and-hold every D steps (D = 50 in the recipe, D = 1 is
+    "current" scaling) and deliberately not serialised in checkpoints;
+  * block scale target T (448 by default) with a per-module override for the
+    upstream gradient (T = 2048 on the Wgrad-dY of the four final
+    mixer.down_proj modules);
+  * nearest-even everywhere except stochastic rounding on dY (both backward
+    GEMMs), 2D 16x16 weight tiles so the forward and backward views agree;
+  * fprop Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X on the FP4 tensor
+    cores.
+
+Every computation runs in libfp4gb300.so; this module only allocates
+buffers, keeps the step counter and passes pointers.
+"""
+import torch
+
+from . import (FP4_FMT_UE5M3_B16, FP4_ROUND_SR, FP4_SF_MMA, _check, fp4_amax, gemm, params,
+               quantize_transpose)
+
+
+class AmaxCache:
+    """Held amax of one operand: a device float32 pair (row view, transposed
+    view), refreshed when ``step % D == 0``.  Kept out of ``state_dict`` on
+    purpose: after a restart the first step is a refresh step."""
+
+    def __init__(self, D, device, hadamard_n=0, hadamard_signs=0):
+        if D < 1:
+            raise ValueError("D must be >= 1")
+        self.D = int(D)
+        self.hadamard_n, self.hadamard_signs = hadamard_n, hadamard_signs
+        self.row = torch.zeros(1, dtype=torch.float32, device=device)
+        self.col = torch.zeros(1, dtype=torch.float32, device=device)
+        self.last_refresh = None
+
+    def due(self, step):
+        return self.last_refresh is None or step % self.D == 0
+
+    def update(self, x, step):
+        """Refresh from x on refresh steps; hold otherwise.  Returns True if
+        the cache was refreshed."""
+        if not self.due(step):
+            return False
+        _check(fp4_amax(x, self.hadamard_n, self.hadamard_signs, self.row, self.col), "fp4_amax")
+        self.last_refresh = step
+        return True
+
+
+class _FP4LinearFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, w, mod):
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        mod.cache_x.update(x2, mod.step)
+        mod.cache_w.update(w, mod.step)
+        xr, xc = quantize_transpose(x2, mod.cache_x.row, mod.cache_x.col, mod.p_x)
+        wr, wc = quantize_transpose(w, mod.cache_w.row, mod.cache_w.col, mod.p_w)
+        y = gemm(xr, wr, out_dtype=torch.bfloat16)
+        ctx.x_shape = x.shape
+        ctx.saved = (xc, wc, mod)
+        return y.reshape(*x.shape[:-1], w.shape[0])
+
+    @staticmethod
+    def backward(ctx, dy):
+        xc, wc, mod = ctx.saved
+        dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
+        mod.cache_dy.update(dy2, mod.step)
+        p = mod.p_dy
+        p.sr_offset = mod.step & 0xFFFFFFFF  # fresh random bits every step
+        dyr, dyc = quantize_transpose(dy2, mod.cache_dy.row, mod.cache_dy.col, p)
+        dx = gemm(dyr, wc, out_dtype=torch.bfloat16)   # [M, K]
+        dw = gemm(dyc, xc, out_dtype=torch.float32)    # [N, K]
+        return dx.reshape(ctx.x_shape), dw.to(mod.weight.dtype), None
+
+
+class FP4Linear(torch.nn.Module):
+    """y = x W^T with the FP4 block-scaled recipe (no bias).
+
+    in_features, out_features and the number of tokens per call must be
+    multiples of 64 (the K dimension of every one of the three GEMMs).
+    ``format`` is one of the library's FP4 formats (UE5M3 block 16 by
+    default); ``T_dy`` is the per-module target for the upstream gradient.
+    Call ``next_step()`` once per optimizer step to advance the
+    sample-and-hold clock."""
+
+    def __init__(self, in_features, out_features, D=50, T=448.0, T_dy=None,
+                 format=FP4_FMT_UE5M3_B16, sr_seed=42, device="cuda", dtype=torch.bfloat16):
+        super().__init__()
+        self.in_features, self.out_features = in_features, out_features
+        self.weight = torch.nn.Parameter(
+            torch.empty(out_features, in_features, device=device, dtype=dtype))
+        torch.nn.init.normal_(self.weight, std=0.02)
+        self.step = 0
+        self.cache_x = AmaxCache(D, device)
+        self.cache_w = AmaxCache(D, device)
+        self.cache_dy = AmaxCache(D, device)
+        self.p_x = params(format=format, T=T, sf_layout=FP4_SF_MMA)
+        self.p_w = params(format=format, T=T, block2d=True, sf_layout=FP4_SF_MMA)
+        self.p_dy = params(format=format, T=T_dy if T_dy is not None else T,
+                           round_row=FP4_ROUND_SR, round_col=FP4_ROUND_SR, sr_seed=sr_seed,
+                           sf_layout=FP4_SF_MMA)
+
+    def next_step(self):
+        self.step += 1
+
+    def forward(self, x):
+        if x.dtype != torch.bfloat16:
+            x = x.to(torch.bfloat16)
+        return _FP4LinearFn.apply(x, self.weight.to(torch.bfloat16).contiguous(), self)
+
+    def extra_repr(self):
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"D={self.cache_x.D}")
+
+
+__all__ = ["AmaxCache", "FP4Linear"]

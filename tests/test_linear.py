@@ -1,0 +1,116 @@
+"""FP4Linear: sample-and-hold policy (CPU) and forward / backward against the
+oracle on the GPU ("UE5M3 FP4 Block Scaling for Stable Language Model
+Pretraining", Approach: held amax refreshed every D steps, SR on the upstream
+gradient, 2D weight tiles)."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_quantize_gb300 as fq
+from fp4_block_scaled_quantize_gb300 import inputs
+from fp4_block_scaled_quantize_gb300.linear import AmaxCache, FP4Linear
+import oracle as orc
+from gpu_util import ORC_FMT, f32, need_gpu
+
+UE, NV, MX = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+
+
+def test_sample_and_hold_schedule():
+    c = AmaxCache(50, "cpu")
+    assert c.due(7)                      # nothing held yet: first step refreshes
+    c.last_refresh = 7
+    due = [s for s in range(8, 200) if c.due(s)]
+    assert due == [50, 100, 150]
+    c1 = AmaxCache(1, "cpu")             # D = 1 is current scaling
+    c1.last_refresh = 0
+    assert all(c1.due(s) for s in range(1, 20))
+    with pytest.raises(ValueError):
+        AmaxCache(0, "cpu")
+
+
+def test_amax_cache_not_in_state_dict():
+    m = FP4Linear(128, 64, device="cpu")
+    assert set(m.state_dict().keys()) == {"weight"}
+    assert m.p_w.block2d == 1 and m.p_x.block2d == 0
+    assert m.p_dy.round_row == fq.FP4_ROUND_SR and m.p_dy.round_col == fq.FP4_ROUND_SR
+    m2 = FP4Linear(128, 64, T_dy=2048.0, device="cpu")
+    assert m2.p_dy.T == 2048.0 and m2.p_x.T == 448.0
+    m.next_step()
+    assert m.step == 1
+
+
+# ----------------------------------------------------------------- GPU parity
+
+def _oracle_layer(X, W, dY, fmt, amax_x, amax_w, amax_dy, T_dy, offset):
+    of = ORC_FMT[fmt]
+    x32, w32, dy32 = f32(X), f32(W), f32(dY)
+    ox_r, ox_c = orc.quantize_transpose(x32, amax_x, amax_x, of)
+    ow_r, ow_c = orc.quantize_transpose(w32, amax_w, amax_w, of, block2d=True)
+    ody_r, ody_c = orc.quantize_transpose(dy32, amax_dy, amax_dy, of, T=T_dy, sr_row=True,
+                                          sr_col=True, seed=42, offset=offset)
+    return (ox_r, ow_r), (ody_r, ow_c), (ody_c, ox_c)
+
+
+def _check_bf16(y_gpu, oa, ob, fmt, K, name):
+    """bf16 output of one GEMM against the oracle's probe-matched model
+    rounded to bf16: within one bf16 ulp plus the GEMM tolerance."""
+    Mo, No = y_gpu.shape
+    mm, nn = np.meshgrid(np.arange(Mo), np.arange(No), indexing="ij")
+    y_model, _, s_abs = orc.gemm_model(oa["q"], oa["sf"], ob["q"], ob["sf"], ORC_FMT[fmt], K,
+                                       oa["s_dec"], ob["s_dec"], mm.ravel(), nn.ravel())
+    g = y_gpu.float().cpu().numpy().ravel().astype(np.float64)
+    ym = torch.from_numpy(y_model).to(torch.bfloat16).float().numpy().astype(np.float64)
+    tol = np.abs(ym) * 2.0 ** -8 + 1e-6 * s_abs
+    err = np.abs(g - ym)
+    assert np.all(err <= tol), f"{name}: max err {err.max()} ({np.sum(err > tol)} outside)"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", [UE, NV, MX])
+def test_linear_forward_backward_matches_oracle(fmt):
+    need_gpu()
+    M, K, N = 256, 384, 192
+    d = inputs.down_proj_8b(M=M, K=K, N=N)
+    X, W, dY = d["X"], d["W"], d["dY"]
+    T_dy = 2048.0 if fmt == UE else 448.0
+    lin = FP4Linear(K, N, D=50, T_dy=T_dy, format=fmt)
+    with torch.no_grad():
+        lin.weight.copy_(W.cuda())
+    x = X.cuda().requires_grad_(True)
+    y = lin(x)
+    y.backward(dY.cuda())
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    assert y.dtype == torch.bfloat16 and x.grad.dtype == torch.bfloat16
+    a32 = lambda t: float(np.max(np.abs(f32(t))))
+    fp, dg, wg = _oracle_layer(X, W, dY, fmt, a32(X), a32(W), a32(dY), T_dy, offset=0)
+    _check_bf16(y, *fp, fmt, K, "fprop")
+    _check_bf16(x.grad, *dg, fmt, N, "dgrad")
+    _check_bf16(lin.weight.grad, *wg, fmt, M, "wgrad")
+
+
+@pytest.mark.gpu
+def test_linear_holds_amax_between_refreshes():
+    """Step 1 of a D = 50 schedule quantises with the amax taken at step 0,
+    even though its input doubled; step 50 refreshes."""
+    need_gpu()
+    M, K, N = 128, 256, 128
+    d = inputs.down_proj_8b(M=M, K=K, N=N)
+    X0, W = d["X"], d["W"]
+    X1 = (X0.float() * 2).to(torch.bfloat16)
+    lin = FP4Linear(K, N, D=50, format=UE)
+    with torch.no_grad():
+        lin.weight.copy_(W.cuda())
+        lin(X0.cuda())
+        lin.next_step()
+        y1 = lin(X1.cuda())
+    a0 = float(np.max(np.abs(f32(X0))))
+    aw = float(np.max(np.abs(f32(W))))
+    assert lin.cache_x.last_refresh == 0
+    assert float(lin.cache_x.row.item()) == a0
+    fp, _, _ = _oracle_layer(X1, W, W, UE, a0, aw, aw, 448.0, 0)
+    _check_bf16(y1, *fp, UE, K, "fprop with held amax")
+    lin.step = 50
+    with torch.no_grad():
+        lin(X1.cuda())
+    assert lin.cache_x.last_refresh == 50
+    assert float(lin.cache_x.row.item()) == 2 * a0
