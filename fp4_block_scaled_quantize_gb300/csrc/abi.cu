@@ -177,6 +177,8 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64
       return FP4_ERR_ALIGNMENT;
     if (A->format == FP4_FMT_UE5M3_B16 && (!A->row_shift || !B->row_shift))
       return FP4_ERR_INVALID_ARG;
+    if (A->format == FP4_FMT_UE5M3_B16 && (!aligned16(A->row_shift) || !aligned16(B->row_shift)))
+      return FP4_ERR_ALIGNMENT;
   }
   GemmJob j{};
   j.qa = A->q;

@@ -10,17 +10,29 @@
 // K in steps of one 64-element MMA into a binary32 accumulator in tensor
 // memory, the grouping the page's probe-matched model describes.
 //
-// Kernel (one persistent CTA per SM, 320 threads):
+// Kernel (one persistent CTA per SM, 448 threads):
 //   warp 0  TMA producer: per 256-element K step, A [128 x 128 B] and
 //           B [256 x 128 B] payload tiles (128-byte swizzle) by tensor TMA,
 //           plus the matching 512-byte scale tiles by bulk copy;
-//   warp 1  MMA issuer: tcgen05.cp of the scale tiles into a per-stage
-//           tensor-memory slot, four tcgen05.mma.kind::mxf4nvf4 (M128 N256
-//           K64) per stage, tcgen05.commit to release the stage / publish
-//           the accumulator;
-//   warps 2-9 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
-//           (two warps per lane quadrant), release, then shift /
-//           canonicalise / alpha and BF16 or binary32 stores.
+//   warp 1  MMA issuer: four tcgen05.mma.kind::mxf4nvf4 (M128 N256 K64) per
+//           stage, tcgen05.commit to release the stage / publish the
+//           accumulator;
+//   warps 2-5 scale warps, one per tensor-memory lane quadrant: block-16
+//           scales go from shared memory through registers into the stage's
+//           tensor-memory slot with tcgen05.st (each lane of every quadrant
+//           gets one 16-byte line of each 512-byte scale tile, the image a
+//           four-way broadcast copy leaves); block-32 (E8M0) scales, half as
+//           many, are copied by one thread with tcgen05.cp.  Measured on
+//           this part, tcgen05.cp of block-16 scales queues in the tensor
+//           pipe for about as long as the MMAs that consume them, and a
+//           thread that both copies scales and issues MMAs stalls the pipe at
+//           every barrier poll;
+//   warps 6-13 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
+//           (two warps per lane quadrant, 128 columns each), release, then
+//           shift / canonicalise / alpha and BF16 or binary32 stores.
+// Tiles are walked n-fastest when B is the smaller operand (m-fastest
+// otherwise), so the CTAs of one wave share the streamed panel and the
+// smaller operand stays resident in L2.
 // Every mbarrier wait is bounded (about one second): on expiry the CTA
 // raises the timeout status bit, drains its own copies and MMAs (again
 // bounded), frees its tensor memory and returns.
@@ -49,7 +61,8 @@ constexpr int SFB_BYTES = 2 * 4 * 512;          // two 128-row groups
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 54 KB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quadrant
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SF_WARPS = 4;    // one per tensor-memory lane quadrant
+constexpr int THREADS = 64 + 32 * SF_WARPS + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // 256 binary32 columns
 // Scale factors get their own tensor-memory slot per pipeline stage, so the
@@ -67,6 +80,7 @@ struct Params {
   void *D;
   int64_t M, N, K;
   int m_tiles, n_tiles, k_tiles, k_steps;
+  int n_fast;      // tile order: n fastest (B stays in L2) or m fastest (A stays)
   int64_t cp4;     // scale tiles per 128-row group (both operands)
   int64_t ngrp_b;  // 128-row groups of B
   int d_bf16, canon;
@@ -208,6 +222,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         : "memory");
   }
 }
+__device__ __forceinline__ void tc_st_16cols(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -223,19 +248,6 @@ __device__ __forceinline__ void tc_ld_32cols_nw(uint32_t taddr, uint32_t (&r)[32
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
-      "15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor (tcgen05 format): K-major, 128-byte
 // swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
@@ -271,7 +283,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, drain
+  // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, drain, abort flag,
+  // tensor-memory address, sf_full[STAGES], drain_cp
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * STAGES + 3);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
   const uint32_t bar0 = smem_u32(bars);
@@ -280,6 +293,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
   const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 1);
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 2);
+  auto sf_full = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
+  const uint32_t drain_cp = bar0 + 8u * (3 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -290,6 +305,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 32 * EPI_WARPS);
     mbar_init(drain, 1);
+    mbar_init(drain_cp, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(sf_full(s), FMT == kMXFP4 ? 1 : SF_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -314,9 +331,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = !p.stall_producer;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
+      const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+        if (!mbar_wait_issuer(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -359,22 +377,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait_issuer(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
       tc_fence_after();
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        if (!mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status)) {
+        if (!mbar_wait_issuer(sf_full(stage), phase, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
-        const uint32_t sfa_s = st + A_BYTES + B_BYTES, sfb_s = sfa_s + SFA_BYTES;
         const int nks = min(4, p.k_steps - 4 * kt);
-        const int natoms = (FMT == kMXFP4) ? (nks + 1) / 2 : nks;
         const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
         const uint32_t sfb_t = sfa_t + 16;
-        for (int a = 0; a < natoms; ++a) {
-          tc_cp_sf(sfa_t + 4 * a, desc_sf(sfa_s + 512 * a));
-          tc_cp_sf(sfb_t + 8 * a, desc_sf(sfb_s + 512 * a));
-          tc_cp_sf(sfb_t + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
-        }
         const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
         for (int kk = 0; kk < nks; ++kk) {
           const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
@@ -397,44 +408,142 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_commit(drain);
       mbar_wait_drain(drain, 0);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 2 + SF_WARPS) {
+    // ------------------------------------------------- scale-factor warps
+    // Warp w writes tensor-memory lanes 32 (w % 4) .. +31 of the stage's
+    // scale slot: lane l of every quadrant gets line l of each 512-byte
+    // scale tile (the rows l, l+32, l+64, l+96 in four columns), the same
+    // image a four-way broadcast copy of the tile would leave.
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    if (FMT == kMXFP4) {
+      // block-32 scales: half as many tiles; one thread copies them with
+      // tcgen05.cp straight from shared memory
+      if (warp == 2 && lane == 0) {
+        bool any = false;
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+          for (int kt = 0; kt < p.k_tiles; ++kt) {
+            if (!mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t sfa_s = st + A_BYTES + B_BYTES, sfb_s = sfa_s + SFA_BYTES;
+            const int nks = min(4, p.k_steps - 4 * kt);
+            const int natoms = (nks + 1) / 2;
+            const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
+            const uint32_t sfb_t = sfa_t + 16;
+            for (int a = 0; a < natoms; ++a) {
+              tc_cp_sf(sfa_t + 4 * a, desc_sf(sfa_s + 512 * a));
+              tc_cp_sf(sfb_t + 8 * a, desc_sf(sfb_s + 512 * a));
+              tc_cp_sf(sfb_t + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
+            }
+            tc_commit(sf_full(stage));
+            any = true;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (any) {
+          tc_commit(drain_cp);
+          mbar_wait_drain(drain_cp, 0);
+        }
+      }
+      ok = false;  // the loop below is the block-16 path
+    }
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        int good = 1;
+        if (lane == 0)
+          good = mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status) ? 1 : 0;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t *st = smem + stage * STAGE_BYTES;
+        const uint8_t *sfa_s = st + A_BYTES + B_BYTES;
+        const uint8_t *sfb_s = sfa_s + SFA_BYTES;
+        uint32_t ra[16], rb0[16], rb1[16];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const uint4 va = *reinterpret_cast<const uint4 *>(sfa_s + 512 * a + 16 * lane);
+          const uint4 v0 = *reinterpret_cast<const uint4 *>(sfb_s + 512 * a + 16 * lane);
+          const uint4 v1 = *reinterpret_cast<const uint4 *>(sfb_s + 4 * 512 + 512 * a + 16 * lane);
+          uint32_t *pa = ra + 4 * a;
+          pa[0] = va.x; pa[1] = va.y; pa[2] = va.z; pa[3] = va.w;
+          // B slot: atom a of row group 0 in columns 8a..8a+3, group 1 in 8a+4..8a+7
+          uint32_t *pb = (a < 2 ? rb0 : rb1) + 8 * (a & 1);
+          pb[0] = v0.x; pb[1] = v0.y; pb[2] = v0.z; pb[3] = v0.w;
+          pb[4] = v1.x; pb[5] = v1.y; pb[6] = v1.z; pb[7] = v1.w;
+        }
+        const uint32_t sfa_t = tmem + lane_base + SF_COL0 + SF_SLOT * (uint32_t)stage;
+        const uint32_t sfb_t = sfa_t + 16;
+        tc_st_16cols(sfa_t, ra);
+        tc_st_16cols(sfb_t, rb0);
+        tc_st_16cols(sfb_t + 16, rb1);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_full(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 2 + SF_WARPS) {
     // --------------------------------------------------------------- epilogue
     // Each warp reads its lane quadrant (warp % 4) and one half of the 256
     // accumulator columns into registers, releases the accumulator to the
     // MMA warp, and only then scales, converts and stores -- the stores of
     // tile t overlap the MMAs of tile t + 1.
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
     const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    // B row shifts (int8) of 32 output columns from n0, packed 4 per word;
+    // N is a multiple of 8 and the array is 16-byte aligned.
+    auto load_shifts = [&](int64_t n0, uint32_t(&sh)[8]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t n = n0 + 8 * i;
+        uint2 v = make_uint2(0u, 0u);
+        if (p.shb && n < p.N) v = __ldg(reinterpret_cast<const uint2 *>(p.shb + n));
+        sh[2 * i] = v.x;
+        sh[2 * i + 1] = v.y;
+      }
+    };
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
+      const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
+      // column shifts of the first 64 columns, fetched before the wait
+      const int64_t nbase = (int64_t)nt * BN + 128 * half;
+      uint32_t sh0[8], sh1[8];
+      load_shifts(nbase, sh0);
+      load_shifts(nbase + 32, sh1);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      uint32_t acc[4][32];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
-      tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
       const int64_t m = (int64_t)mt * BM + row_in_tile;
-      if (m >= p.M) continue;
-      const int sa = p.sha ? (int)__ldg(p.sha + m) : 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t(&r)[32] = acc[q];
+      const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
+      auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
-        if (n0 >= p.N) break;
+        if (m >= p.M || n0 >= p.N) return;
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           float v = __uint_as_float(r[j]);
           if (p.shb) {
-            const int64_t n = n0 + j < p.N ? n0 + j : p.N - 1;
-            const int s = sa + (int)__ldg(p.shb + n);
+            const int s = sa + (int)(int8_t)(sh[j >> 2] >> (8 * (j & 3)));
             v = __fmul_rn(v, __uint_as_float((uint32_t)(127 + s) << 23));
           }
           if (p.canon) v = __fmul_rn(rintf(__fmul_rn(v, 1024.0f)), 0x1p-10f);
@@ -464,7 +573,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             *reinterpret_cast<float4 *>(drow + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
           }
         }
-      }
+      };
+      uint32_t acc[4][32];
+      // all 128 columns of this warp's half into registers, then release
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+      emit(0, acc[0], sh0);
+      emit(1, acc[1], sh1);
+      load_shifts(nbase + 64, sh0);
+      load_shifts(nbase + 96, sh1);
+      emit(2, acc[2], sh0);
+      emit(3, acc[3], sh1);
     }
   }
   tc_fence_before();
@@ -545,6 +668,9 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   p.m_tiles = (int)ceil_div(j.M, BM);
   p.n_tiles = (int)ceil_div(j.N, BN);
   p.k_steps = (int)(j.K / 64);
+  // The CTAs of one wave share the operand that varies slowest; keep the
+  // smaller operand resident in L2 and stream the larger one once.
+  p.n_fast = j.M >= j.N ? 1 : 0;
   p.k_tiles = (int)ceil_div(j.K, 256);
   const int blk = (j.fmt == kMXFP4) ? 32 : 16;
   p.cp4 = ceil_div(j.K / blk, 4);

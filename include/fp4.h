@@ -170,7 +170,7 @@ fp4_status fp4_quantize_transpose(
  * 0) or BF16 (nearest-even), row pitch N elements.
  * Shapes: A->rows == M, B->rows == N, A->k == B->k == K, K % 64 == 0, same
  * format on both sides, N % 8 == 0.  K == 0 writes zeros.  Alignment: q, sf,
- * D 16 bytes. */
+ * D and (UE5M3) row_shift 16 bytes. */
 fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M,
                     int64_t N, int64_t K, void *D, int32_t d_is_bf16,
                     int32_t canonicalize_1024, void *stream);

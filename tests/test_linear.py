@@ -58,7 +58,7 @@ def _check_bf16(y_gpu, oa, ob, fmt, K, name):
     mm, nn = np.meshgrid(np.arange(Mo), np.arange(No), indexing="ij")
     y_model, _, s_abs = orc.gemm_model(oa["q"], oa["sf"], ob["q"], ob["sf"], ORC_FMT[fmt], K,
                                        oa["s_dec"], ob["s_dec"], mm.ravel(), nn.ravel())
-    g = y_gpu.float().cpu().numpy().ravel().astype(np.float64)
+    g = y_gpu.detach().float().cpu().numpy().ravel().astype(np.float64)
     ym = torch.from_numpy(y_model).to(torch.bfloat16).float().numpy().astype(np.float64)
     tol = np.abs(ym) * 2.0 ** -8 + 1e-6 * s_abs
     err = np.abs(g - ym)
