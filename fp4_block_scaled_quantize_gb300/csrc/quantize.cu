@@ -55,13 +55,16 @@ struct Params {
   uint32_t offset, signs;
 };
 
-constexpr uint32_t kMag2 = 0x7FFF7FFFu;  // clears the sign bits of two BF16
-
-// Per-half maximum of two pairs of non-negative BF16 (a selection: exact).
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
-                             *reinterpret_cast<const __nv_bfloat162 *>(&b));
-  return *reinterpret_cast<const uint32_t *>(&r);
+// Per-half max(|a|, |b|) of two BF16 pairs (sign bit = xor of the input
+// signs, ignored by every caller; a selection, exact).
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Larger magnitude of the two halves of a BF16 pair, as binary32.
+__device__ __forceinline__ float amax_halves(uint32_t m) {
+  return fmaxf(__uint_as_float((m << 16) & 0x7FFF0000u), __uint_as_float(m & 0x7FFF0000u));
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
@@ -137,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   constexpr int RU = (HAD > B) ? HAD : B;           // rows per column unit
   constexpr int CPL = 64 / RU;                      // columns per lane
   constexpr int NCG = RU / 16;                      // column groups per tile
-  constexpr int LANES_PER_BLOCK = B / 8;            // lanes per row block
 
   // BF16 tile; rows padded by 16 bytes so the two rows of one 16-byte store
   // instruction land in different banks.
@@ -153,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   const int64_t tr = blockIdx.x / p.tiles_c, tc = blockIdx.x % p.tiles_c;
   const int64_t R0 = tr * kTile, C0 = tc * kTile;
   const int64_t R = p.R, C = p.C;
-  const bool need_smem = p.do_col || TWO_D;
 
   float se_r, sd_r, se_c = 1.0f, sd_c = 1.0f;
   tensor_scale<FMT>(__ldg(p.amax_row), p.T, se_r, sd_r);
@@ -173,76 +174,107 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     __syncthreads();
   }
 
-  // ---- load: lane holds 8 BF16 of row 16w + 2i + (lane >> 4)
-  const int chunk = lane & 15;
-  const int64_t gc = C0 + 8 * chunk;
-  uint4 raw[8];
+  // ---- load: lane copies 8 BF16 of row 16w + 2i + (lane >> 4) into the tile
+  {
+    const int chunk = lane & 15;
+    const int64_t gc = C0 + 8 * chunk;
+    uint4 raw[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int r = 16 * warp + 2 * i + (lane >> 4);
-    int64_t gr = R0 + r;
-    if (gr < R && gc < C)
-      raw[i] = ldg_stream(p.x + gr * C + gc);
-    else
-      raw[i] = make_uint4(0, 0, 0, 0);
-    if (need_smem) *reinterpret_cast<uint4 *>(&xs[r][8 * chunk]) = raw[i];
+    for (int i = 0; i < 8; ++i) {
+      const int64_t gr = R0 + 16 * warp + 2 * i + (lane >> 4);
+      raw[i] = (gr < R && gc < C) ? ldg_stream(p.x + gr * C + gc) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4 *>(&xs[16 * warp + 2 * i + (lane >> 4)][8 * chunk]) = raw[i];
   }
+  __syncthreads();
 
-  // ---- row-wise copy (1 x B blocks along C) from registers
-  auto row_pass = [&](int i, const uint4 &w) {
-    int r = 16 * warp + 2 * i + (lane >> 4);
-    int64_t gr = R0 + r;
-    float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-    float b;
-    if (TWO_D) {
-      b = tmax[r / B][chunk / LANES_PER_BLOCK];
-    } else {
-      const uint32_t m = bmax2(bmax2(w.x & kMag2, w.y & kMag2), bmax2(w.z & kMag2, w.w & kMag2));
-      b = fmaxf(bf16_lo(m), bf16_hi(m));
+  // ---- row-wise copy: thread t encodes blocks t, t + 256, ... of the tile
+  // (a block = B consecutive elements of one tile row) from shared memory;
+  // 128 / B consecutive threads cover one row, so a row's payload leaves as
+  // contiguous 8- or 16-byte stores.  Runs after the transposed pass (the 2D
+  // path needs its tile maxima).
+  auto row_pass = [&]() {
+    constexpr int BPR = kTile / B;               // blocks per tile row
+    constexpr int NB = kTile * BPR / kThreads;   // blocks per thread
+    constexpr int NW = B / 2;                    // BF16 pairs per block
 #pragma unroll
-      for (int o = 1; o < LANES_PER_BLOCK; o <<= 1)
-        b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
-    }
-    float mult;
-    bool zp;
-    uint32_t code = block_scale_tab<FMT>(b, se_r, mtab_r, mult, zp);
-    if (!zp && !isinf(mult)) {
-      // v = RN32(x * mult), two products per packed multiply
-      const uint64_t mm = pack_f32x2(mult, mult);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int i = 0; i < NB; ++i) {
+      const int blk = threadIdx.x + kThreads * i;
+      const int r = blk / BPR, bc = blk % BPR;
+      const int64_t gr = R0 + r, gc = C0 + (int64_t)bc * B;
+      uint32_t w[NW];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(ws[k]), mm);
-        v[2 * k] = f32x2_lo(r2);
-        v[2 * k + 1] = f32x2_hi(r2);
+      for (int h = 0; h < B / 8; ++h) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&xs[r][bc * B + 8 * h]);
+        w[4 * h] = v.x;
+        w[4 * h + 1] = v.y;
+        w[4 * h + 2] = v.z;
+        w[4 * h + 3] = v.w;
       }
-    } else {
-      scale8(v, mult, zp);
+      float b;
+      if (TWO_D) {
+        b = tmax[r / B][bc];
+      } else {
+        uint32_t m = amax2(w[0], w[1]);
+#pragma unroll
+        for (int k = 2; k < NW; ++k) m = amax2(m, w[k]);
+        b = amax_halves(m);
+      }
+      float mult;
+      bool zp;
+      const uint32_t code = block_scale_tab<FMT>(b, se_r, mtab_r, mult, zp);
+      uint32_t out[B / 8];
+      if (__any_sync(0xFFFFFFFFu, zp || isinf(mult))) {
+        // a zero-payload block or an infinite multiplier somewhere in the
+        // warp: the careful path (0 * inf read as 0)
+#pragma unroll
+        for (int h = 0; h < B / 8; ++h) {
+          float v[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[2 * k] = bf16_lo(w[4 * h + k]);
+            v[2 * k + 1] = bf16_hi(w[4 * h + k]);
+          }
+          scale8(v, mult, zp);
+          out[h] = p.sr_row ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
+                                                          ((uint64_t)gr * (uint64_t)C +
+                                                           (uint64_t)(gc + 8 * h)) >> 3))
+                            : e2m1x8_hw(v);
+        }
+      } else {
+        // v = RN32(x * mult), two products per packed multiply
+        const uint64_t mm = pack_f32x2(mult, mult);
+#pragma unroll
+        for (int h = 0; h < B / 8; ++h) {
+          float v[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(w[4 * h + k]), mm);
+            v[2 * k] = f32x2_lo(r2);
+            v[2 * k + 1] = f32x2_hi(r2);
+          }
+          out[h] = p.sr_row ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
+                                                          ((uint64_t)gr * (uint64_t)C +
+                                                           (uint64_t)(gc + 8 * h)) >> 3))
+                            : e2m1x8_hw(v);
+        }
+      }
+      if (gr < R && gc < C) {
+        uint8_t *dst = p.q_row + gr * (C / 2) + gc / 2;
+        if (B == 16)
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(out[0], out[1 % (B / 8)]);
+        else
+          *reinterpret_cast<uint4 *>(dst) =
+              make_uint4(out[0], out[1 % (B / 8)], out[2 % (B / 8)], out[3 % (B / 8)]);
+      }
+      sfr[r][bc] = (uint8_t)code;
     }
-    uint32_t word;
-    if (p.sr_row) {
-      uint64_t g = ((uint64_t)gr * (uint64_t)C + (uint64_t)gc) >> 3;
-      word = encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u, g));
-    } else {
-      word = e2m1x8_hw(v);
-    }
-    if (gr < R && gc < C) {
-      *reinterpret_cast<uint32_t *>(p.q_row + gr * (C / 2) + gc / 2) = word;
-    }
-    if ((chunk % LANES_PER_BLOCK) == 0) sfr[r][chunk / LANES_PER_BLOCK] = (uint8_t)code;
   };
 
-  if (p.do_row && !TWO_D) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) row_pass(i, raw[i]);
-  }
-  // the 2D path re-reads its rows from shared memory after the tile maxima
-  // are known instead of keeping them in registers
-  if (need_smem) __syncthreads();
-
   // ---- transposed copy: unit = RU rows x (32 * CPL) columns per warp
-  if (need_smem) {
+  if (p.do_col || TWO_D) {
     const int rg = warp / NCG, cg = warp % NCG;
     const int row0 = rg * RU;
     const int col0 = cg * (32 * CPL) + lane * CPL;
@@ -322,11 +354,11 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
       float bmax[CPL];
 #pragma unroll
       for (int k = 0; k < WPR; ++k) {
-        uint32_t m = 0;
+        uint32_t m = amax2(w[0][k], w[1][k]);
 #pragma unroll
-        for (int r = 0; r < RU; ++r) m = bmax2(m, w[r][k] & kMag2);
-        bmax[2 * k] = bf16_lo(m);
-        bmax[2 * k + 1] = bf16_hi(m);
+        for (int r = 2; r < RU; ++r) m = amax2(m, w[r][k]);
+        bmax[2 * k] = __uint_as_float((m << 16) & 0x7FFF0000u);
+        bmax[2 * k + 1] = __uint_as_float(m & 0x7FFF0000u);
       }
       if (TWO_D) tile_max_2d(bmax, 0);
       if (p.do_col) {
@@ -338,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
           bool z0, z1;
           const uint32_t code0 = block_scale_tab<FMT>(bmax[2 * k], se_c, mtab_c, m0, z0);
           const uint32_t code1 = block_scale_tab<FMT>(bmax[2 * k + 1], se_c, mtab_c, m1, z1);
-          const bool fast = !z0 && !z1 && !isinf(m0) && !isinf(m1);
+          const bool fast = !__any_sync(0xFFFFFFFFu, z0 || z1 || isinf(m0) || isinf(m1));
           const uint64_t mm = pack_f32x2(m0, m1);
 #pragma unroll
           for (int h8 = 0; h8 < B / 8; ++h8) {
@@ -432,17 +464,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     }
   }
 
-  if (TWO_D) {
-    __syncthreads();
-    if (p.do_row) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 16 * warp + 2 * i + (lane >> 4);
-        row_pass(i, *reinterpret_cast<const uint4 *>(&xs[r][8 * chunk]));
-      }
-    }
-  }
-  __syncthreads();
+  if (p.do_col || TWO_D) __syncthreads();  // tile maxima, staged payload, scales
+  if (p.do_row) row_pass();
 
   // ---- transposed payload: each column's 64 bytes (8 planes x 8 bytes)
   // leave as 8 consecutive 8-byte stores
@@ -457,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     }
   }
   // ---- scales
+  __syncthreads();
   if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
   if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
 }

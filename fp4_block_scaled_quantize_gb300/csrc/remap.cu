@@ -34,8 +34,9 @@ __device__ __forceinline__ uint32_t max_byte(uint32_t w) {
 
 constexpr int kWarps = 8;
 
-// Remap one 32-bit word (4 scale columns of one row) given the row's 2^-shift.
-__device__ __forceinline__ uint32_t remap_word(uint32_t w, float inv, int64_t col0, int64_t cb,
+// Remap one 32-bit word (4 scale columns of one row) given the row's 2^-shift
+// (the general path; kept out of line so the common case stays small).
+__device__ __noinline__ uint32_t remap_word(uint32_t w, float inv, int64_t col0, int64_t cb,
                                                const uint8_t *qrow, uint32_t *status) {
   uint32_t out = 0;
 #pragma unroll
@@ -78,7 +79,7 @@ constexpr int kCache = 4;  // tiles per warp held in registers between the passe
 // of rows l, l+32, l+64, l+96.  Warp w of cluster rank c takes tiles
 // 8c + w, 8c + w + 64, ...; per-row maxima meet first in the CTA's shared
 // memory, then across the cluster.
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(32 * kWarps)
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(32 * kWarps, 4)
     k_remap_ue5m3(uint8_t *sf, const uint8_t *q, int64_t rows, int64_t cols, int64_t cb,
                   int64_t cp4, int8_t *shift, uint32_t *status) {
   namespace cg = cooperative_groups;
