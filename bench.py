@@ -358,16 +358,31 @@ def run_e2e(layer, args, world, ideal, graph=None):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def gemm_source_digest():
+    """Short digest of the GEMM kernel source: a traffic figure measured on
+    another version of the kernel is stale."""
+    import hashlib
+    path = os.path.join(ROOT, "fp4_block_scaled_quantize_gb300", "csrc", "gemm.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def load_traffic(kernel):
-    """dram read+write bytes per launch of the dominant kernel from the
-    committed ncu summary (null when absent or stale)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM read+write bytes per launch of one GEMM direction from the
+    committed ncu summary (its `traffic_per_launch` line), or None when the
+    summary is absent or was taken on another version of the kernel."""
+    import re
+    path = os.path.join(ROOT, "profiles", "k_gemm_down_proj_8b_ue5m3.md")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        d = json.load(f)
-    v = d.get(kernel)
-    return None if v is None else v.get("bytes_per_launch")
+        for line in f:
+            if line.startswith("traffic_per_launch"):
+                fields = dict(re.findall(r"(\w+)=(\w+)", line))
+                if fields.get("source") != gemm_source_digest() or kernel not in fields:
+                    return None
+                return int(fields[kernel])
+    return None
 
 
 # ------------------------------------------------------------ CPU oracle arm
