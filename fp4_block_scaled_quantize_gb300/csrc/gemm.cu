@@ -15,18 +15,19 @@
 //           B [256 x 128 B] payload tiles (128-byte swizzle) by tensor TMA,
 //           plus the matching 512-byte scale tiles by bulk copy;
 //   warp 1  MMA issuer: four tcgen05.mma.kind::mxf4nvf4 (M128 N256 K64) per
-//           stage, tcgen05.commit to release the stage / publish the
-//           accumulator;
-//   warps 2-5 scale warps, one per tensor-memory lane quadrant: block-16
-//           scales go from shared memory through registers into the stage's
-//           tensor-memory slot with tcgen05.st (each lane of every quadrant
-//           gets one 16-byte line of each 512-byte scale tile, the image a
-//           four-way broadcast copy leaves); block-32 (E8M0) scales, half as
-//           many, are copied by one thread with tcgen05.cp.  Measured on
-//           this part, tcgen05.cp of block-16 scales queues in the tensor
-//           pipe for about as long as the MMAs that consume them, and a
-//           thread that both copies scales and issues MMAs stalls the pipe at
-//           every barrier poll;
+//           stage from lane 0, tcgen05.commit to release the stage /
+//           publish the accumulator;
+//   warps 2-5 scale warps, one per tensor-memory lane quadrant: once a
+//           stage's tiles have landed, its scales go from shared memory
+//           through registers into the stage's tensor-memory slot with
+//           tcgen05.st (each lane of every quadrant gets one 16-byte line of
+//           each 512-byte scale tile, the image a four-way broadcast copy
+//           leaves).  The stage is then handed to the MMA warp through a
+//           named barrier that also ORs an abort flag across both sides.
+//           Measured on this part: tcgen05.cp of block-16 scales occupies
+//           the tensor pipe about as long as the MMAs that consume them, and
+//           the MMA warp's shared-memory barrier polls stall on a port the
+//           operand reads keep busy;
 //   warps 6-13 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
 //           (two warps per lane quadrant, 128 columns each), release, then
 //           shift / canonicalise / alpha and BF16 or binary32 stores.
@@ -63,6 +64,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barrier
 constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quadrant
 constexpr int SF_WARPS = 4;    // one per tensor-memory lane quadrant
 constexpr int THREADS = 64 + 32 * SF_WARPS + 32 * EPI_WARPS;
+constexpr uint32_t kHandoffThreads = 32 * (1 + SF_WARPS);  // MMA warp + scale warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // 256 binary32 columns
 // Scale factors get their own tensor-memory slot per pipeline stage, so the
@@ -165,6 +167,23 @@ __device__ __noinline__ bool mbar_wait_issuer(uint32_t bar, uint32_t parity,
     }
   }
 }
+// Named barrier `id` over `nthreads` threads (whole warps) that also ORs a
+// predicate across them: the per-stage hand-off between the scale warps and
+// the MMA warp.  A hardware barrier keeps the issuing warp off the shared
+// memory port, which the tensor core's operand reads keep busy; the OR
+// carries an abort from either side, so both sides leave together.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.aligned.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+constexpr uint32_t kHandoffBar = 1;  // barrier 0 is __syncthreads
+
 // Bounded wait used while draining after an abort (no abort check).
 __device__ __noinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -197,10 +216,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
 template <int FMT>
@@ -254,11 +269,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Descriptor of one 512-byte scale tile: 32 rows of 16 bytes, no swizzle.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t addr) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) |
-         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
 // Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, K-major A and B,
 // M = 128, N = 256; scale type E4M3 (block 16) or E8M0 (block 32).
 template <int FMT>
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                               ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
   // bars: full[STAGES], empty[STAGES], acc_full, acc_empty, drain, abort flag,
-  // tensor-memory address, sf_full[STAGES], drain_cp
+  // tensor-memory address
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * STAGES + 3);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
   const uint32_t bar0 = smem_u32(bars);
@@ -293,8 +303,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t acc_full = bar0 + 8u * (2 * STAGES);
   const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 1);
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 2);
-  auto sf_full = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
-  const uint32_t drain_cp = bar0 + 8u * (3 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -305,8 +313,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 32 * EPI_WARPS);
     mbar_init(drain, 1);
-    mbar_init(drain_cp, 1);
-    for (int s = 0; s < STAGES; ++s) mbar_init(sf_full(s), FMT == kMXFP4 ? 1 : SF_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -368,46 +374,54 @@ __global__ void __launch_bounds__(THREADS, 1)
     // make sure no copy into this CTA's shared memory is still in flight
     for (int s = 0; s < STAGES; ++s)
       if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (issued_parity >> s) & 1u);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
+    // The whole warp walks the stages (the hand-off barrier is per warp);
+    // lane 0 issues the tensor-core work.
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
-    bool ok = true, any = false;
-    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      if (!mbar_wait_issuer(acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
-      tc_fence_after();
+    bool abort_seen = false, any = false;
+    for (int tile = blockIdx.x; !abort_seen && tile < ntiles; tile += gridDim.x) {
+      int good = 1;
+      if (lane == 0) good = mbar_wait_issuer(acc_empty, acc_phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+      bool local_abort = __shfl_sync(0xFFFFFFFFu, good, 0) == 0;
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        if (!mbar_wait_issuer(sf_full(stage), phase, abort_flag, p.status)) {
-          ok = false;
+        // scales written and operand tiles landed for this stage (or abort)
+        if (bar_red_or(kHandoffBar, kHandoffThreads, local_abort)) {
+          abort_seen = true;
           break;
         }
-        tc_fence_after();
-        const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
-        const int nks = min(4, p.k_steps - 4 * kt);
-        const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
-        const uint32_t sfb_t = sfa_t + 16;
-        const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
-        for (int kk = 0; kk < nks; ++kk) {
-          const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
-          const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
-          tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id), sfa_t + 4 * a,
-                      sfb_t + 8 * a, (kt | kk) != 0);
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
+          const int nks = min(4, p.k_steps - 4 * kt);
+          const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
+          const uint32_t sfb_t = sfa_t + 16;
+          const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
+          for (int kk = 0; kk < nks; ++kk) {
+            const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
+            const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
+            tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id),
+                        sfa_t + 4 * a, sfb_t + 8 * a, (kt | kk) != 0);
+          }
+          tc_commit(empty_bar(stage));
           any = true;
         }
-        tc_commit(empty_bar(stage));
+        __syncwarp();
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (!ok) break;
-      tc_commit(acc_full);
+      if (abort_seen) break;
+      if (lane == 0) tc_commit(acc_full);
       acc_phase ^= 1u;
     }
-    if (any) {  // all of this thread's tcgen05 operations have completed
+    if (lane == 0 && any) {  // all of this thread's tcgen05 operations have completed
       tc_commit(drain);
       mbar_wait_drain(drain, 0);
     }
+    __syncwarp();
   } else if (warp >= 2 && warp < 2 + SF_WARPS) {
     // ------------------------------------------------- scale-factor warps
     // Warp w writes tensor-memory lanes 32 (w % 4) .. +31 of the stage's
@@ -419,44 +433,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    if (FMT == kMXFP4) {
-      // block-32 scales: half as many tiles; one thread copies them with
-      // tcgen05.cp straight from shared memory
-      if (warp == 2 && lane == 0) {
-        bool any = false;
-        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-          for (int kt = 0; kt < p.k_tiles; ++kt) {
-            if (!mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
-            const uint32_t sfa_s = st + A_BYTES + B_BYTES, sfb_s = sfa_s + SFA_BYTES;
-            const int nks = min(4, p.k_steps - 4 * kt);
-            const int natoms = (nks + 1) / 2;
-            const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
-            const uint32_t sfb_t = sfa_t + 16;
-            for (int a = 0; a < natoms; ++a) {
-              tc_cp_sf(sfa_t + 4 * a, desc_sf(sfa_s + 512 * a));
-              tc_cp_sf(sfb_t + 8 * a, desc_sf(sfb_s + 512 * a));
-              tc_cp_sf(sfb_t + 8 * a + 4, desc_sf(sfb_s + 4 * 512 + 512 * a));
-            }
-            tc_commit(sf_full(stage));
-            any = true;
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        if (any) {
-          tc_commit(drain_cp);
-          mbar_wait_drain(drain_cp, 0);
-        }
-      }
-      ok = false;  // the loop below is the block-16 path
-    }
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         int good = 1;
@@ -464,6 +440,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           good = mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status) ? 1 : 0;
         good = __shfl_sync(0xFFFFFFFFu, good, 0);
         if (!good) {
+          // release the MMA warp at this stage's barrier with the abort set
+          bar_red_or(kHandoffBar, kHandoffThreads, true);
           ok = false;
           break;
         }
@@ -491,8 +469,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_st_16cols(sfb_t + 16, rb1);
         tc_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sf_full(stage));
+        if (bar_red_or(kHandoffBar, kHandoffThreads, false)) {
+          ok = false;
+          break;
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
