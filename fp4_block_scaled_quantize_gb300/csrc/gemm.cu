@@ -263,6 +263,51 @@ __device__ __forceinline__ void tc_ld_32cols_nw(uint32_t taddr, uint32_t (&r)[32
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// Conditional swap (two selects).
+__device__ __forceinline__ void swap_if(bool c, uint32_t &a, uint32_t &b) {
+  const uint32_t t = c ? b : a;
+  b = c ? a : b;
+  a = t;
+}
+// Transpose of 16-byte chunks within each group of four lanes.  On entry
+// lane k (= lane % 4) holds chunks 0..3 (w[4i..4i+3]) of "its" row k of the
+// group; on exit it holds chunk k of rows 0..3 (row r in w[4r..4r+3]).  Two
+// butterfly exchanges (lane distance 2, then 1) and a final reordering.
+__device__ __forceinline__ void transpose4x16B(uint32_t (&w)[16], int k) {
+  const bool b1 = (k & 2) != 0, b0 = (k & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    swap_if(b1, w[j], w[8 + j]);
+    swap_if(b1, w[4 + j], w[12 + j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[8 + j] = __shfl_xor_sync(0xFFFFFFFFu, w[8 + j], 2);
+    w[12 + j] = __shfl_xor_sync(0xFFFFFFFFu, w[12 + j], 2);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    swap_if(b0, w[j], w[4 + j]);
+    swap_if(b0, w[8 + j], w[12 + j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[4 + j] = __shfl_xor_sync(0xFFFFFFFFu, w[4 + j], 1);
+    w[12 + j] = __shfl_xor_sync(0xFFFFFFFFu, w[12 + j], 1);
+  }
+  // slot s now holds row k ^ s; move row r to slot r
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    swap_if(b0, w[j], w[4 + j]);
+    swap_if(b0, w[8 + j], w[12 + j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    swap_if(b1, w[j], w[8 + j]);
+    swap_if(b1, w[4 + j], w[12 + j]);
+  }
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): K-major, 128-byte
 // swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
@@ -515,9 +560,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
       const int64_t m = (int64_t)mt * BM + row_in_tile;
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
+      // Output: each lane's row segment of 32 values is exchanged within its
+      // group of four lanes so that every store instruction writes eight
+      // 64-byte row pieces instead of 32 scattered 16-byte pieces.
+      const int k4 = lane & 3;
+      const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
-        if (m >= p.M || n0 >= p.N) return;
+        if (n0 >= p.N) return;  // warp-uniform
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -530,27 +580,35 @@ __global__ void __launch_bounds__(THREADS, 1)
           y[j] = __fmul_rn(v, alpha);
         }
         if (p.d_bf16) {
-          __nv_bfloat16 *drow = reinterpret_cast<__nv_bfloat16 *>(p.D) + m * p.N + n0;
+          uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            if (n0 + j >= p.N) break;
-            uint4 w;
-            w.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 1])) << 16);
-            w.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 2])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 3])) << 16);
-            w.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 4])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 5])) << 16);
-            w.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 6])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[j + 7])) << 16);
-            *reinterpret_cast<uint4 *>(drow + j) = w;
+          for (int j = 0; j < 16; ++j)
+            w[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[2 * j])) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y[2 * j + 1])) << 16);
+          transpose4x16B(w, k4);
+          const int64_t n = n0 + 8 * k4;
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int64_t mm = grp_m + rr;
+            if (mm < p.M && n < p.N)
+              *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.D) + mm * p.N + n) =
+                  make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]);
           }
         } else {
-          float *drow = reinterpret_cast<float *>(p.D) + m * p.N + n0;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            if (n0 + j >= p.N) break;
-            *reinterpret_cast<float4 *>(drow + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+          for (int u = 0; u < 2; ++u) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(y[16 * u + j]);
+            transpose4x16B(w, k4);
+            const int64_t n = n0 + 16 * u + 4 * k4;
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int64_t mm = grp_m + rr;
+              if (mm < p.M && n < p.N)
+                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.D) + mm * p.N + n) =
+                    make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]);
+            }
           }
         }
       };
