@@ -9,14 +9,17 @@
 // "Technical summary: LLM pretraining with MXFP4", Findings: deterministic
 // H16 / H32 rotation on the weight-gradient (transposed) copy.
 //
-// Design (one CTA of 256 threads per 128 x 128 BF16 tile, HBM-bound):
-//  * loads: 16 B per lane; warp w owns tile rows 16w..16w+15, two rows per
-//    load instruction (16 lanes x 16 B = one 256 B row), so each lane holds
-//    one half of a 16-element row block -- the row-wise copy is computed
-//    straight from registers (block max = one shuffle).
-//  * the transposed copy reads the tile back from shared memory column-wise:
-//    each lane owns 64 values (4 columns x 16 rows, or 2 x 32 with a 32-row
-//    rotation / block); 8-byte row-contiguous reads are conflict-free.
+// Design (persistent, three CTAs of 256 threads per SM, 128 x 128 BF16 tiles,
+// HBM-bound): tensor scales and the per-code multiplier tables are set up
+// once per CTA, which then walks tiles with a stride of the grid.
+//  * loads: 16 B per lane (warp w owns tile rows 16w..16w+15, two rows per
+//    load instruction), staged in shared memory (rows padded by 16 bytes).
+//  * the transposed copy reads the tile column-wise: each lane owns 64
+//    values (4 columns x 16 rows, or 2 x 32 with a 32-row rotation / block);
+//    8-byte row-contiguous reads are conflict-free; block maxima by packed
+//    max.xorsign.abs on BF16 pairs.
+//  * the row-wise copy then encodes one block per thread from shared memory
+//    (so the 2D path can use the tile maxima of the transposed pass).
 //  * transposed payload bytes are staged in shared memory so every column
 //    segment leaves as contiguous 8-byte stores; scales leave as whole
 //    512-byte tensor-core tiles (or plain rows).
@@ -43,7 +46,7 @@ constexpr int kColqPitch = kTile * 8 + 32;     // bytes per 16-row plane
 struct Params {
   const uint16_t *x;
   int64_t R, C;
-  int64_t tiles_c;
+  int64_t tiles_r, tiles_c;
   const float *amax_row, *amax_col;
   float T;
   uint8_t *q_row, *sf_row;
@@ -152,9 +155,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   __shared__ float tmax[8][8];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tr = blockIdx.x / p.tiles_c, tc = blockIdx.x % p.tiles_c;
-  const int64_t R0 = tr * kTile, C0 = tc * kTile;
   const int64_t R = p.R, C = p.C;
+  const int64_t ntiles = p.tiles_r * p.tiles_c;
 
   float se_r, sd_r, se_c = 1.0f, sd_c = 1.0f;
   tensor_scale<FMT>(__ldg(p.amax_row), p.T, se_r, sd_r);
@@ -174,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     __syncthreads();
   }
 
+  // Persistent: the tensor scales and multiplier tables above are set up
+  // once per CTA; the CTA then walks tiles with a stride of the grid.
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+  const int64_t R0 = (tile / p.tiles_c) * kTile, C0 = (tile % p.tiles_c) * kTile;
   // ---- load: lane copies 8 BF16 of row 16w + 2i + (lane >> 4) into the tile
   {
     const int chunk = lane & 15;
@@ -483,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   __syncthreads();
   if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
   if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
+  __syncthreads();  // the tile and staging buffers are reused by the next tile
+  }  // tile loop
 }
 
 // s_dec only (empty tensors).
@@ -502,7 +510,18 @@ __global__ void k_scale_only(const float *amax_row, const float *amax_col, float
 
 template <int FMT, int HAD, bool TWO_D>
 fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
-  k_quantize<FMT, HAD, TWO_D><<<(unsigned)tiles, kThreads, 0, s>>>(p);
+  // three resident CTAs per SM, each walking tiles
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4_ERR_CUDA;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return FP4_ERR_CUDA;
+    sms[dev] = n;
+  }
+  const int64_t cap = 3 * (int64_t)sms[dev];
+  k_quantize<FMT, HAD, TWO_D><<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -548,9 +567,9 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
     }
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
   }
-  const int64_t tiles_r = ceil_div(j.R, kTile);
+  p.tiles_r = ceil_div(j.R, kTile);
   p.tiles_c = ceil_div(j.C, kTile);
-  const int64_t tiles = tiles_r * p.tiles_c;
+  const int64_t tiles = p.tiles_r * p.tiles_c;
   const bool two_d = j.block2d != 0;
   const int had = p.do_col ? j.had_n : 0;
   fp4_status st;
