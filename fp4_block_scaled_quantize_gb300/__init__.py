@@ -49,8 +49,8 @@ class FP4Error(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_sf_bytes",
-           "fp4_block_size", "fp4_status_sync", "fp4_status_string")
+EXPORTS = ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
+           "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync", "fp4_status_string")
 
 
 def lib():
@@ -69,6 +69,7 @@ def lib():
         L.fp4_quantize_transpose.argtypes = [vp, i64, i64, vp, vp, qp, vp, vp, vp, vp, vp, vp, vp,
                                              vp, vp]
         L.fp4_gemm.argtypes = [op, op, i64, i64, i64, vp, i32, i32, vp]
+        L.fp4_gemm_quantize.argtypes = [op, op, i64, i64, i64, vp, qp, vp, vp, vp, vp, i32, vp]
         L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
         L.fp4_sf_bytes.restype = i64
         L.fp4_block_size.argtypes = [i32]
@@ -77,7 +78,7 @@ def lib():
         L.fp4_status_string.argtypes = [i32]
         L.fp4_status_string.restype = ctypes.c_char_p
         for f in ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
-                  "fp4_status_sync"):
+                  "fp4_gemm_quantize", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -132,6 +133,13 @@ def fp4_quantize_transpose(x, amax_row, amax_col, p, q_row, sf_row, s_dec_row, s
 def fp4_gemm(A, B, M, N, K, D, d_is_bf16, canonicalize_1024=0, stream=None):
     return lib().fp4_gemm(ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(D), int(d_is_bf16),
                           int(canonicalize_1024), _stream(stream))
+
+
+def fp4_gemm_quantize(A, B, M, N, K, amax, p, q, sf, s_dec, row_shift=None, canonicalize_1024=0,
+                      stream=None):
+    return lib().fp4_gemm_quantize(ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(amax),
+                                   ctypes.byref(p), _ptr(q), _ptr(sf), _ptr(s_dec), _ptr(row_shift),
+                                   int(canonicalize_1024), _stream(stream))
 
 
 def fp4_sf_bytes(format, rows, cols, layout):
@@ -224,3 +232,14 @@ def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, strea
     _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
                     canonicalize_1024, stream), "fp4_gemm")
     return D
+
+
+def gemm_quantize(a, b, amax_dev, p, remap=True, canonicalize_1024=False, stream=None):
+    """Row-wise FP4 copy of y = alpha * A B^T, quantised in the GEMM epilogue
+    (the product is never stored).  Returns a Quantized of y [M, N]."""
+    M, N, K = a.rows, b.rows, a.k
+    out = _alloc_copy(M, N, p, a.q.device, _want_shift(p, remap))
+    _check(fp4_gemm_quantize(a.operand(), b.operand(), M, N, K, amax_dev, p, out.q, out.sf,
+                             out.s_dec, out.row_shift, canonicalize_1024, stream),
+           "fp4_gemm_quantize")
+    return out

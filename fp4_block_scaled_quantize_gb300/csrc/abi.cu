@@ -162,25 +162,20 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   return launch_quantize(j, as_stream(stream));
 }
 
-fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N, int64_t K,
-                    void *D, int32_t d_is_bf16, int32_t canonicalize_1024, void *stream) {
-  if (!A || !B || M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
-  if (!valid_format(A->format) || A->format != B->format) return FP4_ERR_INVALID_ARG;
-  if (A->rows != M || B->rows != N || A->k != K || B->k != K) return FP4_ERR_SHAPE;
-  if (K % 64 != 0 || N % 8 != 0) return FP4_ERR_SHAPE;
-  if (M == 0 || N == 0) return FP4_OK;
-  if (!D) return FP4_ERR_INVALID_ARG;
-  if (!aligned16(D)) return FP4_ERR_ALIGNMENT;
-  if (K > 0) {
-    if (!A->q || !A->sf || !B->q || !B->sf || !A->s_dec || !B->s_dec) return FP4_ERR_INVALID_ARG;
-    if (!aligned16(A->q) || !aligned16(A->sf) || !aligned16(B->q) || !aligned16(B->sf))
-      return FP4_ERR_ALIGNMENT;
-    if (A->format == FP4_FMT_UE5M3_B16 && (!A->row_shift || !B->row_shift))
-      return FP4_ERR_INVALID_ARG;
-    if (A->format == FP4_FMT_UE5M3_B16 && (!aligned16(A->row_shift) || !aligned16(B->row_shift)))
-      return FP4_ERR_ALIGNMENT;
-  }
-  GemmJob j{};
+}  // extern "C"
+
+namespace {
+
+// Operand checks shared by the two GEMM entry points (K > 0 here).
+fp4_status gemm_operands(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
+                         int64_t K, GemmJob &j) {
+  if (!A->q || !A->sf || !B->q || !B->sf || !A->s_dec || !B->s_dec) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(A->q) || !aligned16(A->sf) || !aligned16(B->q) || !aligned16(B->sf))
+    return FP4_ERR_ALIGNMENT;
+  if (A->format == FP4_FMT_UE5M3_B16 && (!A->row_shift || !B->row_shift))
+    return FP4_ERR_INVALID_ARG;
+  if (A->format == FP4_FMT_UE5M3_B16 && (!aligned16(A->row_shift) || !aligned16(B->row_shift)))
+    return FP4_ERR_ALIGNMENT;
   j.qa = A->q;
   j.sfa = A->sf;
   j.qb = B->q;
@@ -193,9 +188,76 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64
   j.M = M;
   j.N = N;
   j.K = K;
+  return FP4_OK;
+}
+
+fp4_status gemm_shapes(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
+                       int64_t K) {
+  if (!A || !B || M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+  if (!valid_format(A->format) || A->format != B->format) return FP4_ERR_INVALID_ARG;
+  if (A->rows != M || B->rows != N || A->k != K || B->k != K) return FP4_ERR_SHAPE;
+  if (K % 64 != 0 || N % 8 != 0) return FP4_ERR_SHAPE;
+  return FP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N, int64_t K,
+                    void *D, int32_t d_is_bf16, int32_t canonicalize_1024, void *stream) {
+  fp4_status st = gemm_shapes(A, B, M, N, K);
+  if (st != FP4_OK) return st;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!D) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(D)) return FP4_ERR_ALIGNMENT;
+  GemmJob j{};
+  if (K > 0) {
+    st = gemm_operands(A, B, M, N, K, j);
+    if (st != FP4_OK) return st;
+  }
+  j.M = M;
+  j.N = N;
+  j.K = K;
+  j.fmt = A->format;
   j.D = D;
   j.d_bf16 = d_is_bf16 != 0;
   j.canon = canonicalize_1024 != 0;
+  return launch_gemm(j, as_stream(stream));
+}
+
+fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
+                             int64_t K, const float *amax_dev, const fp4_quant_params *p,
+                             uint8_t *q, uint8_t *sf, float *s_dec_dev, int8_t *row_shift,
+                             int32_t canonicalize_1024, void *stream) {
+  fp4_status st = gemm_shapes(A, B, M, N, K);
+  if (st != FP4_OK) return st;
+  st = check_params(p);
+  if (st != FP4_OK) return st;
+  if (p->block2d || p->hadamard_n || p->round_col != FP4_ROUND_RNE) return FP4_ERR_UNSUPPORTED;
+  if (row_shift && !(p->format == FP4_FMT_UE5M3_B16 && p->sf_layout == FP4_SF_MMA))
+    return FP4_ERR_UNSUPPORTED;
+  if (K == 0 || N % block_of(p->format) != 0) return FP4_ERR_SHAPE;
+  if (!amax_dev || !s_dec_dev) return FP4_ERR_INVALID_ARG;
+  if (!aligned4(amax_dev) || !aligned4(s_dec_dev)) return FP4_ERR_ALIGNMENT;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!q || !sf) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(sf)) return FP4_ERR_ALIGNMENT;
+  GemmJob j{};
+  st = gemm_operands(A, B, M, N, K, j);
+  if (st != FP4_OK) return st;
+  j.canon = canonicalize_1024 != 0;
+  j.q_out = q;
+  j.sf_out = sf;
+  j.sd_out = s_dec_dev;
+  j.shift_out = row_shift;
+  j.amax_out = amax_dev;
+  j.T_out = p->T;
+  j.fmt_out = p->format;
+  j.sr_out = p->round_row == FP4_ROUND_SR;
+  j.sf_mma_out = p->sf_layout == FP4_SF_MMA;
+  j.seed_out = p->sr_seed;
+  j.offset_out = p->sr_offset;
   return launch_gemm(j, as_stream(stream));
 }
 

@@ -70,6 +70,15 @@ struct GemmJob {
   int64_t M, N, K;
   void *D;
   int d_bf16, canon;
+  // fused row-wise quantisation of the output (q_out != nullptr): D unused
+  uint8_t *q_out, *sf_out;
+  float *sd_out;
+  int8_t *shift_out;
+  const float *amax_out;
+  float T_out;
+  int fmt_out, sr_out, sf_mma_out;
+  uint64_t seed_out;
+  uint32_t offset_out;
 };
 fp4_status launch_gemm(const GemmJob &j, cudaStream_t s);
 

@@ -284,4 +284,27 @@ __device__ __forceinline__ uint32_t sr_r16(const uint4 &w, int j) {
   return (word >> (16 * (j & 1))) & 0xFFFFu;
 }
 
+// Eight stochastically rounded E2M1 codes (value j in bits 4j..4j+3) from
+// the group's random bits.
+__device__ __forceinline__ uint32_t encode8_sr(const float *v, const uint4 &bits) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w |= e2m1_sr(v[j], sr_r16(bits, j)) << (4 * j);
+  return w;
+}
+
+// Scale 8 values of a block by mult (0 * inf read as 0; zero payload -> 0).
+__device__ __forceinline__ void scale8(float *v, float mult, bool zero_payload) {
+  if (zero_payload) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+  } else if (isinf(mult)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = scale_elem(v[j], mult);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], mult);
+  }
+}
+
 }  // namespace fp4

@@ -88,6 +88,15 @@ struct Params {
   int d_bf16, canon;
   int stall_producer;  // test switch: the producer never arrives (waits run out)
   uint32_t *status;
+  // fused row-wise quantisation of the output (q_out != nullptr)
+  uint8_t *q_out, *sf_out;
+  float *sd_out;
+  const float *amax_out;
+  float T_out;
+  int fmt_out, sr_out, sf_mma_out, qb_out;
+  int64_t cb_out, cp4_out;  // output scale columns; 512-byte tiles per 128 rows
+  uint64_t seed_out;
+  uint32_t offset_out;
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -263,6 +272,23 @@ __device__ __forceinline__ void tc_ld_32cols_nw(uint32_t taddr, uint32_t (&r)[32
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// Format chosen at run time (the fused epilogue quantiser).
+__device__ __forceinline__ void tensor_scale_rt(int fmt, float amax, float T, float &se,
+                                                float &sd) {
+  if (fmt == kMXFP4)
+    tensor_scale<kMXFP4>(amax, T, se, sd);
+  else if (fmt == kUE5M3)
+    tensor_scale<kUE5M3>(amax, T, se, sd);
+  else
+    tensor_scale<kNVFP4>(amax, T, se, sd);
+}
+__device__ __forceinline__ uint32_t block_scale_rt(int fmt, float b, float se, float sd,
+                                                   float &mult, bool &zp) {
+  if (fmt == kMXFP4) return block_scale<kMXFP4>(b, se, sd, mult, zp);
+  if (fmt == kUE5M3) return block_scale<kUE5M3>(b, se, sd, mult, zp);
+  return block_scale<kNVFP4>(b, se, sd, mult, zp);
+}
+
 // Conditional swap (two selects).
 __device__ __forceinline__ void swap_if(bool c, uint32_t &a, uint32_t &b) {
   const uint32_t t = c ? b : a;
@@ -329,7 +355,7 @@ __device__ __forceinline__ uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
   return d;
 }
 
-template <int FMT>
+template <int FMT, bool QOUT>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
            const Params p) {
@@ -534,6 +560,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
     const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    float se_o = 1.0f, sd_o = 1.0f;  // tensor scale of the fused output copy
+    if (QOUT) {
+      tensor_scale_rt(p.fmt_out, __ldg(p.amax_out), p.T_out, se_o, sd_o);
+      if (blockIdx.x == 0 && threadIdx.x == 32 * (2 + SF_WARPS)) *p.sd_out = sd_o;
+    }
     // B row shifts (int8) of 32 output columns from n0, packed 4 per word;
     // N is a multiple of 8 and the array is 16-byte aligned.
     auto load_shifts = [&](int64_t n0, uint32_t(&sh)[8]) {
@@ -565,6 +596,49 @@ __global__ void __launch_bounds__(THREADS, 1)
       // 64-byte row pieces instead of 32 scattered 16-byte pieces.
       const int k4 = lane & 3;
       const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
+      // Fused producer: the row-wise FP4 copy of this lane's 32 output values
+      // (one or two blocks along N), in place of the stores of y.
+      auto quant_out = [&](int64_t n0, const float(&y)[32]) {
+        if (m >= p.M) return;
+        const int nb = 32 / p.qb_out;
+        uint32_t w[4];
+        uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          if (blk >= nb || n0 + blk * p.qb_out >= p.N) break;
+          const int QB = p.qb_out, o = blk * QB;
+          float b = 0.0f;
+          for (int j = 0; j < QB; ++j) b = fmaxf(b, fabsf(y[o + j]));
+          float mult;
+          bool zp;
+          codes[blk] = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
+          for (int h = 0; h < QB / 8; ++h) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
+            scale8(v, mult, zp);
+            const int64_t n = n0 + o + 8 * h;
+            w[2 * blk + h] =
+                p.sr_out ? encode8_sr(v, sr_group_bits(p.seed_out, p.offset_out, 0u,
+                                                       ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 3))
+                         : e2m1x8_hw(v);
+          }
+        }
+        uint8_t *qrow = p.q_out + m * (p.N / 2) + n0 / 2;
+        *reinterpret_cast<uint2 *>(qrow) = make_uint2(w[0], w[1]);
+        if (n0 + 16 < p.N) *reinterpret_cast<uint2 *>(qrow + 8) = make_uint2(w[2], w[3]);
+        for (int blk = 0; blk < nb; ++blk) {
+          const int64_t col = n0 / p.qb_out + blk;
+          if (col >= p.cb_out) break;
+          int64_t off;
+          if (p.sf_mma_out)
+            off = ((m >> 7) * p.cp4_out + (col >> 2)) * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4 +
+                  (col & 3);
+          else
+            off = m * p.cb_out + col;
+          p.sf_out[off] = (uint8_t)codes[blk];
+        }
+      };
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform
@@ -578,6 +652,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (p.canon) v = __fmul_rn(rintf(__fmul_rn(v, 1024.0f)), 0x1p-10f);
           y[j] = __fmul_rn(v, alpha);
+        }
+        if (QOUT) {
+          quant_out(n0, y);
+          return;
         }
         if (p.d_bf16) {
           uint32_t w[16];
@@ -665,17 +743,17 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
   return r == CUDA_SUCCESS;
 }
 
-template <int FMT>
+template <int FMT, bool QOUT>
 fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int grid,
                       cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(k_gemm<FMT, QOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
-  k_gemm<FMT><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  k_gemm<FMT, QOUT><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -726,8 +804,37 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  if (j.fmt == kMXFP4) return launch_fmt<kMXFP4>(ma, mb, p, grid, s);
-  return launch_fmt<kNVFP4>(ma, mb, p, grid, s);
+  if (j.q_out) {
+    p.q_out = j.q_out;
+    p.sf_out = j.sf_out;
+    p.sd_out = j.sd_out;
+    p.amax_out = j.amax_out;
+    p.T_out = j.T_out;
+    p.fmt_out = j.fmt_out;
+    p.sr_out = j.sr_out;
+    p.sf_mma_out = j.sf_mma_out;
+    p.seed_out = j.seed_out;
+    p.offset_out = j.offset_out;
+    p.qb_out = j.fmt_out == kMXFP4 ? 32 : 16;
+    p.cb_out = j.N / p.qb_out;
+    p.cp4_out = ceil_div(p.cb_out, 4);
+    // tensor-core layout: padding rows and scale columns read as zero
+    if (j.sf_mma_out &&
+        cudaMemsetAsync(j.sf_out, 0, (size_t)(ceil_div(j.M, 128) * 128 * p.cp4_out * 4), s) !=
+            cudaSuccess)
+      return FP4_ERR_CUDA;
+  }
+  fp4_status st;
+  if (j.q_out)
+    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, true>(ma, mb, p, grid, s)
+                           : launch_fmt<kNVFP4, true>(ma, mb, p, grid, s);
+  else
+    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, false>(ma, mb, p, grid, s)
+                           : launch_fmt<kNVFP4, false>(ma, mb, p, grid, s);
+  if (st != FP4_OK || !j.q_out) return st;
+  if (j.fmt_out == kUE5M3 && j.sf_mma_out && j.shift_out)
+    return launch_remap_ue5m3(j.sf_out, j.q_out, j.M, j.N, j.shift_out, s);
+  return FP4_OK;
 }
 
 }  // namespace fp4

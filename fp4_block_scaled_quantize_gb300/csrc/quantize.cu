@@ -78,27 +78,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t encode8_sr(const float *v, const uint4 &bits) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) w |= e2m1_sr(v[j], sr_r16(bits, j)) << (4 * j);
-  return w;
-}
-
-// Scale a block of 8 values by mult (0 * inf read as 0; zero payload -> 0).
-__device__ __forceinline__ void scale8(float *v, float mult, bool zero_payload) {
-  if (zero_payload) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-  } else if (isinf(mult)) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = scale_elem(v[j], mult);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], mult);
-  }
-}
-
 // Write one copy's scales for this tile.  sfs[r][j] holds the codes of tile
 // row r (copy rows r0 + r) and scale columns c0b + j; `rows_valid` and
 // `cols_valid` bound the real part (the rest is padding, written as 0 in the

@@ -175,6 +175,28 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M,
                     int64_t N, int64_t K, void *D, int32_t d_is_bf16,
                     int32_t canonicalize_1024, void *stream);
 
+/* GEMM with the next consumer's producer fused into its epilogue ([FAF]
+ * Abstract: format-aware fusion -- the producer runs where the data already
+ * is, saving the output's round trip through HBM).  The product
+ * y = alpha * A B^T is formed exactly as fp4_gemm forms its binary32 output
+ * (d_is_bf16 == 0, same canonicalize_1024), and, instead of being stored,
+ * its row-wise copy is quantised exactly as fp4_quantize quantises a
+ * binary32 input: tensor scale from the held amax *amax_dev and p->T, one
+ * scale per p->format block along N, RNE or (p->round_row == SR) Philox
+ * stochastic rounding with counter group (m N + n) >> 3 and copy 0,
+ * zero-scale rule, scales in p->sf_layout; UE5M3 with the MMA layout and a
+ * non-NULL row_shift is remapped onto E4M3 as in fp4_quantize.  Only the
+ * row-wise copy is produced (block2d, hadamard_n and round_col must be 0).
+ * Outputs: q [M][N/2], sf (fp4_sf_bytes(p->format, M, N, p->sf_layout)),
+ * s_dec_dev (one float), row_shift [M] (UE5M3 + MMA layout only).
+ * Shapes: as fp4_gemm, and N % B == 0.  Alignment: q, sf, operands 16
+ * bytes.  Errors as fp4_gemm; K > 0 (K == 0 returns FP4_ERR_SHAPE). */
+fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t M,
+                             int64_t N, int64_t K, const float *amax_dev,
+                             const fp4_quant_params *p, uint8_t *q, uint8_t *sf,
+                             float *s_dec_dev, int8_t *row_shift,
+                             int32_t canonicalize_1024, void *stream);
+
 /* Bytes of one scale-factor output for a copy with `rows` rows and `cols`
  * elements per row; -1 for an invalid format/layout. */
 int64_t fp4_sf_bytes(int32_t format, int64_t rows, int64_t cols,
