@@ -289,6 +289,7 @@ def run_gpu(args, world, rank, local):
     traffic = load_traffic(dominant)
 
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
+    fused = run_fused_producer(layer, flush)
     e2e = run_e2e(layer, args, world, ideal, graph)
 
     clocks = clk.summary()
@@ -320,10 +321,70 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks,
         "gpu_launches": layer.launches_per_step * args.steps,
         "e2e": e2e,
+        "epilogue_fused_producer": fused,
     }
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(args, ideal)
         print(json.dumps(out))
+
+
+def graph_ms(fn, flush, reps=20):
+    """Device time of fn() per call: CUDA graphs of [L2 flush, fn] and of
+    [L2 flush] alone, replayed back to back, difference of the two."""
+    def cap(with_fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            flush.fill_(1)
+            if with_fn:
+                fn()
+        return g
+
+    def t(g):
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    return t(cap(True)) - t(cap(False))
+
+
+def run_fused_producer(layer, flush):
+    """fprop with the next layer's producer fused into the GEMM epilogue
+    (fp4_gemm_quantize: the row-wise FP4 copy of Y is written instead of Y)
+    against the unfused pair (BF16 Y written, then read back by
+    fp4_quantize).  Held amax of Y from a previous step."""
+    fq = layer.fq
+    fq.gemm(layer.xr, layer.wr, out=layer.Y)
+    amax_y, _ = fq.amax(layer.Y)
+    p = fq.params(format=layer.fmt, T=448.0, sf_layout=fq.FP4_SF_MMA)
+    ws = fq._want_shift(p, True)
+    fused_out = fq._alloc_copy(M_TOK, N_MODEL, p, layer.Y.device, ws)
+    plain_out = fq._alloc_copy(M_TOK, N_MODEL, p, layer.Y.device, ws)
+    a, b = layer.xr.operand(), layer.wr.operand()
+
+    def fused():
+        fq._check(fq.fp4_gemm_quantize(a, b, M_TOK, N_MODEL, K_FF, amax_y, p, fused_out.q,
+                                       fused_out.sf, fused_out.s_dec, fused_out.row_shift),
+                  "fused")
+
+    def unfused():
+        fq.gemm(layer.xr, layer.wr, out=layer.Y)
+        fq._check(fq.fp4_quantize(layer.Y, amax_y, p, plain_out.q, plain_out.sf,
+                                  plain_out.s_dec, plain_out.row_shift), "unfused")
+
+    t_f = graph_ms(fused, flush)
+    t_u = graph_ms(unfused, flush)
+    fq._check(fq.fp4_status_sync(), "fused producer")
+    return {"gemm": "fprop %d x %d x %d" % (M_TOK, N_MODEL, K_FF),
+            "fused_ms": round(t_f, 4), "unfused_ms": round(t_u, 4),
+            "hbm_bytes_avoided": 2 * M_TOK * N_MODEL * 2,
+            "note": "fused quantises the binary32 product; unfused quantises the stored BF16 Y"}
 
 
 def run_e2e(layer, args, world, ideal, graph=None):

@@ -597,46 +597,73 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int k4 = lane & 3;
       const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
       // Fused producer: the row-wise FP4 copy of this lane's 32 output values
-      // (one or two blocks along N), in place of the stores of y.
-      auto quant_out = [&](int64_t n0, const float(&y)[32]) {
-        if (m >= p.M) return;
+      // (one or two blocks along N) goes to qacc[q] / qcodes; flush_out()
+      // writes the lane's 128 columns once all four are encoded.
+      uint32_t qacc[16];        // payload: chunk q (16 bytes) = words 4q..4q+3
+      uint32_t qcodes[2];       // scale codes of the 128 columns, 4 per word
+      auto quant_out = [&](int q, int64_t n0, const float(&y)[32]) {
         const int nb = 32 / p.qb_out;
-        uint32_t w[4];
-        uint32_t codes[2] = {0u, 0u};
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          if (blk >= nb || n0 + blk * p.qb_out >= p.N) break;
+          if (blk >= nb) break;
+          uint32_t code = 0u;
           const int QB = p.qb_out, o = blk * QB;
-          float b = 0.0f;
-          for (int j = 0; j < QB; ++j) b = fmaxf(b, fabsf(y[o + j]));
-          float mult;
-          bool zp;
-          codes[blk] = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
-          for (int h = 0; h < QB / 8; ++h) {
-            float v[8];
+          if (n0 + o < p.N) {
+            float b = 0.0f;
+            for (int j = 0; j < QB; ++j) b = fmaxf(b, fabsf(y[o + j]));
+            float mult;
+            bool zp;
+            code = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
+            for (int h = 0; h < QB / 8; ++h) {
+              float v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
-            scale8(v, mult, zp);
-            const int64_t n = n0 + o + 8 * h;
-            w[2 * blk + h] =
-                p.sr_out ? encode8_sr(v, sr_group_bits(p.seed_out, p.offset_out, 0u,
-                                                       ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 3))
-                         : e2m1x8_hw(v);
+              for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
+              scale8(v, mult, zp);
+              const int64_t n = n0 + o + 8 * h;
+              qacc[4 * q + 2 * blk + h] =
+                  p.sr_out ? encode8_sr(v, sr_group_bits(p.seed_out, p.offset_out, 0u,
+                                                         ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 3))
+                           : e2m1x8_hw(v);
+            }
+          }
+          // code of scale column (q * nb + blk) of this lane's 128 columns
+          const int c = q * nb + blk;
+          qcodes[c >> 2] |= code << (8 * (c & 3));
+        }
+      };
+      auto flush_out = [&](int64_t nbase) {
+        // payload: four lanes exchange their 16-byte chunks so each store
+        // instruction writes eight 64-byte row pieces
+        transpose4x16B(qacc, k4);
+        const int64_t n = nbase + 32 * k4;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int64_t mm = grp_m + rr;
+          if (mm >= p.M || n >= p.N) continue;
+          uint8_t *dst = p.q_out + mm * (p.N / 2) + n / 2;  // 8-byte aligned (N % 16 == 0)
+          if (n + 32 <= p.N && (p.N & 31) == 0) {
+            *reinterpret_cast<uint4 *>(dst) =
+                make_uint4(qacc[4 * rr], qacc[4 * rr + 1], qacc[4 * rr + 2], qacc[4 * rr + 3]);
+          } else {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(qacc[4 * rr], qacc[4 * rr + 1]);
+            if (n + 32 <= p.N)
+              *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(qacc[4 * rr + 2], qacc[4 * rr + 3]);
           }
         }
-        uint8_t *qrow = p.q_out + m * (p.N / 2) + n0 / 2;
-        *reinterpret_cast<uint2 *>(qrow) = make_uint2(w[0], w[1]);
-        if (n0 + 16 < p.N) *reinterpret_cast<uint2 *>(qrow + 8) = make_uint2(w[2], w[3]);
-        for (int blk = 0; blk < nb; ++blk) {
-          const int64_t col = n0 / p.qb_out + blk;
+        if (m >= p.M) return;
+        const int ncodes = 128 / p.qb_out;
+        const int64_t c0 = nbase / p.qb_out;
+        for (int wd = 0; wd < ncodes / 4; ++wd) {
+          const int64_t col = c0 + 4 * wd;  // first of four scale columns
           if (col >= p.cb_out) break;
-          int64_t off;
-          if (p.sf_mma_out)
-            off = ((m >> 7) * p.cp4_out + (col >> 2)) * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4 +
-                  (col & 3);
-          else
-            off = m * p.cb_out + col;
-          p.sf_out[off] = (uint8_t)codes[blk];
+          if (p.sf_mma_out) {
+            const int64_t off = ((m >> 7) * p.cp4_out + (col >> 2)) * 512 + (m & 31) * 16 +
+                                ((m >> 5) & 3) * 4;
+            *reinterpret_cast<uint32_t *>(p.sf_out + off) = qcodes[wd];
+          } else {
+            for (int c = 0; c < 4 && col + c < p.cb_out; ++c)
+              p.sf_out[m * p.cb_out + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
+          }
         }
       };
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
@@ -654,7 +681,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           y[j] = __fmul_rn(v, alpha);
         }
         if (QOUT) {
-          quant_out(n0, y);
+          quant_out(q, n0, y);
           return;
         }
         if (p.d_bf16) {
@@ -698,12 +725,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(acc_empty);
       acc_phase ^= 1u;
+      if (QOUT) {
+        qcodes[0] = qcodes[1] = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qacc[i] = 0u;
+      }
       emit(0, acc[0], sh0);
       emit(1, acc[1], sh1);
       load_shifts(nbase + 64, sh0);
       load_shifts(nbase + 96, sh1);
       emit(2, acc[2], sh0);
       emit(3, acc[3], sh1);
+      if (QOUT && nbase < p.N) flush_out(nbase);
     }
   }
   tc_fence_before();
