@@ -115,7 +115,9 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
   }
 }
 
-template <int FMT, int HAD, bool TWO_D>
+// SR: the kernel carries the stochastic-rounding code (dY); the RNE-only
+// instantiations leave it out, which keeps them small in the instruction cache.
+template <int FMT, int HAD, bool TWO_D, bool SR>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   constexpr int B = Fmt<FMT>::B;
   constexpr int NSC = kTile / B;                    // scale columns per tile
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
             v[2 * k + 1] = bf16_hi(w[4 * h + k]);
           }
           scale8(v, mult, zp);
-          out[h] = p.sr_row ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
+          out[h] = (SR && p.sr_row) ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
                                                           ((uint64_t)gr * (uint64_t)C +
                                                            (uint64_t)(gc + 8 * h)) >> 3))
                             : e2m1x8_hw(v);
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
             v[2 * k] = f32x2_lo(r2);
             v[2 * k + 1] = f32x2_hi(r2);
           }
-          out[h] = p.sr_row ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
+          out[h] = (SR && p.sr_row) ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
                                                           ((uint64_t)gr * (uint64_t)C +
                                                            (uint64_t)(gc + 8 * h)) >> 3))
                             : e2m1x8_hw(v);
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
         scale8(e, mult, zp);
         uint32_t word;
         const int trow = row0 + rb + 8 * h8;
-        if (p.sr_col) {
+        if (SR && p.sr_col) {
           uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
           word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
         } else {
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
               }
             }
             const int trow = row0 + 8 * h8;
-            if (p.sr_col) {
+            if (SR && p.sr_col) {
               const uint64_t g0 = ((uint64_t)(C0 + col0 + 2 * k) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
               const uint64_t g1 = ((uint64_t)(C0 + col0 + 2 * k + 1) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
               cw[2 * k][h8] = encode8_sr(v0, sr_group_bits(p.seed, p.offset, 1u, g0));
@@ -487,7 +489,7 @@ __global__ void k_scale_only(const float *amax_row, const float *amax_col, float
   }
 }
 
-template <int FMT, int HAD, bool TWO_D>
+template <int FMT, int HAD, bool TWO_D, bool SR>
 fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
   // three resident CTAs per SM, each walking tiles
   static int sms[64] = {0};
@@ -500,16 +502,19 @@ fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
     sms[dev] = n;
   }
   const int64_t cap = 3 * (int64_t)sms[dev];
-  k_quantize<FMT, HAD, TWO_D><<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(p);
+  k_quantize<FMT, HAD, TWO_D, SR><<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 template <int FMT>
 fp4_status launch_fmt(const Params &p, int64_t tiles, int had, bool two_d, cudaStream_t s) {
-  if (two_d) return launch_t<FMT, 0, true>(p, tiles, s);
-  if (had == 16) return launch_t<FMT, 16, false>(p, tiles, s);
-  if (had == 32) return launch_t<FMT, 32, false>(p, tiles, s);
-  return launch_t<FMT, 0, false>(p, tiles, s);
+  if (two_d) return launch_t<FMT, 0, true, false>(p, tiles, s);  // 2D tiles: RNE only
+  const bool sr = p.sr_row || p.sr_col;
+  if (had == 16)
+    return sr ? launch_t<FMT, 16, false, true>(p, tiles, s) : launch_t<FMT, 16, false, false>(p, tiles, s);
+  if (had == 32)
+    return sr ? launch_t<FMT, 32, false, true>(p, tiles, s) : launch_t<FMT, 32, false, false>(p, tiles, s);
+  return sr ? launch_t<FMT, 0, false, true>(p, tiles, s) : launch_t<FMT, 0, false, false>(p, tiles, s);
 }
 
 }  // namespace
