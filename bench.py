@@ -290,6 +290,7 @@ def run_gpu(args, world, rank, local):
 
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     fused = run_fused_producer(layer, flush)
+    linear = run_linear(layer, flush)
     e2e = run_e2e(layer, args, world, ideal, graph)
 
     clocks = clk.summary()
@@ -322,6 +323,7 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": layer.launches_per_step * args.steps,
         "e2e": e2e,
         "epilogue_fused_producer": fused,
+        "linear_layer": linear,
     }
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(args, ideal)
@@ -385,6 +387,48 @@ def run_fused_producer(layer, flush):
             "fused_ms": round(t_f, 4), "unfused_ms": round(t_u, 4),
             "hbm_bytes_avoided": 2 * M_TOK * N_MODEL * 2,
             "note": "fused quantises the binary32 product; unfused quantises the stored BF16 Y"}
+
+
+def run_linear(layer, flush, steps=10):
+    """FP4Linear (the autograd layer over the same entry points) on the same
+    shapes: forward + backward of one step, eager, with the amax caches on a
+    hold step (D = 50) and on a refresh step."""
+    from fp4_block_scaled_quantize_gb300.linear import FP4Linear
+    dev = layer.X.device
+    lin = FP4Linear(K_FF, N_MODEL, D=50, format=layer.fmt, device=dev)
+    with torch.no_grad():
+        lin.weight.copy_(layer.W)
+    x = layer.X.detach().clone().requires_grad_(True)
+    dy = layer.dY
+
+    def one():
+        x.grad = None
+        lin.weight.grad = None
+        lin(x).backward(dy)
+
+    one()                      # step 0: refresh
+    lin.next_step()
+    one()
+    torch.cuda.synchronize()
+    out = {}
+    for name, step in (("hold_step_ms", 1), ("refresh_step_ms", 50)):
+        tot = 0.0
+        for _ in range(steps):
+            lin.step = step
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            one()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        out[name] = round(tot / steps, 4)
+    layer.fq._check(layer.fq.fp4_status_sync(), "linear")
+    out["shape"] = "x [%d, %d], W [%d, %d]" % (M_TOK, K_FF, N_MODEL, K_FF)
+    out["launch"] = "eager autograd (Python dispatch included)"
+    return out
 
 
 def run_e2e(layer, args, world, ideal, graph=None):
