@@ -6,7 +6,8 @@ CPU-baseline leg may import this package.  It never imports the CUDA library
 and the CUDA library never imports it.
 
 Inputs are float32 numpy arrays (BF16 tensors widened exactly).  Format ids
-are this module's own: UE5M3=0, NVFP4=1, MXFP4=2.
+are this module's own: UE5M3=0, NVFP4=1, MXFP4=2, UE5M3_B32=3 (the block-32
+control of the UE5M3 recipe).
 
 Composition helpers (``quantize``, ``quantize_transpose``, ``amax_pair``)
 follow the method's steps in the pages' order: per-tensor scale from the held
@@ -25,7 +26,7 @@ import numpy as np
 
 from . import build as _build
 
-UE5M3, NVFP4, MXFP4 = 0, 1, 2
+UE5M3, NVFP4, MXFP4, UE5M3_B32 = 0, 1, 2, 3
 
 _lib = None
 

@@ -22,7 +22,7 @@
 /* Number formats                                                         */
 /* ===================================================================== */
 
-int orc_block_size(int fmt) { return fmt == ORC_MXFP4 ? 32 : 16; }
+int orc_block_size(int fmt) { return (fmt == ORC_MXFP4 || fmt == ORC_UE5M3_B32) ? 32 : 16; }
 
 /* E2M1: sign bit, two exponent bits, one fraction bit
  * ([UE5M3] Approach: "payload E2M1 (sign, 2 exponent, 1 fraction)").
@@ -116,13 +116,13 @@ double orc_e8m0_value(int code) {
 }
 
 double orc_scale_value(int fmt, int code) {
-  if (fmt == ORC_UE5M3) return orc_ue5m3_value(code);
+  if (fmt == ORC_UE5M3 || fmt == ORC_UE5M3_B32) return orc_ue5m3_value(code);
   if (fmt == ORC_NVFP4) return orc_e4m3_value(code);
   return orc_e8m0_value(code);
 }
 
 static int scale_encode(int fmt, float v) {
-  return fmt == ORC_UE5M3 ? orc_ue5m3_rne_sat(v) : orc_e4m3_rne_sat(v);
+  return (fmt == ORC_UE5M3 || fmt == ORC_UE5M3_B32) ? orc_ue5m3_rne_sat(v) : orc_e4m3_rne_sat(v);
 }
 
 /* ===================================================================== */

@@ -31,6 +31,8 @@ extern "C" {
 #define ORC_UE5M3 0 /* E2M1 payload, unsigned E5M3 block scale, block 16 */
 #define ORC_NVFP4 1 /* E2M1 payload, E4M3 block scale, block 16          */
 #define ORC_MXFP4 2 /* E2M1 payload, E8M0 block scale, block 32          */
+#define ORC_UE5M3_B32 3 /* E2M1 payload, unsigned E5M3 block scale, block 32
+                           ([UE5M3] Approach: the block-32 control)    */
 
 int orc_block_size(int fmt);
 

@@ -294,7 +294,7 @@ def test_worked_block_by_hand():
     assert nib[7] == 8  # -0 keeps its sign bit
 
 
-@pytest.mark.parametrize("fmt,one", [(orc.UE5M3, 0x78), (orc.NVFP4, 0x38)])
+@pytest.mark.parametrize("fmt,one", [(orc.UE5M3, 0x78), (orc.NVFP4, 0x38), (orc.UE5M3_B32, 0x78)])
 def test_zero_scale_rule(fmt, one):
     se, sd = orc.tensor_scale(fmt, 448.0, 1.0)
     x = np.zeros((2, 32), F32)
@@ -302,6 +302,29 @@ def test_zero_scale_rule(fmt, one):
     q, sf = orc.quantize_rows(x, fmt, se, sd)
     assert (sf == one).all()
     assert (q & 0x77 == 0).all()
+
+
+def test_ue5m3_b32_block_shares_the_joint_max():
+    # Block-32 control ([UE5M3] Approach): one UE5M3 scale per 32 elements.
+    # amax 2688 = 6*448 gives s_enc = s_dec = 1.  First half max 6 -> scale
+    # 1.0, so the whole 32-block is encoded with multiplier 1: the second
+    # half's 0.5, 1.5, 3.0 keep codes 1, 3, 5.  Block 16 would give the
+    # second half its own scale 0.5 (max 3) and multiplier 2: codes 2, 5, 7.
+    x = np.zeros((1, 32), F32)
+    x[0, 0] = 6.0
+    x[0, 16:19] = [0.5, 1.5, 3.0]
+    b32 = orc.quantize(x, 2688.0, orc.UE5M3_B32, T=448.0)
+    b16 = orc.quantize(x, 2688.0, orc.UE5M3, T=448.0)
+    assert orc.block_size(orc.UE5M3_B32) == 32
+    assert b32["sf"].shape == (1, 1) and orc.ue5m3_value(int(b32["sf"][0, 0])) == 1.0
+    assert [orc.ue5m3_value(int(c)) for c in b16["sf"][0]] == [1.0, 0.5]
+    nib = lambda q: np.stack([q & 15, q >> 4], -1).ravel()
+    assert list(nib(b32["q"][0])[16:19]) == [1, 3, 5]
+    assert list(nib(b16["q"][0])[16:19]) == [2, 5, 7]
+    # where both halves carry the same max the two block sizes agree
+    x[0, 16] = 6.0
+    np.testing.assert_array_equal(orc.quantize(x, 2688.0, orc.UE5M3_B32)["q"],
+                                  orc.quantize(x, 2688.0, orc.UE5M3)["q"])
 
 
 def test_mxfp4_scale_rule():
@@ -317,20 +340,22 @@ def test_mxfp4_scale_rule():
     assert sf[0, 1] == 131 and (q[0, 16:] == 0x77).all()
 
 
-def test_2d_views_agree():
+@pytest.mark.parametrize("fmt", [orc.UE5M3, orc.UE5M3_B32])
+def test_2d_views_agree(fmt):
     rng = np.random.default_rng(6)
+    B = orc.block_size(fmt)
     x = (rng.standard_normal((64, 96)) * 0.02).astype(F32)
-    se, sd = orc.tensor_scale(orc.UE5M3, 448.0, orc.amax(x))
-    q_r, sf_r, q_c, sf_c = orc.quantize_2d(x, orc.UE5M3, se, sd)
+    se, sd = orc.tensor_scale(fmt, 448.0, orc.amax(x))
+    q_r, sf_r, q_c, sf_c = orc.quantize_2d(x, fmt, se, sd)
     nib_r = np.stack([q_r & 15, q_r >> 4], -1).reshape(64, 96)
     nib_c = np.stack([q_c & 15, q_c >> 4], -1).reshape(96, 64)
     np.testing.assert_array_equal(nib_r.T, nib_c)  # payload = nibble transpose
-    np.testing.assert_array_equal(np.repeat(sf_r, 16, 1).T, np.repeat(sf_c, 16, 1))
-    # each 16x16 tile has one scale
-    t = np.repeat(sf_r, 16, 1)
-    for i in range(0, 64, 16):
-        for j in range(0, 96, 16):
-            assert len(np.unique(t[i:i + 16, j:j + 16])) == 1
+    np.testing.assert_array_equal(np.repeat(sf_r, B, 1).T, np.repeat(sf_c, B, 1))
+    # each B x B tile has one scale
+    t = np.repeat(sf_r, B, 1)
+    for i in range(0, 64, B):
+        for j in range(0, 96, B):
+            assert len(np.unique(t[i:i + B, j:j + B])) == 1
 
 
 def test_decoded_block_error_bound():
@@ -487,13 +512,13 @@ def test_canonicalisation_ties():
     assert torch.equal(got, ref)
 
 
-@pytest.mark.parametrize("fmt", [orc.UE5M3, orc.NVFP4, orc.MXFP4])
+@pytest.mark.parametrize("fmt", [orc.UE5M3, orc.NVFP4, orc.MXFP4, orc.UE5M3_B32])
 def test_model_equals_exact_dot_on_small_integer_products(fmt):
     # codes with scale 1 and small payloads: every partial sum is an exactly
     # representable binary32 value, so all readings equal the exact dot product
     rng = np.random.default_rng(10 + fmt)
     K, M, N = 256, 6, 5
-    one = {orc.UE5M3: 0x78, orc.NVFP4: 0x38, orc.MXFP4: 127}[fmt]
+    one = {orc.UE5M3: 0x78, orc.NVFP4: 0x38, orc.MXFP4: 127, orc.UE5M3_B32: 0x78}[fmt]
     B = orc.block_size(fmt)
     qa = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
     qb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
@@ -530,3 +555,21 @@ def test_model_within_fp32_bound_of_exact_on_random_scales():
     Bm = dec(np.stack([qb & 15, qb >> 4], -1).reshape(N, K)) * np.repeat(sc(sfb), 16, 1)
     ref = (A @ Bm.T) * 0.125
     np.testing.assert_allclose(ye, ref, rtol=1e-12, atol=1e-12 * sa.max())
+
+
+def test_model_b32_scales_equal_duplicated_b16_scales():
+    # A block-32 scale applies to both 16-element halves, so the UE5M3-b32
+    # model equals the block-16 model with every scale column duplicated
+    # (how the tensor-core path carries the block-32 control).
+    rng = np.random.default_rng(12)
+    K, M, N = 384, 5, 7
+    qa = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    qb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sfa = rng.integers(0x60, 0x90, (M, K // 32)).astype(np.uint8)
+    sfb = rng.integers(0x60, 0x90, (N, K // 32)).astype(np.uint8)
+    y32, e32, s32 = orc.gemm_model_full(qa, sfa, qb, sfb, orc.UE5M3_B32, K, 0.25, 0.5)
+    y16, e16, s16 = orc.gemm_model_full(qa, np.repeat(sfa, 2, 1), qb, np.repeat(sfb, 2, 1),
+                                        orc.UE5M3, K, 0.25, 0.5)
+    np.testing.assert_array_equal(y32, y16)
+    np.testing.assert_array_equal(e32, e16)
+    np.testing.assert_array_equal(s32, s16)
