@@ -37,7 +37,7 @@ import torch  # noqa: E402
 
 M_TOK, K_FF, N_MODEL = 8192, 14336, 4096
 WORKLOAD = "8B MLP down_proj fwd+bwd (refresh step), UE5M3-b16"
-FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32"}
+FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32", 3: "UE5M3-b32"}
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor ratio on GB300
 
 
@@ -53,7 +53,7 @@ def peaks():
 
 def work_model(fmt):
     """Algorithmic bytes / flops of one step (what the method must move)."""
-    B = 32 if fmt == 2 else 16
+    B = 32 if fmt in (2, 3) else 16
     per_copy = 0.5 + 1.0 / B
     ex, ew, edy = M_TOK * K_FF, N_MODEL * K_FF, M_TOK * N_MODEL
     amax_bytes = 2.0 * (ex + ew + edy)
@@ -644,7 +644,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--format", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--format", type=int, default=0, choices=[0, 1, 2, 3])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps kernel by kernel instead of as a CUDA graph")

@@ -19,7 +19,7 @@ from . import inputs  # noqa: F401  (seeded workload generators)
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libfp4gb300.so")
 
-FP4_FMT_UE5M3_B16, FP4_FMT_NVFP4_B16, FP4_FMT_MXFP4_B32 = 0, 1, 2
+FP4_FMT_UE5M3_B16, FP4_FMT_NVFP4_B16, FP4_FMT_MXFP4_B32, FP4_FMT_UE5M3_B32 = 0, 1, 2, 3
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
 FP4_SF_PLAIN, FP4_SF_MMA = 0, 1
 FP4_OK = 0
@@ -195,7 +195,8 @@ def _alloc_copy(rows, cols, p, device, with_shift):
 
 
 def _want_shift(p, remap):
-    return bool(remap) and p.format == FP4_FMT_UE5M3_B16 and p.sf_layout == FP4_SF_MMA
+    return (bool(remap) and p.format in (FP4_FMT_UE5M3_B16, FP4_FMT_UE5M3_B32)
+            and p.sf_layout == FP4_SF_MMA)
 
 
 def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):

@@ -34,7 +34,10 @@ using namespace fp4;
 
 namespace {
 
-bool valid_format(int32_t f) { return f == FP4_FMT_UE5M3_B16 || f == FP4_FMT_NVFP4_B16 || f == FP4_FMT_MXFP4_B32; }
+bool valid_format(int32_t f) {
+  return f == FP4_FMT_UE5M3_B16 || f == FP4_FMT_NVFP4_B16 || f == FP4_FMT_MXFP4_B32 ||
+         f == FP4_FMT_UE5M3_B32;
+}
 bool valid_round(int32_t r) { return r == FP4_ROUND_RNE || r == FP4_ROUND_SR; }
 bool valid_layout(int32_t l) { return l == FP4_SF_PLAIN || l == FP4_SF_MMA; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -60,8 +63,9 @@ int32_t fp4_block_size(int32_t format) { return valid_format(format) ? block_of(
 
 int64_t fp4_sf_bytes(int32_t format, int64_t rows, int64_t cols, int32_t layout) {
   if (!valid_format(format) || !valid_layout(layout) || rows < 0 || cols < 0) return -1;
-  const int64_t cb = cols / block_of(format);
-  if (layout == FP4_SF_PLAIN) return rows * cb;
+  if (layout == FP4_SF_PLAIN) return rows * (cols / block_of(format));
+  // UE5M3-b32 in the MMA layout is stored at block-16 granularity (duplicated)
+  const int64_t cb = cols / (format == FP4_FMT_UE5M3_B32 ? 16 : block_of(format));
   return ceil_div(rows, 128) * 128 * ceil_div(cb, 4) * 4;
 }
 
@@ -88,7 +92,7 @@ fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const fl
   const bool empty = rows == 0 || cols == 0;
   if (!empty && (!x_bf16 || !q || !sf)) return FP4_ERR_INVALID_ARG;
   if (cols % B != 0 || (p->block2d && rows % B != 0)) return FP4_ERR_SHAPE;
-  if (row_shift && !(p->format == FP4_FMT_UE5M3_B16 && p->sf_layout == FP4_SF_MMA))
+  if (row_shift && !(is_ue5m3_fmt(p->format) && p->sf_layout == FP4_SF_MMA))
     return FP4_ERR_UNSUPPORTED;
   if (!empty && (!aligned16(x_bf16) || !aligned16(q) || !aligned16(sf))) return FP4_ERR_ALIGNMENT;
   if (!aligned4(s_dec_dev) || !aligned4(amax_dev)) return FP4_ERR_ALIGNMENT;
@@ -127,7 +131,7 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   if (!empty && (!x_bf16 || !q_row || !sf_row || !q_col || !sf_col)) return FP4_ERR_INVALID_ARG;
   if (rows % B != 0 || cols % B != 0 || (p->hadamard_n && rows % p->hadamard_n != 0))
     return FP4_ERR_SHAPE;
-  const bool mma_ue5m3 = p->format == FP4_FMT_UE5M3_B16 && p->sf_layout == FP4_SF_MMA;
+  const bool mma_ue5m3 = is_ue5m3_fmt(p->format) && p->sf_layout == FP4_SF_MMA;
   if ((shift_row || shift_col) && !mma_ue5m3) return FP4_ERR_UNSUPPORTED;
   if (!empty && (!aligned16(x_bf16) || !aligned16(q_row) || !aligned16(sf_row) ||
                  !aligned16(q_col) || !aligned16(sf_col)))
@@ -172,9 +176,9 @@ fp4_status gemm_operands(const fp4_operand *A, const fp4_operand *B, int64_t M, 
   if (!A->q || !A->sf || !B->q || !B->sf || !A->s_dec || !B->s_dec) return FP4_ERR_INVALID_ARG;
   if (!aligned16(A->q) || !aligned16(A->sf) || !aligned16(B->q) || !aligned16(B->sf))
     return FP4_ERR_ALIGNMENT;
-  if (A->format == FP4_FMT_UE5M3_B16 && (!A->row_shift || !B->row_shift))
+  if (is_ue5m3_fmt(A->format) && (!A->row_shift || !B->row_shift))
     return FP4_ERR_INVALID_ARG;
-  if (A->format == FP4_FMT_UE5M3_B16 && (!aligned16(A->row_shift) || !aligned16(B->row_shift)))
+  if (is_ue5m3_fmt(A->format) && (!aligned16(A->row_shift) || !aligned16(B->row_shift)))
     return FP4_ERR_ALIGNMENT;
   j.qa = A->q;
   j.sfa = A->sf;
@@ -182,8 +186,8 @@ fp4_status gemm_operands(const fp4_operand *A, const fp4_operand *B, int64_t M, 
   j.sfb = B->sf;
   j.sda = A->s_dec;
   j.sdb = B->s_dec;
-  j.sha = A->format == FP4_FMT_UE5M3_B16 ? A->row_shift : nullptr;
-  j.shb = B->format == FP4_FMT_UE5M3_B16 ? B->row_shift : nullptr;
+  j.sha = is_ue5m3_fmt(A->format) ? A->row_shift : nullptr;
+  j.shb = is_ue5m3_fmt(B->format) ? B->row_shift : nullptr;
   j.fmt = A->format;
   j.M = M;
   j.N = N;
@@ -235,7 +239,8 @@ fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t
   st = check_params(p);
   if (st != FP4_OK) return st;
   if (p->block2d || p->hadamard_n || p->round_col != FP4_ROUND_RNE) return FP4_ERR_UNSUPPORTED;
-  if (row_shift && !(p->format == FP4_FMT_UE5M3_B16 && p->sf_layout == FP4_SF_MMA))
+  if (p->format == FP4_FMT_UE5M3_B32) return FP4_ERR_UNSUPPORTED;  // fused path: block 16 / MX
+  if (row_shift && !(is_ue5m3_fmt(p->format) && p->sf_layout == FP4_SF_MMA))
     return FP4_ERR_UNSUPPORTED;
   if (K == 0 || N % block_of(p->format) != 0) return FP4_ERR_SHAPE;
   if (!amax_dev || !s_dec_dev) return FP4_ERR_INVALID_ARG;

@@ -29,7 +29,12 @@ inline bool aligned16(const void *p) {
 }
 
 inline int block_of(int32_t fmt) {
-  return fmt == FP4_FMT_MXFP4_B32 ? 32 : (fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_NVFP4_B16 ? 16 : -1);
+  if (fmt == FP4_FMT_MXFP4_B32 || fmt == FP4_FMT_UE5M3_B32) return 32;
+  return (fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_NVFP4_B16) ? 16 : -1;
+}
+// UE5M3 scales (block 16 or 32): row shifts onto the tensor core's E4M3 path.
+inline bool is_ue5m3_fmt(int32_t fmt) {
+  return fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_UE5M3_B32;
 }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -11,11 +11,13 @@
 
 namespace fp4 {
 
-enum { kUE5M3 = 0, kNVFP4 = 1, kMXFP4 = 2 };
+enum { kUE5M3 = 0, kNVFP4 = 1, kMXFP4 = 2, kUE5M3B32 = 3 };
+// UE5M3 scale codes (block 16, or the block-32 control).
+__host__ __device__ constexpr bool is_ue5m3(int f) { return f == kUE5M3 || f == kUE5M3B32; }
 
 template <int FMT>
 struct Fmt {
-  static constexpr int B = (FMT == kMXFP4) ? 32 : 16;
+  static constexpr int B = (FMT == kMXFP4 || FMT == kUE5M3B32) ? 32 : 16;
 };
 
 // ---------------------------------------------------------------- BF16
@@ -190,9 +192,9 @@ __device__ __forceinline__ uint32_t block_scale(float b, float s_enc, float s_de
     return (uint32_t)(E + 127);
   } else {
     float raw = __fmul_rn(__fdiv_rn(b, 6.0f), s_enc);
-    uint32_t code = (FMT == kUE5M3) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
-    if (code == 0) code = (FMT == kUE5M3) ? 0x78u : 0x38u;
-    float dec = (FMT == kUE5M3) ? ue5m3_dec(code) : e4m3_dec(code);
+    uint32_t code = is_ue5m3(FMT) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
+    if (code == 0) code = is_ue5m3(FMT) ? 0x78u : 0x38u;
+    float dec = is_ue5m3(FMT) ? ue5m3_dec(code) : e4m3_dec(code);
     float sd = __fmul_rn(dec, s_dec);
     zero_payload = (sd == 0.0f);
     mult = __fdiv_rn(1.0f, sd);
@@ -205,7 +207,7 @@ __device__ __forceinline__ uint32_t block_scale(float b, float s_enc, float s_de
 // payload).  Built once per CTA; unused for MX.
 template <int FMT>
 __device__ __forceinline__ float mult_of_code(uint32_t code, float s_dec) {
-  const float dec = (FMT == kUE5M3) ? ue5m3_dec(code) : e4m3_dec(code);
+  const float dec = is_ue5m3(FMT) ? ue5m3_dec(code) : e4m3_dec(code);
   const float sd = __fmul_rn(dec, s_dec);
   return sd == 0.0f ? 0.0f : __fdiv_rn(1.0f, sd);
 }
@@ -222,8 +224,8 @@ __device__ __forceinline__ uint32_t block_scale_tab(float b, float s_enc, const 
     return (uint32_t)(E + 127);
   } else {
     const float raw = __fmul_rn(div6_rn(b), s_enc);
-    uint32_t code = (FMT == kUE5M3) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
-    if (code == 0) code = (FMT == kUE5M3) ? 0x78u : 0x38u;
+    uint32_t code = is_ue5m3(FMT) ? ue5m3_rne_sat(raw) : e4m3_rne_sat(raw);
+    if (code == 0) code = is_ue5m3(FMT) ? 0x78u : 0x38u;
     mult = tab[code];
     zero_payload = (mult == 0.0f);
     return code;

@@ -82,7 +82,10 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 // row r (copy rows r0 + r) and scale columns c0b + j; `rows_valid` and
 // `cols_valid` bound the real part (the rest is padding, written as 0 in the
 // tensor-core layout and not written in the plain layout).
-template <int NSC>
+// DUP: the tile's block-32 codes go to the MMA layout at block-16
+// granularity, each code in both of its halves' columns (NSC, copy_cb and
+// c0b then count block-16 columns; sfs[r][j / 2] is column j's code).
+template <int NSC, bool DUP = false>
 __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *sf, int64_t copy_rows,
                                              int64_t copy_cb, int64_t r0, int64_t c0b, int sf_mma) {
   const int t = threadIdx.x;
@@ -101,7 +104,7 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         int j = atom * 4 + c;
-        uint32_t code = (r < rows_valid && j < cols_valid) ? sfs[r][j] : 0u;
+        uint32_t code = (r < rows_valid && j < cols_valid) ? sfs[r][DUP ? j / 2 : j] : 0u;
         w |= code << (8 * c);
       }
       int64_t base = ((r0 / 128) * cp4 + atom_col) * 512;
@@ -468,8 +471,13 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
   }
   // ---- scales
   __syncthreads();
-  if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
-  if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
+  if (FMT == kUE5M3B32 && p.sf_mma) {
+    if (p.do_row) write_scales<2 * NSC, true>(sfr, p.sf_row, R, C / 16, R0, C0 / 16, 1);
+    if (p.do_col) write_scales<2 * NSC, true>(sfc, p.sf_col, C, R / 16, C0, R0 / 16, 1);
+  } else {
+    if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
+    if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
+  }
   __syncthreads();  // the tile and staging buffers are reused by the next tile
   }  // tile loop
 }
@@ -545,7 +553,8 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
     float *sdr = j.s_dec_row;
     float *sdc = j.s_dec_col;
     switch (j.fmt) {
-      case kUE5M3: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
+      case kUE5M3:
+      case kUE5M3B32: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
       case kNVFP4: k_scale_only<kNVFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
       default: k_scale_only<kMXFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
     }
@@ -559,11 +568,12 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   fp4_status st;
   switch (j.fmt) {
     case kUE5M3: st = launch_fmt<kUE5M3>(p, tiles, had, two_d, s); break;
+    case kUE5M3B32: st = launch_fmt<kUE5M3B32>(p, tiles, had, two_d, s); break;
     case kNVFP4: st = launch_fmt<kNVFP4>(p, tiles, had, two_d, s); break;
     default: st = launch_fmt<kMXFP4>(p, tiles, had, two_d, s); break;
   }
   if (st != FP4_OK) return st;
-  if (j.fmt == kUE5M3 && j.sf_mma) {
+  if (is_ue5m3(j.fmt) && j.sf_mma) {  // (block-32 scales sit at block-16 granularity)
     if (p.do_row && j.shift_row) {
       st = launch_remap_ue5m3(j.sf_row, j.q_row, j.R, j.C, j.shift_row, s);
       if (st != FP4_OK) return st;

@@ -61,11 +61,17 @@ typedef enum {
  *   UE5M3_B16: unsigned E5M3 (bias 15, largest value 61,440), 16 elements
  *              -- the primary recipe of [UE5M3] Approach;
  *   NVFP4_B16: E4M3 (bias 7, largest value 448), 16 elements;
- *   MXFP4_B32: E8M0 (2^(code-127)), 32 elements, no per-tensor scale. */
+ *   MXFP4_B32: E8M0 (2^(code-127)), 32 elements, no per-tensor scale;
+ *   UE5M3_B32: unsigned E5M3, 32 elements -- the block-32 control of the
+ *              UE5M3 recipe ([UE5M3] Approach).  In the MMA layout its
+ *              scales are stored duplicated per 16-element half (the
+ *              block-16 tiling, E4M3 images after the remap), so the tensor
+ *              core consumes it through the block-16 path. */
 typedef enum {
   FP4_FMT_UE5M3_B16 = 0,
   FP4_FMT_NVFP4_B16 = 1,
-  FP4_FMT_MXFP4_B32 = 2
+  FP4_FMT_MXFP4_B32 = 2,
+  FP4_FMT_UE5M3_B32 = 3
 } fp4_format;
 
 typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_rounding;

@@ -8,7 +8,8 @@ import oracle as orc
 
 # library format id -> oracle format id (each side keeps its own enum)
 ORC_FMT = {fq.FP4_FMT_UE5M3_B16: orc.UE5M3, fq.FP4_FMT_NVFP4_B16: orc.NVFP4,
-           fq.FP4_FMT_MXFP4_B32: orc.MXFP4}
+           fq.FP4_FMT_MXFP4_B32: orc.MXFP4, fq.FP4_FMT_UE5M3_B32: orc.UE5M3_B32}
+UE_FORMATS = (fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_UE5M3_B32)
 
 
 def need_gpu():
@@ -36,14 +37,26 @@ def mismatch_report(got, want, name):
                              f"gpu={got[i]} oracle={want[i]}")
 
 
+def b16_view(fmt_lib, sf_plain):
+    """Scales at block-16 granularity: the tensor-core layout stores the
+    UE5M3 block-32 control's codes once per 16-element half."""
+    return np.repeat(sf_plain, 2, 1) if fmt_lib == fq.FP4_FMT_UE5M3_B32 else sf_plain
+
+
 def expect_sf(fmt_lib, sf_plain, q_plain, layout, remap):
     """Oracle-side expected scale bytes and shift for one copy."""
     if layout == fq.FP4_SF_PLAIN:
         return sf_plain.ravel(), None
-    if fmt_lib == fq.FP4_FMT_UE5M3_B16 and remap:
-        e4, shift, fails = orc.remap_ue5m3(sf_plain, q_plain)
+    sf16 = b16_view(fmt_lib, sf_plain)
+    if fmt_lib in UE_FORMATS and remap:
+        e4, shift, fails = orc.remap_ue5m3(sf16, q_plain)
         return orc.sf_to_mma(e4), shift
-    return orc.sf_to_mma(sf_plain), None
+    return orc.sf_to_mma(sf16), None
+
+
+def remap_fails(fmt_lib, sf_plain, q_plain):
+    """Blocks with no exact E4M3 image under the per-row shift (oracle)."""
+    return orc.remap_ue5m3(b16_view(fmt_lib, sf_plain), q_plain)[2]
 
 
 def set_device_scalar(v, device="cuda"):

@@ -14,11 +14,12 @@ import torch
 import fp4_block_scaled_quantize_gb300 as fq
 from fp4_block_scaled_quantize_gb300 import inputs
 import oracle as orc
-from gpu_util import ORC_FMT, f32, need_gpu
+from gpu_util import ORC_FMT, UE_FORMATS, b16_view, f32, need_gpu
 
 pytestmark = pytest.mark.gpu
 
 UE, NV, MX = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+U32 = fq.FP4_FMT_UE5M3_B32
 TOL_MODEL, TOL_EXACT = 1e-6, 1e-3
 
 
@@ -26,8 +27,8 @@ def upload(oq, fmt):
     """Oracle-quantised copy -> GPU operand in the tensor-core scale layout."""
     q = torch.from_numpy(np.ascontiguousarray(oq["q"])).cuda()
     shift = None
-    if fmt == UE:
-        e4, sh, fails = orc.remap_ue5m3(oq["sf"], oq["q"])
+    if fmt in UE_FORMATS:
+        e4, sh, fails = orc.remap_ue5m3(b16_view(fmt, oq["sf"]), oq["q"])
         assert fails == 0
         sf = orc.sf_to_mma(e4)
         shift = torch.from_numpy(sh).cuda()
@@ -83,7 +84,7 @@ def check(y_gpu, oa, ob, fmt, K, mi, ni, canon=False, bf16=False, name=""):
     assert np.all(rel_exact <= TOL_EXACT), f"{name}: exact-reference error {rel_exact.max()}"
 
 
-@pytest.mark.parametrize("fmt", [NV, UE, MX])
+@pytest.mark.parametrize("fmt", [NV, UE, MX, U32])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (200, 328, 320),
                                    (384, 264, 1088)])
 def test_gemm_full_parity_small(fmt, M, N, K):
@@ -172,7 +173,7 @@ def test_gemm_shape_errors():
     assert fq.fp4_gemm(A, A, 128, 124, 128, D, 0) == 3  # N % 8
 
 
-@pytest.mark.parametrize("fmt", [UE, NV, MX])
+@pytest.mark.parametrize("fmt", [UE, NV, MX, U32])
 def test_end_to_end_layer_small(fmt):
     """Whole GPU path (amax -> producers -> remap -> fprop / dgrad / wgrad)
     against the whole oracle path, on the 8B down_proj distributions at a
@@ -182,7 +183,7 @@ def test_end_to_end_layer_small(fmt):
     d = inputs.down_proj_8b(M=M, K=K, N=N)
     X, W, dY = d["X"], d["W"], d["dY"]
     of = ORC_FMT[fmt]
-    T_dy = 2048.0 if fmt == UE else 448.0
+    T_dy = 2048.0 if fmt in UE_FORMATS else 448.0
     # GPU
     P = lambda **kw: fq.params(format=fmt, sf_layout=fq.FP4_SF_MMA, **kw)
     xg, wg, dyg = X.cuda(), W.cuda(), dY.cuda()

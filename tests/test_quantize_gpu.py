@@ -7,11 +7,13 @@ import torch
 import fp4_block_scaled_quantize_gb300 as fq
 from fp4_block_scaled_quantize_gb300 import inputs
 import oracle as orc
-from gpu_util import ORC_FMT, expect_sf, f32, mismatch_report, need_gpu, np_u8, set_device_scalar
+from gpu_util import (ORC_FMT, expect_sf, f32, mismatch_report, need_gpu, np_u8, remap_fails,
+                      set_device_scalar)
 
 pytestmark = pytest.mark.gpu
 
 UE, NV, MX = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+U32 = fq.FP4_FMT_UE5M3_B32
 
 
 def _edge_tensor(rows, cols, seed):
@@ -45,7 +47,7 @@ def _check_copy(name, got, want, fmt, layout, remap):
     fails = 0
     if eshift is not None:
         mismatch_report(got.row_shift.cpu().numpy()[:len(eshift)], eshift, name + ".shift")
-        fails = orc.remap_ue5m3(want["sf"], want["q"])[2]
+        fails = remap_fails(fmt, want["sf"], want["q"])
     return fails
 
 
@@ -77,6 +79,13 @@ CASES = [
     (288, 160, MX, False, False, 16, 0x1234, fq.FP4_SF_MMA),
     (16, 16, UE, False, False, 0, 0, fq.FP4_SF_MMA),
     (32, 32, MX, False, False, 0, 0, fq.FP4_SF_PLAIN),
+    # UE5M3 block-32 control
+    (256, 384, U32, False, False, 0, 0, fq.FP4_SF_PLAIN),
+    (224, 352, U32, False, False, 0, 0, fq.FP4_SF_MMA),
+    (256, 384, U32, True, False, 0, 0, fq.FP4_SF_MMA),
+    (256, 256, U32, False, True, 0, 0, fq.FP4_SF_MMA),
+    (256, 256, U32, False, False, 32, 0x5A5A, fq.FP4_SF_MMA),
+    (32, 32, U32, False, False, 0, 0, fq.FP4_SF_MMA),
 ]
 
 
@@ -104,10 +113,11 @@ def test_quantize_transpose_parity(rows, cols, fmt, block2d, sr, had, signs, lay
 @pytest.mark.parametrize("fmt,layout,block2d,sr", [
     (UE, fq.FP4_SF_PLAIN, False, False), (UE, fq.FP4_SF_MMA, False, True),
     (NV, fq.FP4_SF_MMA, True, False), (MX, fq.FP4_SF_PLAIN, False, True),
-    (MX, fq.FP4_SF_MMA, True, False)])
+    (MX, fq.FP4_SF_MMA, True, False), (U32, fq.FP4_SF_MMA, False, True),
+    (U32, fq.FP4_SF_PLAIN, True, False)])
 def test_quantize_rowwise_parity(fmt, layout, block2d, sr):
     need_gpu()
-    rows, cols = (160, 416) if fmt != MX else (160, 416 - 32)
+    rows, cols = (160, 416) if fq.fp4_block_size(fmt) == 16 else (160, 416 - 32)
     x = _edge_tensor(rows, cols, seed=3)
     xg = x.cuda()
     a, _ = fq.amax(xg)
