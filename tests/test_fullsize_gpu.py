@@ -141,3 +141,22 @@ def test_sweep_wgrad_hadamard(fmt, had, signs):
     got = y.cpu().numpy()[mi, ni]
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel < 0.2, rel
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (16384, 2048, 2048), (2048, 16384, 2048),
+                                   (2048, 2048, 16384), (4096, 8192, 16384),
+                                   (8192, 14336, 4096), (14336, 8192, 4096)])
+def test_c5_sweep_shapes(M, N, K):
+    """Config-5 shape sweep (a spread of its {2048..16384}^3 grid plus the
+    (8192, 14336, 4096) pair): sweep operands (N(0,1), 1% x50), both
+    quantised by the oracle and uploaded, GEMM sampled against the model."""
+    need_gpu()
+    from test_gemm_gpu import oracle_operand, upload
+    fmt = UE
+    a_x = inputs.sweep_operand(M, K, seed=M + K)
+    b_x = inputs.sweep_operand(N, K, seed=N + 2 * K)
+    oa, ob = oracle_operand(a_x, fmt), oracle_operand(b_x, fmt)
+    y = fq.gemm(upload(oa, fmt), upload(ob, fmt))
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    mi, ni = sample_indices(M, N, 512, seed=M ^ N ^ K)
+    check(y, oa, ob, fmt, K, mi, ni, name=f"C5 {M}x{N}x{K}")
