@@ -12,8 +12,10 @@
 // Design (persistent, three CTAs of 256 threads per SM, 128 x 128 BF16 tiles,
 // HBM-bound): tensor scales and the per-code multiplier tables are set up
 // once per CTA, which then walks tiles with a stride of the grid.
-//  * loads: 16 B per lane (warp w owns tile rows 16w..16w+15, two rows per
-//    load instruction), staged in shared memory (rows padded by 16 bytes).
+//  * loads: one tensor-TMA copy per tile (zero fill outside the tensor) into
+//    a dense 256-byte-row tile buffer, completion on an mbarrier; the next
+//    tile's copy is issued as soon as the row pass has finished reading the
+//    buffer, so it lands while this tile's payload and scales are stored.
 //  * the transposed copy reads the tile column-wise: each lane owns 64
 //    values (4 columns x 16 rows, or 2 x 32 with a 32-row rotation / block);
 //    8-byte row-contiguous reads are conflict-free; block maxima by packed
@@ -23,8 +25,11 @@
 //  * transposed payload bytes are staged in shared memory so every column
 //    segment leaves as contiguous 8-byte stores; scales leave as whole
 //    512-byte tensor-core tiles (or plain rows).
-#include <cuda_bf16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "formats.cuh"
@@ -40,7 +45,6 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
-constexpr int kXsPad = 8;                      // BF16 elements (16 bytes)
 constexpr int kColqPitch = kTile * 8 + 32;     // bytes per 16-row plane
 
 struct Params {
@@ -54,9 +58,58 @@ struct Params {
   uint8_t *q_col, *sf_col;
   float *s_dec_col;
   int do_row, do_col, sr_row, sr_col, sf_mma;
+  uint32_t *status;
   uint64_t seed;
   uint32_t offset, signs;
 };
+
+// ---- tile loads by tensor TMA into a double buffer, completion on an mbarrier
+constexpr int kTileBytes = kTile * kTile * 2;  // one 128 x 128 BF16 tile, 32 KB
+constexpr int kDynSmem = kTileBytes + 1024;  // one tile, 1 KB alignment slack
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init_q(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx_q(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_q(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (about one second); false if it ran out.
+__device__ __noinline__ bool mbar_wait_q(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_q(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    if (mbar_try_wait_q(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > kWaitNs) return false;
+  }
+}
+// One 128 x 128 BF16 tile at element (x = column, y = row); rows and columns
+// outside the tensor read as zero.
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
+                                         int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
 
 // Per-half max(|a|, |b|) of two BF16 pairs (sign bit = xor of the input
 // signs, ignored by every caller; a selection, exact).
@@ -68,14 +121,6 @@ __device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
 // Larger magnitude of the two halves of a BF16 pair, as binary32.
 __device__ __forceinline__ float amax_halves(uint32_t m) {
   return fmaxf(__uint_as_float((m << 16) & 0x7FFF0000u), __uint_as_float(m & 0x7FFF0000u));
-}
-
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 
 // Write one copy's scales for this tile.  sfs[r][j] holds the codes of tile
@@ -121,16 +166,21 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
 // SR: the kernel carries the stochastic-rounding code (dY); the RNE-only
 // instantiations leave it out, which keeps them small in the instruction cache.
 template <int FMT, int HAD, bool TWO_D, bool SR>
-__global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
+__global__ void __launch_bounds__(kThreads, 3)
+    k_quantize(const __grid_constant__ CUtensorMap tmap, Params p) {
   constexpr int B = Fmt<FMT>::B;
   constexpr int NSC = kTile / B;                    // scale columns per tile
   constexpr int RU = (HAD > B) ? HAD : B;           // rows per column unit
   constexpr int CPL = 64 / RU;                      // columns per lane
   constexpr int NCG = RU / 16;                      // column groups per tile
 
-  // BF16 tile; rows padded by 16 bytes so the two rows of one 16-byte store
-  // instruction land in different banks.
-  __shared__ __align__(16) uint16_t xs[kTile][kTile + kXsPad];
+  // Two BF16 tiles (dense 256-byte rows), filled by TMA: the next tile lands
+  // while this one is encoded.
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t *qsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t tbar[2];
+  __shared__ int tfail;
   // Transposed payload staged per 16-row plane: colq[plane][col][8 bytes];
   // planes padded by 32 bytes so the store loop's 8-byte reads are <= 2-way.
   __shared__ __align__(16) uint8_t colq[kTile / 16][kColqPitch];
@@ -162,23 +212,37 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
 
   // Persistent: the tensor scales and multiplier tables above are set up
   // once per CTA; the CTA then walks tiles with a stride of the grid.
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-  const int64_t R0 = (tile / p.tiles_c) * kTile, C0 = (tile % p.tiles_c) * kTile;
-  // ---- load: lane copies 8 BF16 of row 16w + 2i + (lane >> 4) into the tile
-  {
-    const int chunk = lane & 15;
-    const int64_t gc = C0 + 8 * chunk;
-    uint4 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t gr = R0 + 16 * warp + 2 * i + (lane >> 4);
-      raw[i] = (gr < R && gc < C) ? ldg_stream(p.x + gr * C + gc) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4 *>(&xs[16 * warp + 2 * i + (lane >> 4)][8 * chunk]) = raw[i];
+  const uint32_t bar_a[2] = {smem_addr(&tbar[0]), smem_addr(&tbar[1])};
+  if (threadIdx.x == 0) {
+    mbar_init_q(bar_a[0], 1);
+    mbar_init_q(bar_a[1], 1);
+    tfail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  auto load_tile = [&](int64_t t, int b) {
+    mbar_expect_tx_q(bar_a[b], kTileBytes);
+    tma_tile(smem_addr(qsm + b * kTileBytes), &tmap, bar_a[b], (int)((t % p.tiles_c) * kTile),
+             (int)((t / p.tiles_c) * kTile));
+  };
+  if (threadIdx.x == 0 && (int64_t)blockIdx.x < ntiles) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+    load_tile(blockIdx.x, 0);
+  }
+  const int buf = 0;
+  uint32_t phase[2] = {0u, 0u};
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+  const int64_t R0 = (tile / p.tiles_c) * kTile, C0 = (tile % p.tiles_c) * kTile;
+  // The other buffer was last read in the previous iteration, which ended at
+  // a barrier: the next tile can stream into it now.
+  if (!mbar_wait_q(bar_a[buf], phase[buf])) tfail = 1;
+  phase[buf] ^= 1u;
+  __syncthreads();
+  if (tfail) {
+    if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
+    return;
+  }
+  uint16_t(*xs)[kTile] = reinterpret_cast<uint16_t(*)[kTile]>(qsm + buf * kTileBytes);
 
   // ---- row-wise copy: thread t encodes blocks t, t + 256, ... of the tile
   // (a block = B consecutive elements of one tile row) from shared memory;
@@ -456,6 +520,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
 
   if (p.do_col || TWO_D) __syncthreads();  // tile maxima, staged payload, scales
   if (p.do_row) row_pass();
+  // the tile buffer is free: the next tile streams in during the stores
+  __syncthreads();
+  if (threadIdx.x == 0 && tile + gridDim.x < ntiles) load_tile(tile + gridDim.x, buf);
 
   // ---- transposed payload: each column's 64 bytes (8 planes x 8 bytes)
   // leave as 8 consecutive 8-byte stores
@@ -470,7 +537,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     }
   }
   // ---- scales
-  __syncthreads();
   if (FMT == kUE5M3B32 && p.sf_mma) {
     if (p.do_row) write_scales<2 * NSC, true>(sfr, p.sf_row, R, C / 16, R0, C0 / 16, 1);
     if (p.do_col) write_scales<2 * NSC, true>(sfc, p.sf_col, C, R / 16, C0, R0 / 16, 1);
@@ -478,8 +544,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(Params p) {
     if (p.do_row) write_scales<NSC>(sfr, p.sf_row, R, C / B, R0, C0 / B, p.sf_mma);
     if (p.do_col) write_scales<NSC>(sfc, p.sf_col, C, R / B, C0, R0 / B, p.sf_mma);
   }
-  __syncthreads();  // the tile and staging buffers are reused by the next tile
-  }  // tile loop
+  }  // tile loop (the next iteration's first barrier protects the staging buffers)
 }
 
 // s_dec only (empty tensors).
@@ -497,6 +562,33 @@ __global__ void k_scale_only(const float *amax_row, const float *amax_col, float
   }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_q() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// x [R][C] BF16, 128 x 128 boxes, no swizzle (dense 256-byte rows), zero fill.
+bool tile_map(CUtensorMap *m, const void *x, int64_t R, int64_t C) {
+  auto fn = encode_q();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)R};
+  cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTile, (cuuint32_t)kTile};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int FMT, int HAD, bool TWO_D, bool SR>
 fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
   // three resident CTAs per SM, each walking tiles
@@ -509,8 +601,17 @@ fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
       return FP4_ERR_CUDA;
     sms[dev] = n;
   }
+  auto kern = k_quantize<FMT, HAD, TWO_D, SR>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+  });
+  if (attr != cudaSuccess) return FP4_ERR_CUDA;
+  CUtensorMap map;
+  if (!tile_map(&map, p.x, p.R, p.C)) return FP4_ERR_CUDA;
   const int64_t cap = 3 * (int64_t)sms[dev];
-  k_quantize<FMT, HAD, TWO_D, SR><<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(p);
+  kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kDynSmem, s>>>(map, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -547,6 +648,8 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   p.sr_col = j.sr_col;
   p.sf_mma = j.sf_mma;
   p.seed = j.seed;
+  p.status = status_word();
+  if (!p.status) return FP4_ERR_CUDA;
   p.offset = j.offset;
   p.signs = j.signs;
   if (j.R == 0 || j.C == 0) {
