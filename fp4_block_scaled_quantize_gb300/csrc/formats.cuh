@@ -232,6 +232,66 @@ __device__ __forceinline__ uint32_t block_scale_tab(float b, float s_enc, const 
   }
 }
 
+// The same rule for a block maximum b that is a BF16 value, by a 128-entry
+// per-tensor table.  With b = (1 + m/128) 2^E, b >= 2^-100 (so b/6 is
+// normal) and a normal s_enc = S 2^F, rounding commutes with the
+// power-of-two factors: RN32(RN32(b/6) s_enc) = RN32(RN32((1 + m/128)/6) S)
+// 2^(E+F).  The nearest-even UE5M3 / E4M3 code of that product is therefore
+// the code of the m-only product with 8 (E + F) added to it, wherever the
+// result lies in the scale format's normal range, and it saturates exactly as
+// the direct rule does.  code_tab_entry(m) is that code for a biased exponent
+// of b of 0, so code = min(tab[m] + 8 * (biased exponent of b), largest
+// code); codes below 16 (near the subnormal range), b < 2^-100, b = 0 and
+// non-finite b take the direct rule.  The two were compared on every
+// positive BF16 b for about 3000 values of s_enc per format.
+template <int FMT>
+__device__ __forceinline__ int code_tab_entry(int m, float s_enc) {
+  const uint32_t su = __float_as_uint(s_enc);
+  const int F = (int)(su >> 23);
+  if (F == 0 || F == 255) return -(1 << 20);  // subnormal or non-finite s_enc: never used
+  const float S = __uint_as_float((su & 0x7FFFFFu) | 0x3F800000u);
+  const float M = __uint_as_float(0x3F800000u | ((uint32_t)m << 16));
+  uint32_t pu = __float_as_uint(__fmul_rn(__fdiv_rn(M, 6.0f), S));
+  pu += 0x7FFFFu + ((pu >> 20) & 1u);  // mantissa to 3 bits, ties to even
+  constexpr int bias = is_ue5m3(FMT) ? 15 : 7;
+  return 8 * ((int)(pu >> 23) + F - 3 * 127 + bias) + (int)((pu >> 20) & 7u);
+}
+
+struct ScaleCode {
+  uint32_t code;
+  float mult;
+};
+template <int FMT>
+__device__ __noinline__ ScaleCode block_scale_direct(float b, float s_enc, const float *tab) {
+  ScaleCode r;
+  bool zp;
+  r.code = block_scale_tab<FMT>(b, s_enc, tab, r.mult, zp);
+  return r;
+}
+
+// block_scale_tab for a BF16-valued b (identical results); MX unchanged.
+template <int FMT>
+__device__ __forceinline__ uint32_t block_scale_bf16(float b, float s_enc, const int *ctab,
+                                                     const float *tab, float &mult,
+                                                     bool &zero_payload) {
+  if (FMT == kMXFP4) return block_scale_tab<FMT>(b, s_enc, tab, mult, zero_payload);
+  const uint32_t u = __float_as_uint(b);
+  const uint32_t bexp = u >> 23;
+  const int ext = ctab[(u >> 16) & 0x7Fu] + (int)(bexp << 3);
+  uint32_t code;
+  if (ext >= 16 && bexp - 27u <= 227u) {
+    constexpr int cmax = is_ue5m3(FMT) ? 0xF7 : 0x7E;
+    code = (uint32_t)(ext < cmax ? ext : cmax);
+    mult = tab[code];
+  } else {
+    const ScaleCode r = block_scale_direct<FMT>(b, s_enc, tab);
+    code = r.code;
+    mult = r.mult;
+  }
+  zero_payload = (mult == 0.0f);
+  return code;
+}
+
 // Per-tensor scale: s_enc = RN32(RN32(6 T) / amax) (1 for amax 0 or
 // non-finite, FLT_MAX on overflow), s_dec = RN32(1 / s_enc); MX: 1, 1.
 template <int FMT>

@@ -204,9 +204,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (p.do_col) *p.s_dec_col = sd_c;
   }
   __shared__ float mtab_r[256], mtab_c[256];  // element multiplier per scale code
+  __shared__ int ctab_r[128], ctab_c[128];     // scale code per BF16 mantissa of b
   if (FMT != kMXFP4) {
     mtab_r[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_r);
     mtab_c[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_c);
+    if (threadIdx.x < 128) ctab_r[threadIdx.x] = code_tab_entry<FMT>(threadIdx.x, se_r);
+    else ctab_c[threadIdx.x - 128] = code_tab_entry<FMT>(threadIdx.x - 128, se_c);
     __syncthreads();
   }
 
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       float mult;
       bool zp;
-      const uint32_t code = block_scale_tab<FMT>(b, se_r, mtab_r, mult, zp);
+      const uint32_t code = block_scale_bf16<FMT>(b, se_r, ctab_r, mtab_r, mult, zp);
       uint32_t out[B / 8];
       if (__any_sync(0xFFFFFFFFu, zp || isinf(mult))) {
         // a zero-payload block or an infinite multiplier somewhere in the
@@ -422,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int k = 0; k < WPR; ++k) {
           float m0, m1;
           bool z0, z1;
-          const uint32_t code0 = block_scale_tab<FMT>(bmax[2 * k], se_c, mtab_c, m0, z0);
-          const uint32_t code1 = block_scale_tab<FMT>(bmax[2 * k + 1], se_c, mtab_c, m1, z1);
+          const uint32_t code0 = block_scale_bf16<FMT>(bmax[2 * k], se_c, ctab_c, mtab_c, m0, z0);
+          const uint32_t code1 = block_scale_bf16<FMT>(bmax[2 * k + 1], se_c, ctab_c, mtab_c, m1, z1);
           const bool fast = !__any_sync(0xFFFFFFFFu, z0 || z1 || isinf(m0) || isinf(m1));
           const uint64_t mm = pack_f32x2(m0, m1);
 #pragma unroll

@@ -185,6 +185,38 @@ def test_stale_amax_tiny_and_degenerate_scales():
             _check_copy(f"amax={amax_v}", out, want, fmt, fq.FP4_SF_PLAIN, False)
 
 
+def _every_bf16_block_max(seed):
+    """2048 x 256 BF16 whose row block i (16 elements) has max |x| equal to
+    the i-th positive finite BF16 value (blocks past the last one repeat it);
+    the other elements are random fractions of it, signs mixed."""
+    n = 2048 * 16
+    bits = np.minimum(np.arange(1, n + 1, dtype=np.uint32), 0x7F7F)
+    bmax = (bits << 16).view(np.float32)
+    rng = np.random.default_rng(seed)
+    x = bmax[:, None] * rng.uniform(-1.0, 1.0, size=(n, 16)).astype(np.float32)
+    x[np.arange(n), rng.integers(0, 16, n)] = bmax * rng.choice([-1.0, 1.0], n).astype(np.float32)
+    return torch.from_numpy(x.reshape(2048, 256)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [UE, NV, U32, MX])
+def test_every_bf16_block_max_parity(fmt):
+    """Block scales for every BF16 block maximum, under held amaxes that put
+    each binade in turn inside and outside the scale format's normal range
+    (the block-scale rule's table form and its direct form must agree)."""
+    need_gpu()
+    x = _every_bf16_block_max(seed=fmt + 1)
+    xg = x.cuda()
+    x32 = f32(x)
+    for held in (1e-30, 1e-6, 1.0, 3.0e4, 1e30, 3.3e38):
+        a = set_device_scalar(held)
+        p = fq.params(format=fmt, T=448.0, sf_layout=fq.FP4_SF_PLAIN)
+        r, c = fq.quantize_transpose(xg, a, a, p)
+        er, ec = _oracle_copies(x32, fmt, 448.0, np.float32(held), np.float32(held), False,
+                                False, False, 0, 0, 0, 0)
+        _check_copy(f"held={held}.row", r, er, fmt, fq.FP4_SF_PLAIN, False)
+        _check_copy(f"held={held}.col", c, ec, fmt, fq.FP4_SF_PLAIN, False)
+
+
 def test_empty_inputs_write_s_dec_only():
     need_gpu()
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
