@@ -182,7 +182,8 @@ class Layer:
         self.Y = torch.empty((M_TOK, N_MODEL), dtype=torch.bfloat16, device=device)
         self.dX = torch.empty((M_TOK, K_FF), dtype=torch.bfloat16, device=device)
         self.dW = torch.empty((N_MODEL, K_FF), dtype=torch.float32, device=device)
-        self.launches_per_step = 3 + 3 + 3 + (6 if fmt in (0, 3) else 0)
+        # amax x3, producers x3, GEMMs x3, one remap per UE5M3 producer
+        self.launches_per_step = 3 + 3 + 3 + (3 if fmt in (0, 3) else 0)
 
     def _qt(self, x, key, p, r, c):
         fq = self.fq

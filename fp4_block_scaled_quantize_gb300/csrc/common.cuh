@@ -63,7 +63,15 @@ struct QuantJob {
 };
 fp4_status launch_quantize(const QuantJob &j, cudaStream_t s);
 
-// UE5M3 -> E4M3 image of an MMA-layout scale buffer, in place, plus shifts.
+// UE5M3 -> E4M3 image of an MMA-layout scale buffer, in place, plus shifts
+// (one copy, or up to two copies of one producer in a single launch).
+struct RemapCopy {
+  uint8_t *sf;
+  const uint8_t *q;
+  int64_t rows, cols;
+  int8_t *shift;
+};
+fp4_status launch_remap_ue5m3(const RemapCopy *copies, int n, cudaStream_t s);
 fp4_status launch_remap_ue5m3(uint8_t *sf_mma, const uint8_t *q, int64_t rows, int64_t cols,
                               int8_t *shift, cudaStream_t s);
 

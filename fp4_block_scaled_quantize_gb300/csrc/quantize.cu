@@ -680,14 +680,11 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   }
   if (st != FP4_OK) return st;
   if (is_ue5m3(j.fmt) && j.sf_mma) {  // (block-32 scales sit at block-16 granularity)
-    if (p.do_row && j.shift_row) {
-      st = launch_remap_ue5m3(j.sf_row, j.q_row, j.R, j.C, j.shift_row, s);
-      if (st != FP4_OK) return st;
-    }
-    if (p.do_col && j.shift_col) {
-      st = launch_remap_ue5m3(j.sf_col, j.q_col, j.C, j.R, j.shift_col, s);
-      if (st != FP4_OK) return st;
-    }
+    RemapCopy cp[2];
+    int n = 0;
+    if (p.do_row && j.shift_row) cp[n++] = RemapCopy{j.sf_row, j.q_row, j.R, j.C, j.shift_row};
+    if (p.do_col && j.shift_col) cp[n++] = RemapCopy{j.sf_col, j.q_col, j.C, j.R, j.shift_col};
+    if (n) return launch_remap_ue5m3(cp, n, s);
   }
   return FP4_OK;
 }
