@@ -42,6 +42,14 @@ class fp4_operand(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("k", ctypes.c_int64)]
 
 
+FP4_AMAX_MAX_JOBS = 8
+
+
+class fp4_amax_job(ctypes.Structure):
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("amax_dev", ctypes.c_void_p)]
+
+
 class FP4Error(RuntimeError):
     def __init__(self, code, where):
         super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
@@ -49,7 +57,7 @@ class FP4Error(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
+EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
            "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync", "fp4_status_string")
 
 
@@ -65,6 +73,7 @@ def lib():
         qp = ctypes.POINTER(fp4_quant_params)
         op = ctypes.POINTER(fp4_operand)
         L.fp4_amax.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp]
+        L.fp4_amax_many.argtypes = [ctypes.POINTER(fp4_amax_job), i32, vp]
         L.fp4_quantize.argtypes = [vp, i64, i64, vp, qp, vp, vp, vp, vp, vp]
         L.fp4_quantize_transpose.argtypes = [vp, i64, i64, vp, vp, qp, vp, vp, vp, vp, vp, vp, vp,
                                              vp, vp]
@@ -77,7 +86,7 @@ def lib():
         L.fp4_status_sync.argtypes = [vp]
         L.fp4_status_string.argtypes = [i32]
         L.fp4_status_string.restype = ctypes.c_char_p
-        for f in ("fp4_amax", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
+        for f in ("fp4_amax", "fp4_amax_many", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
@@ -113,6 +122,17 @@ def fp4_amax(x, hadamard_n, hadamard_signs, amax_row, amax_col=None, stream=None
     rows, cols = x.shape
     return lib().fp4_amax(_ptr(x), rows, cols, hadamard_n, hadamard_signs, _ptr(amax_row),
                           _ptr(amax_col), _stream(stream))
+
+
+def fp4_amax_many(xs, outs, stream=None):
+    """Raw call: plain amax of each 2-D BF16 tensor in xs into the matching
+    device float of outs, one launch."""
+    n = len(xs)
+    jobs = (fp4_amax_job * max(n, 1))()
+    for k, (x, o) in enumerate(zip(xs, outs)):
+        rows, cols = x.shape
+        jobs[k] = fp4_amax_job(x.data_ptr() if x.numel() else None, rows, cols, o.data_ptr())
+    return lib().fp4_amax_many(jobs, n, _stream(stream))
 
 
 def fp4_quantize(x, amax, p, q, sf, s_dec, row_shift=None, stream=None):
@@ -205,6 +225,13 @@ def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
     b = torch.empty(1, dtype=torch.float32, device=x.device)
     _check(fp4_amax(x, hadamard_n, hadamard_signs, a, b, stream), "fp4_amax")
     return a, b
+
+
+def amax_many(xs, stream=None):
+    """[amax] device float32 tensors of shape [1], one per tensor, one launch."""
+    outs = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
+    _check(fp4_amax_many(xs, outs, stream), "fp4_amax_many")
+    return outs
 
 
 def quantize(x, amax_dev, p, remap=True, stream=None):

@@ -82,6 +82,24 @@ fp4_status fp4_amax(const void *x_bf16, int64_t rows, int64_t cols, int32_t hada
                      as_stream(stream));
 }
 
+fp4_status fp4_amax_many(const fp4_amax_job *jobs, int32_t n, void *stream) {
+  if (n < 0 || n > FP4_AMAX_MAX_JOBS || (n > 0 && !jobs)) return FP4_ERR_INVALID_ARG;
+  const void *x[FP4_AMAX_MAX_JOBS];
+  int64_t elems[FP4_AMAX_MAX_JOBS];
+  float *out[FP4_AMAX_MAX_JOBS];
+  for (int k = 0; k < n; ++k) {
+    const fp4_amax_job &j = jobs[k];
+    if (!j.amax_dev || j.rows < 0 || j.cols < 0) return FP4_ERR_INVALID_ARG;
+    if (j.rows * j.cols > 0 && !j.x_bf16) return FP4_ERR_INVALID_ARG;
+    if (j.cols % 8 != 0) return FP4_ERR_SHAPE;
+    if ((j.x_bf16 && !aligned16(j.x_bf16)) || !aligned4(j.amax_dev)) return FP4_ERR_ALIGNMENT;
+    x[k] = j.x_bf16;
+    elems[k] = j.rows * j.cols;
+    out[k] = j.amax_dev;
+  }
+  return launch_amax_many(x, elems, out, n, as_stream(stream));
+}
+
 fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const float *amax_dev,
                         const fp4_quant_params *p, uint8_t *q, uint8_t *sf, float *s_dec_dev,
                         int8_t *row_shift, void *stream) {

@@ -8,6 +8,13 @@
 // on the binary32 bit pattern of the result (non-negative binary32 values
 // order like their bit patterns).  Inf/NaN patterns are >= 0x7F80.
 //
+// Launch shape: the outputs are zeroed by a one-block kernel and the amax
+// kernel follows it as a programmatic dependent launch: its CTAs start while
+// the zeroing runs, read and reduce their part of the tensor, and wait for
+// the zeroing (griddepcontrol.wait) only before their atomicMax.  Several
+// plain tensors can share one launch (CTAs split among them in proportion
+// to their sizes).
+//
 // Hadamard variant ("Technical summary: LLM pretraining with MXFP4",
 // Findings: deterministic H16/H32 on the weight-gradient operand): the amax
 // of the transposed copy after rotating every n consecutive rows of each
@@ -22,6 +29,7 @@ namespace fp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxAmaxJobs = FP4_AMAX_MAX_JOBS;
 
 __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
 #pragma unroll
@@ -40,6 +48,7 @@ __device__ __forceinline__ void block_max_to(uint32_t v, float *out_a, float *ou
     w = warp_max(w);
     if (threadIdx.x == 0) {
       if (w >= 0x7F800000u) raise_status(status, kStatusNonfinite);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the outputs are zeroed
       if (out_a) atomicMax(reinterpret_cast<unsigned int *>(out_a), w);
       if (out_b) atomicMax(reinterpret_cast<unsigned int *>(out_b), w);
     }
@@ -50,13 +59,11 @@ __device__ __forceinline__ uint32_t mag2(uint32_t w) {
   return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
 }
 
-// max |x| over n16 chunks of 8 BF16 values (16 bytes each).
-__global__ void __launch_bounds__(kThreads) k_amax_plain(const uint4 *__restrict__ x, int64_t n16,
-                                                         float *out_a, float *out_b,
-                                                         uint32_t *status) {
+// max |x| (as BF16 magnitude bits) over the chunks b, b + nb, b + 2 nb, ...
+// (chunk = 8 BF16 values, 16 bytes) of one thread.
+__device__ __forceinline__ uint32_t chunk_max(const uint4 *__restrict__ x, int64_t n16, int64_t i,
+                                              int64_t stride) {
   uint32_t m = 0;
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
-  int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x;
   // four independent 16-byte loads in flight per thread
   for (; i + 3 * stride < n16; i += 4 * stride) {
     uint4 v[4];
@@ -70,7 +77,44 @@ __global__ void __launch_bounds__(kThreads) k_amax_plain(const uint4 *__restrict
     uint4 v = __ldg(x + i);
     m = max(m, max(max(mag2(v.x), mag2(v.y)), max(mag2(v.z), mag2(v.w))));
   }
+  return m;
+}
+
+// max |x| over n16 chunks of 8 BF16 values (16 bytes each).
+__global__ void __launch_bounds__(kThreads) k_amax_plain(const uint4 *__restrict__ x, int64_t n16,
+                                                         float *out_a, float *out_b,
+                                                         uint32_t *status) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const uint32_t m = chunk_max(x, n16, blockIdx.x * (int64_t)kThreads + threadIdx.x, stride);
   block_max_to(m << 16, out_a, out_b, status);
+}
+
+// Several plain amaxes in one launch: job k owns CTAs [first[k], first[k+1]).
+struct AmaxMany {
+  const uint4 *x[kMaxAmaxJobs];
+  int64_t n16[kMaxAmaxJobs];
+  float *out[kMaxAmaxJobs];
+  int first[kMaxAmaxJobs + 1];
+  int n;
+  uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads) k_amax_many(const __grid_constant__ AmaxMany a) {
+  int k = 0;
+  for (int i = 1; i < a.n; ++i)
+    if ((int)blockIdx.x >= a.first[i]) k = i;
+  const int64_t nb = a.first[k + 1] - a.first[k];
+  const int64_t b = (int64_t)blockIdx.x - a.first[k];
+  const uint32_t m = chunk_max(a.x[k], a.n16[k], b * kThreads + threadIdx.x, nb * kThreads);
+  block_max_to(m << 16, a.out[k], nullptr, a.status);
+}
+
+// Zero up to 2 * kMaxAmaxJobs output floats (null entries skipped).
+struct ZeroList {
+  float *p[2 * kMaxAmaxJobs];
+};
+__global__ void k_zero_outputs(const __grid_constant__ ZeroList z) {
+  if (threadIdx.x < 2 * kMaxAmaxJobs && z.p[threadIdx.x]) *z.p[threadIdx.x] = 0.0f;
 }
 
 // Both amaxes: plain max |x| and max |H-rotated transposed view|.  Each
@@ -123,13 +167,35 @@ __global__ void __launch_bounds__(kThreads) k_amax_hadamard(const uint32_t *__re
   block_max_to(m_rot, out_col, nullptr, status);
 }
 
-int grid_for(int64_t work) {
+int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+int grid_for(int64_t work) {
   int64_t want = ceil_div(work, kThreads);
-  int64_t cap = (int64_t)sms * 4;  // 4 resident 256-thread CTAs per SM, 4 loads each
+  int64_t cap = (int64_t)sm_count() * 4;  // 4 resident 256-thread CTAs per SM, 4 loads each
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+// Launch `kern` as a programmatic dependent launch after the zeroing kernel.
+template <typename... KArgs, typename... Args>
+fp4_status launch_after_zero(const ZeroList &z, void (*kern)(KArgs...), int grid, cudaStream_t s,
+                             Args... args) {
+  k_zero_outputs<<<1, 32, 0, s>>>(z);
+  if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 }  // namespace
@@ -138,25 +204,63 @@ fp4_status launch_amax(const void *x, int64_t rows, int64_t cols, int had_n, uin
                        float *amax_row, float *amax_col, cudaStream_t s) {
   uint32_t *status = status_word();
   if (!status) return FP4_ERR_CUDA;
-  if (cudaMemsetAsync(amax_row, 0, sizeof(float), s) != cudaSuccess) return FP4_ERR_CUDA;
-  if (amax_col && cudaMemsetAsync(amax_col, 0, sizeof(float), s) != cudaSuccess)
-    return FP4_ERR_CUDA;
+  ZeroList z{};
+  z.p[0] = amax_row;
+  z.p[1] = amax_col;
   int64_t n = rows * cols;
-  if (n == 0) return FP4_OK;
-  if (had_n == 0 || amax_col == nullptr) {
-    int64_t n16 = n / 8;
-    k_amax_plain<<<grid_for(n16), kThreads, 0, s>>>(reinterpret_cast<const uint4 *>(x), n16,
-                                                   amax_row, amax_col, status);
-  } else {
-    int64_t items = (rows / had_n) * (cols / 2);
-    if (had_n == 16)
-      k_amax_hadamard<16><<<grid_for(items), kThreads, 0, s>>>(
-          reinterpret_cast<const uint32_t *>(x), rows, cols, signs, amax_row, amax_col, status);
-    else
-      k_amax_hadamard<32><<<grid_for(items), kThreads, 0, s>>>(
-          reinterpret_cast<const uint32_t *>(x), rows, cols, signs, amax_row, amax_col, status);
+  if (n == 0) {
+    k_zero_outputs<<<1, 32, 0, s>>>(z);
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+  if (had_n == 0 || amax_col == nullptr) {
+    const int64_t n16 = n / 8;
+    return launch_after_zero(z, k_amax_plain, grid_for(n16), s, reinterpret_cast<const uint4 *>(x),
+                             n16, amax_row, amax_col, status);
+  }
+  const int64_t items = (rows / had_n) * (cols / 2);
+  const uint32_t *xw = reinterpret_cast<const uint32_t *>(x);
+  if (had_n == 16)
+    return launch_after_zero(z, k_amax_hadamard<16>, grid_for(items), s, xw, rows, cols, signs,
+                             amax_row, amax_col, status);
+  return launch_after_zero(z, k_amax_hadamard<32>, grid_for(items), s, xw, rows, cols, signs,
+                           amax_row, amax_col, status);
+}
+
+fp4_status launch_amax_many(const void *const *x, const int64_t *n_elems, float *const *amax, int n,
+                            cudaStream_t s) {
+  if (n < 0 || n > kMaxAmaxJobs) return FP4_ERR_INVALID_ARG;
+  AmaxMany a{};
+  a.status = status_word();
+  if (!a.status) return FP4_ERR_CUDA;
+  ZeroList z{};
+  int64_t total = 0;
+  for (int k = 0; k < n; ++k) {
+    z.p[k] = amax[k];
+    total += n_elems[k] / 8;
+  }
+  if (total == 0) {
+    k_zero_outputs<<<1, 32, 0, s>>>(z);
+    return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+  }
+  // CTAs in proportion to each tensor's chunks (at least one per non-empty
+  // tensor), about four per SM in all.
+  const int64_t cap = (int64_t)sm_count() * 4;
+  int blocks = 0;
+  for (int k = 0; k < n; ++k) {
+    const int64_t n16 = n_elems[k] / 8;
+    if (n16 == 0) continue;
+    int64_t nb = (cap * n16 + total - 1) / total;
+    const int64_t want = ceil_div(n16, kThreads);
+    nb = nb < want ? nb : want;
+    a.x[a.n] = reinterpret_cast<const uint4 *>(x[k]);
+    a.n16[a.n] = n16;
+    a.out[a.n] = amax[k];
+    a.first[a.n] = blocks;
+    blocks += (int)(nb > 0 ? nb : 1);
+    ++a.n;
+  }
+  a.first[a.n] = blocks;
+  return launch_after_zero(z, k_amax_many, blocks, s, a);
 }
 
 }  // namespace fp4

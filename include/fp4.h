@@ -125,6 +125,23 @@ fp4_status fp4_amax(const void *x_bf16, int64_t rows, int64_t cols,
                     int32_t hadamard_n, uint32_t hadamard_signs,
                     float *amax_row_dev, float *amax_col_dev, void *stream);
 
+/* Plain amax (hadamard_n == 0 above) of several BF16 tensors in one launch
+ * ([UE5M3] Approach: on a refresh step every operand's amax cache is
+ * recomputed; batching them lets the small tensors share the GPU with the
+ * large ones).  jobs[k].amax_dev receives max |x_k|, exactly as fp4_amax
+ * would write it.  n in [0, FP4_AMAX_MAX_JOBS]; per job: rows, cols >= 0,
+ * cols % 8 == 0, x 16-byte aligned (may be NULL when empty; then the amax
+ * is 0), amax_dev non-NULL and 4-byte aligned.  Inf/NaN sets
+ * FP4_ERR_NONFINITE in the status word.  Argument errors are returned
+ * before anything is launched. */
+#define FP4_AMAX_MAX_JOBS 8
+typedef struct {
+  const void *x_bf16;
+  int64_t rows, cols;
+  float *amax_dev;
+} fp4_amax_job;
+fp4_status fp4_amax_many(const fp4_amax_job *jobs, int32_t n, void *stream);
+
 /* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
  * payload, RNE or SR, zero-scale rule, 2D weight tiles):
  *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);

@@ -78,3 +78,24 @@ def test_invalid_arguments_rejected_before_any_launch(L):
     A = fq.fp4_operand(None, None, None, None, 0, 4, 64)
     B = fq.fp4_operand(None, None, None, None, 1, 8, 64)
     assert fq.fp4_gemm(A, B, 4, 8, 64, None, 0, 0, stream=type("S", (), {"cuda_stream": 0})()) == 1
+
+
+def test_amax_many_argument_errors_before_any_launch(L):
+    job = fq.fp4_amax_job
+    arr = (job * 9)()
+    assert L.fp4_amax_many(arr, 9, None) == 1  # more than FP4_AMAX_MAX_JOBS
+    assert L.fp4_amax_many(None, 1, None) == 1
+    assert L.fp4_amax_many(arr, -1, None) == 1
+    arr[0] = job(None, 4, 16, None)  # no output
+    assert L.fp4_amax_many(arr, 1, None) == 1
+    arr[0] = job(None, 4, 16, 256)  # data missing for a non-empty tensor
+    assert L.fp4_amax_many(arr, 1, None) == 1
+    arr[0] = job(4096, 4, 12, 256)  # cols % 8
+    assert L.fp4_amax_many(arr, 1, None) == 3
+    arr[0] = job(4104, 4, 16, 256)  # x not 16-byte aligned
+    assert L.fp4_amax_many(arr, 1, None) == 2
+    arr[0] = job(4096, 4, 16, 258)  # output not 4-byte aligned
+    assert L.fp4_amax_many(arr, 1, None) == 2
+    arr[0] = job(4096, 4, 16, 256)
+    arr[1] = job(4096, -1, 16, 256)  # a later job is checked too
+    assert L.fp4_amax_many(arr, 2, None) == 1

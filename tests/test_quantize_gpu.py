@@ -232,6 +232,42 @@ def test_empty_inputs_write_s_dec_only():
     assert ar.item() == 0.0
 
 
+def test_amax_many_matches_oracle_and_restarts_each_call():
+    """Several tensors in one launch (large, ragged, single-row, all-zero with
+    -0.0, empty): each amax equals the oracle's; a second call into the same
+    outputs with smaller tensors reports their own (smaller) maxima."""
+    need_gpu()
+    g = torch.Generator().manual_seed(9)
+    big = torch.randn((1024, 4096), generator=g)
+    big[517, 3001] = -37.5
+    shapes = [big, torch.randn((13, 40), generator=g), torch.randn((1, 8), generator=g) * 1e-3,
+              torch.zeros((64, 64)), torch.zeros((0, 64)), torch.randn((300, 2056), generator=g)]
+    shapes[3][5, 7] = -0.0
+    xs = [t.to(torch.bfloat16).cuda() for t in shapes]
+    outs = fq.amax_many(xs)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    for t, o in zip(xs, outs):
+        assert o.item() == float(orc.amax(f32(t.cpu()))), t.shape
+    small = [x * 0.25 for x in xs]
+    fq._check(fq.fp4_amax_many(small, outs), "fp4_amax_many")
+    for t, o in zip(small, outs):
+        assert o.item() == float(orc.amax(f32(t.cpu()))), t.shape
+    # the per-tensor entry point gives the same values
+    for t, o in zip(small, outs):
+        a, b = fq.amax(t)
+        assert a.item() == b.item() == o.item()
+
+
+def test_amax_many_reports_nonfinite():
+    need_gpu()
+    a = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
+    b[7, 9] = float("nan")
+    fq.amax_many([a, b])
+    assert fq.fp4_status_sync() == 7  # FP4_ERR_NONFINITE
+    assert fq.fp4_status_sync() == fq.FP4_OK
+
+
 def test_nonfinite_amax_is_reported():
     need_gpu()
     x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
