@@ -48,7 +48,7 @@ __device__ __forceinline__ void block_max_to(uint32_t v, float *out_a, float *ou
     w = warp_max(w);
     if (threadIdx.x == 0) {
       if (w >= 0x7F800000u) raise_status(status, kStatusNonfinite);
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // the outputs are zeroed
+      dependent_wait();  // the outputs are zeroed
       if (out_a) atomicMax(reinterpret_cast<unsigned int *>(out_a), w);
       if (out_b) atomicMax(reinterpret_cast<unsigned int *>(out_b), w);
     }
@@ -186,16 +186,9 @@ fp4_status launch_after_zero(const ZeroList &z, void (*kern)(KArgs...), int grid
                              Args... args) {
   k_zero_outputs<<<1, 32, 0, s>>>(z);
   if (cudaGetLastError() != cudaSuccess) return FP4_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kThreads), 0, s, args...) == cudaSuccess
+             ? FP4_OK
+             : FP4_ERR_CUDA;
 }
 
 }  // namespace

@@ -24,6 +24,32 @@ __device__ __forceinline__ void raise_status(uint32_t *status, uint32_t bit) {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch: a kernel launched by launch_dependent may
+// start while the previous kernel on the stream is finishing; before it
+// reads what that kernel wrote it waits for its completion and memory
+// (dependent_wait, a no-op in a kernel launched normally).  Used for the
+// short kernels that follow a small predecessor (amax after the zeroing of
+// its outputs, the UE5M3 remap after its producer); for the producers and
+// GEMMs it measured no gain.
+__device__ __forceinline__ void dependent_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }

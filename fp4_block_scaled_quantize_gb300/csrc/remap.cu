@@ -94,7 +94,7 @@ struct RemapArgs {
 // of rows l, l+32, l+64, l+96.  Warp w takes tiles w, w + 32, ...; per-row
 // code maxima and minima meet in shared memory.
 __global__ void __launch_bounds__(kRThreads, 1) k_remap_ue5m3(const __grid_constant__ RemapArgs args) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the producer's scales are complete
+  dependent_wait();  // the producer's scales are complete
   __shared__ uint32_t wmax[kRWarps][128], wmin[kRWarps][128];
   __shared__ float inv_s[128];
   __shared__ uint32_t delta_s[128];
@@ -254,17 +254,10 @@ fp4_status launch_remap_ue5m3(const RemapCopy *copies, int n, cudaStream_t s) {
   }
   if (k == 0) return FP4_OK;
   args.groups0 = groups[0];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(groups[0] + groups[1]));
-  cfg.blockDim = dim3(kRThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_remap_ue5m3, args) == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+  return launch_dependent(k_remap_ue5m3, dim3((unsigned)(groups[0] + groups[1])), dim3(kRThreads),
+                          0, s, args) == cudaSuccess
+             ? FP4_OK
+             : FP4_ERR_CUDA;
 }
 
 fp4_status launch_remap_ue5m3(uint8_t *sf_mma, const uint8_t *q, int64_t rows, int64_t cols,
