@@ -696,8 +696,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int rr = 0; rr < 4; ++rr) {
             const int64_t mm = grp_m + rr;
             if (mm < p.M && n < p.N)
-              *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.D) + mm * p.N + n) =
-                  make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]);
+              __stcs(reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.D) + mm * p.N + n),
+                     make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]));
           }
         } else {
 #pragma unroll
@@ -711,8 +711,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int rr = 0; rr < 4; ++rr) {
               const int64_t mm = grp_m + rr;
               if (mm < p.M && n < p.N)
-                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.D) + mm * p.N + n) =
-                    make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]);
+                __stcs(reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.D) + mm * p.N + n),
+                       make_uint4(w[4 * rr], w[4 * rr + 1], w[4 * rr + 2], w[4 * rr + 3]));
             }
           }
         }
