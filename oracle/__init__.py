@@ -69,6 +69,7 @@ def lib():
             "orc_gemm_model": (None, [u8p, u8p, u8p, u8p, i32, i64, i64, i64, f32, f32, i32,
                                       i64p, i64p, i64, f32p, f64p, f64p]),
             "orc_canon1024": (f32, [f32]),
+            "orc_mxfp4_to_fp8": (None, [u8p, u8p, i64, i64, u8p, f32p]),
             "orc_round_sum_f32": (f32, [f64p, i32, i32]),
         }
         for name, (res, args) in sig.items():
@@ -285,6 +286,22 @@ def remap_ue5m3(sf, q):
     fails = lib().orc_remap_ue5m3(_p(sf, ctypes.c_uint8), _p(q, ctypes.c_uint8), R, Cb,
                                   _p(out, ctypes.c_uint8), _p(shift, ctypes.c_int8))
     return out, shift, fails
+
+
+# --------------------------------------------------- FP4 -> FP8 re-encoding
+
+def mxfp4_to_fp8(q, sf):
+    """MXFP4-b32 copy (q [R][C/2] bytes, plain E8M0 scales [R][C/32]) ->
+    (E4M3 bytes [R][C], binary32 scales [R][C/128]); see orc_mxfp4_to_fp8."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    R, C = q.shape[0], q.shape[1] * 2
+    assert C % 128 == 0 and sf.shape == (R, C // 32)
+    q8 = np.zeros((R, C), np.uint8)
+    s8 = np.zeros((R, C // 128), np.float32)
+    lib().orc_mxfp4_to_fp8(_p(q, ctypes.c_uint8), _p(sf, ctypes.c_uint8), R, C,
+                           _p(q8, ctypes.c_uint8), _p(s8, ctypes.c_float))
+    return q8, s8
 
 
 # ------------------------------------------------------------------ GEMM

@@ -669,3 +669,44 @@ void orc_gemm_model(const uint8_t *qa, const uint8_t *sfa,
     s_abs[t] = acc_to_f64(&absacc) * alpha_exact;
   }
 }
+
+/* ===================================================================== */
+/* Direct MXFP4 -> FP8 re-encoding ([HOP] Method: a bit-wise FP4-to-FP8    */
+/* conversion without a BF16 intermediate; hierarchical scale alignment     */
+/* bridges MXFP4's 32-element E8M0 blocks and FP8's 128-element blocks).    */
+/* Reading (the page gives the idea, not the constants): the 128 elements   */
+/* of an FP8 block are four MXFP4 blocks with exponents E_i (E8M0 code -    */
+/* 127; code 255 read as 128); their common scale is 2^(max E_i - 6), the   */
+/* offset 6 being the largest k with 6 * 2^k <= 448 (E4M3's largest value), */
+/* and element j of block i becomes the E4M3 code nearest to                */
+/* |e2m1(q_j)| * 2^(E_i - max E + 6), ties to the even code, with the E2M1  */
+/* sign bit copied (so -0 stays -0).  Blocks up to 14 binades below the     */
+/* largest convert exactly; smaller ones round into E4M3's subnormals.      */
+/* ===================================================================== */
+static double e4m3_mag(int code) { return orc_e4m3_value(code & 0x7F); }
+
+void orc_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
+                      uint8_t *q8, float *s8) {
+  const int64_t cb32 = C / 32, cb128 = C / 128;
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < cb128; ++b) {
+      int emax = -1000;
+      for (int i = 0; i < 4; ++i) {
+        int e = (int)sf[r * cb32 + 4 * b + i] - 127;
+        if (e > emax) emax = e;
+      }
+      s8[r * cb128 + b] = (float)ldexp(1.0, emax - 6);
+      for (int i = 0; i < 4; ++i) {
+        int e = (int)sf[r * cb32 + 4 * b + i] - 127;
+        for (int j = 0; j < 32; ++j) {
+          int64_t col = 128 * b + 32 * i + j;
+          int nib = (q[r * (C / 2) + col / 2] >> (4 * (col & 1))) & 15;
+          double t = fabs(orc_e2m1_value(nib)) * ldexp(1.0, e - emax + 6);
+          int code = encode_rne_sat(t, 0x7E, e4m3_mag);
+          if (nib & 8) code |= 0x80;
+          q8[r * C + col] = (uint8_t)code;
+        }
+      }
+    }
+  }
+}

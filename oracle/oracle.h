@@ -14,7 +14,9 @@
  *   [FAF]    "Format-Aware Fusion for Fast FP4 Pretraining" -- Abstract
  *            (row-gradient stochastic rounding, fixed-sign 32-point Hadamard)
  *   [HOP]    "Practical FP4 Training for Large-Scale MoE Models on Hopper
- *            GPUs" -- Method (MXFP4 = E2M1 payload, block 32)
+ *            GPUs" -- Method (MXFP4 = E2M1 payload, block 32; direct
+ *            bit-wise FP4-to-FP8 conversion with hierarchical scale
+ *            alignment, MXFP4-b32 -> E4M3-b128)
  *
  * Pinned by tests/test_oracle_pins.py except where a function says
  * "parity unpinned".
@@ -72,6 +74,13 @@ int64_t orc_sf_mma_bytes(int64_t R, int64_t Cb);
 void orc_sf_to_mma(const uint8_t *sf, int64_t R, int64_t Cb, uint8_t *out);
 int orc_remap_ue5m3(const uint8_t *sf, const uint8_t *q, int64_t R,
                     int64_t Cb, uint8_t *sf_e4m3, int8_t *shift);
+
+/* ---- FP4 -> FP8 re-encoding ------------------------------------------------ */
+/* [HOP] Method (direct bit-wise FP4-to-FP8 conversion, hierarchical scale
+ * alignment): MXFP4-b32 row-wise copy (q [R][C/2], E8M0 sf [R][C/32]) ->
+ * E4M3 payload q8 [R][C] and binary32 scales s8 [R][C/128]; C % 128 == 0. */
+void orc_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
+                      uint8_t *q8, float *s8);
 
 /* ---- GEMM models ----------------------------------------------------------- */
 void orc_gemm_model(const uint8_t *qa, const uint8_t *sfa,

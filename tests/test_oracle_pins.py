@@ -573,3 +573,70 @@ def test_model_b32_scales_equal_duplicated_b16_scales():
     np.testing.assert_array_equal(y32, y16)
     np.testing.assert_array_equal(e32, e16)
     np.testing.assert_array_equal(s32, s16)
+
+
+# ------------------------------------------------ MXFP4 -> FP8 re-encoding
+# ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs", Method:
+# direct bit-wise FP4-to-FP8 conversion with hierarchical scale alignment.)
+
+def _fp8_block(codes, nibbles):
+    """One 128-element row: four E8M0 codes, 128 nibbles (element j's nibble
+    in the low half of byte j/2 when j is even)."""
+    nib = np.asarray(nibbles, np.uint8)
+    q = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)[None, :]
+    return orc.mxfp4_to_fp8(q, np.asarray([codes], np.uint8))
+
+
+def test_fp8_reencode_worked_examples():
+    # E = 3, 1, -17, 0 -> common scale 2^(3 - 6); element = |e2m1| * 2^(E_i - 3 + 6)
+    nib = [7] * 32 + [7, 1] + [7] * 30 + [7, 0xF] + [7] * 30 + [3, 0xB, 0, 8] + [3] * 28
+    q8, s8 = _fp8_block([130, 128, 110, 127], nib)
+    assert s8[0, 0] == 0.125
+    # 6 * 2^6 = 384 = 1.5 * 2^8: exponent field 15, mantissa 100b
+    assert q8[0, 0] == 0x7C
+    # 6 * 2^4 = 96 = 1.5 * 2^6 -> 0x6C; 0.5 * 2^4 = 8 = 2^3 -> field 10 -> 0x50
+    assert q8[0, 32] == 0x6C and q8[0, 33] == 0x50
+    # 20 binades down: 6 * 2^-14 is 0.1875 units of 2^-9 -> rounds to +-0
+    assert q8[0, 64] == 0x00 and q8[0, 65] == 0x80
+    # 1.5 * 2^3 = 12 = 1.5 * 2^3 -> field 10, mantissa 100b -> 0x54 (and negative)
+    assert q8[0, 96] == 0x54 and q8[0, 97] == 0xD4
+    # +0 and -0 keep their sign
+    assert q8[0, 98] == 0x00 and q8[0, 99] == 0x80
+
+
+def test_fp8_reencode_subnormal_rounding():
+    # d = 15 and 16 below the block maximum: values land on E4M3's 2^-9 grid
+    nib = [7] * 32 + [7, 3, 1, 2] + [0] * 28 + [7, 3, 5] + [0] * 29 + [0] * 32
+    q8, _ = _fp8_block([142, 127, 126, 0], nib)
+    # d = 15: 6*2^-9 = 6 units; 1.5*2^-9 = 1.5 units -> 2 (even); 0.5 units -> 0 (even); 1 unit
+    assert list(q8[0, 32:36]) == [0x06, 0x02, 0x00, 0x01]
+    # d = 16: 6*2^-10 = 3 units; 1.5*2^-10 = 0.75 -> 1; 3*2^-10 = 1.5 -> 2 (even)
+    assert list(q8[0, 64:67]) == [0x03, 0x01, 0x02]
+    # code 0 is 142 binades below: all zero
+    assert not q8[0, 96:].any()
+
+
+def test_fp8_reencode_scale_is_power_of_two_with_subnormal_range():
+    q8, s8 = _fp8_block([0, 0, 0, 0], [2] * 128)
+    assert s8[0, 0] == np.float32(2.0 ** -133)  # a binary32 subnormal, exact
+    assert (q8 == 0x68).all()  # 1.0 * 2^6 = 64: field 6 + 7 = 13, mantissa 0
+    q8, s8 = _fp8_block([254, 200, 254, 3], [7] * 128)
+    assert s8[0, 0] == np.float32(2.0 ** 121)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fp8_reencode_is_exact_within_fourteen_binades(seed):
+    """Dequantised FP8 equals dequantised MXFP4 element for element whenever
+    every block is at most 14 binades below its FP8 block's largest one."""
+    rng = np.random.default_rng(seed)
+    R, C = 37, 512
+    q = rng.integers(0, 256, size=(R, C // 2), dtype=np.uint8)
+    base = rng.integers(20, 230, size=(R, C // 128, 1))
+    sf = (base - rng.integers(0, 15, size=(R, C // 128, 4))).reshape(R, C // 32).astype(np.uint8)
+    q8, s8 = orc.mxfp4_to_fp8(q, sf)
+    nib = np.stack([q & 15, q >> 4], axis=-1).reshape(R, C)
+    fp4 = np.vectorize(orc.e2m1_value)(nib) * np.ldexp(1.0, np.repeat(sf.astype(int) - 127, 32, 1))
+    fp8 = np.vectorize(orc.e4m3_value)(q8) * np.repeat(s8.astype(np.float64), 128, 1)
+    assert np.array_equal(fp4, fp8)
+    # and the signs of zeros survive
+    assert np.array_equal(nib >= 8, q8 >= 0x80)
