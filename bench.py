@@ -296,6 +296,7 @@ def run_gpu(args, world, rank, local):
 
     # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     fused = run_fused_producer(layer, flush)
+    reencode = run_reencode(layer, flush, pk["hbm_gbs"])
     linear = run_linear(layer, flush)
     e2e = run_e2e(layer, args, world, ideal, graph)
 
@@ -329,6 +330,7 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": layer.launches_per_step * args.steps,
         "e2e": e2e,
         "epilogue_fused_producer": fused,
+        "mxfp4_to_fp8": reencode,
         "linear_layer": linear,
     }
     if rank == 0:
@@ -393,6 +395,26 @@ def run_fused_producer(layer, flush):
             "fused_ms": round(t_f, 4), "unfused_ms": round(t_u, 4),
             "hbm_bytes_avoided": 2 * M_TOK * N_MODEL * 2,
             "note": "fused quantises the binary32 product; unfused quantises the stored BF16 Y"}
+
+
+def run_reencode(layer, flush, hbm_gbs):
+    """Direct MXFP4-b32 -> FP8 E4M3-b128 re-encoding (fp4_mxfp4_to_fp8) of X's
+    MXFP4 row-wise copy, 8192 x 14336: 0.5 + 1/32 B read and 1 + 4/128 B
+    written per element."""
+    fq = layer.fq
+    p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
+    mx = fq.quantize(layer.X, layer.amax["X"][0], p)
+    sf = mx.sf.view(M_TOK, K_FF // 32)
+    q8 = torch.empty((M_TOK, K_FF), dtype=torch.uint8, device=layer.X.device)
+    s8 = torch.empty((M_TOK, K_FF // 128), dtype=torch.float32, device=layer.X.device)
+    run = lambda: fq._check(fq.fp4_mxfp4_to_fp8(mx.q, sf, M_TOK, K_FF, q8, s8), "reencode")
+    run()
+    ms = graph_ms(run, flush)
+    nbytes = M_TOK * K_FF * (0.5 + 1 / 32 + 1 + 4 / 128)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"shape": [M_TOK, K_FF], "ms": round(ms, 4), "gbs": round(gbs, 1),
+            "frac": round(gbs / hbm_gbs, 4), "bytes_per_launch": int(nbytes),
+            "bound": "hbm"}
 
 
 def run_linear(layer, flush, steps=10):
@@ -637,6 +659,14 @@ def run_profile(args, local):
         "dgrad": lambda: fq.gemm(layer.dyr, layer.wc, out=layer.dX),
         "wgrad": lambda: fq.gemm(layer.dyc, layer.xc, out=layer.dW),
     }
+    if args.profile == "reencode":
+        p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
+        mx = fq.quantize(layer.X, layer.amax["X"][0], p)
+        sf = mx.sf.view(M_TOK, K_FF // 32)
+        q8 = torch.empty((M_TOK, K_FF), dtype=torch.uint8, device=layer.X.device)
+        s8 = torch.empty((M_TOK, K_FF // 128), dtype=torch.float32, device=layer.X.device)
+        ops["reencode"] = lambda: fq._check(fq.fp4_mxfp4_to_fp8(mx.q, sf, M_TOK, K_FF, q8, s8),
+                                            "reencode")
     torch.cuda.synchronize()
     for _ in range(3):
         ops[args.profile]()
@@ -655,7 +685,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", default=None,
-                    choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad"],
+                    choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad",
+                             "reencode"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     world, rank, local = dist_init()

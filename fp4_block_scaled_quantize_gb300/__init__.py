@@ -57,7 +57,7 @@ class FP4Error(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
+EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
            "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync", "fp4_status_string")
 
 
@@ -74,6 +74,7 @@ def lib():
         op = ctypes.POINTER(fp4_operand)
         L.fp4_amax.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp]
         L.fp4_amax_many.argtypes = [ctypes.POINTER(fp4_amax_job), i32, vp]
+        L.fp4_mxfp4_to_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp]
         L.fp4_quantize.argtypes = [vp, i64, i64, vp, qp, vp, vp, vp, vp, vp]
         L.fp4_quantize_transpose.argtypes = [vp, i64, i64, vp, vp, qp, vp, vp, vp, vp, vp, vp, vp,
                                              vp, vp]
@@ -86,7 +87,7 @@ def lib():
         L.fp4_status_sync.argtypes = [vp]
         L.fp4_status_string.argtypes = [i32]
         L.fp4_status_string.restype = ctypes.c_char_p
-        for f in ("fp4_amax", "fp4_amax_many", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
+        for f in ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
@@ -133,6 +134,11 @@ def fp4_amax_many(xs, outs, stream=None):
         rows, cols = x.shape
         jobs[k] = fp4_amax_job(x.data_ptr() if x.numel() else None, rows, cols, o.data_ptr())
     return lib().fp4_amax_many(jobs, n, _stream(stream))
+
+
+def fp4_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, stream=None):
+    return lib().fp4_mxfp4_to_fp8(_ptr(q), _ptr(sf), rows, cols, _ptr(q8), _ptr(s8),
+                                  _stream(stream))
 
 
 def fp4_quantize(x, amax, p, q, sf, s_dec, row_shift=None, stream=None):
@@ -232,6 +238,17 @@ def amax_many(xs, stream=None):
     outs = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
     _check(fp4_amax_many(xs, outs, stream), "fp4_amax_many")
     return outs
+
+
+def mxfp4_to_fp8(q, sf, stream=None):
+    """FP8 E4M3-b128 copy (q8 uint8 [R][C], s8 float32 [R][C/128]) of an
+    MXFP4-b32 row-wise copy given by its payload q [R][C/2] and plain-layout
+    E8M0 scales sf [R][C/32]."""
+    rows, cols = q.shape[0], q.shape[1] * 2
+    q8 = torch.empty((rows, cols), dtype=torch.uint8, device=q.device)
+    s8 = torch.empty((rows, cols // 128), dtype=torch.float32, device=q.device)
+    _check(fp4_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, stream), "fp4_mxfp4_to_fp8")
+    return q8, s8
 
 
 def quantize(x, amax_dev, p, remap=True, stream=None):

@@ -26,6 +26,7 @@ UNITS = {
     "amax.cu": ["-fmad=false"],
     "quantize.cu": ["-fmad=false"],
     "remap.cu": ["-fmad=false"],
+    "convert.cu": ["-fmad=false"],
     "gemm.cu": [],
 }
 

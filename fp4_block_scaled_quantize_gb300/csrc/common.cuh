@@ -68,6 +68,10 @@ inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s
 // Enqueue-only entry points launched by abi.cu.
 fp4_status launch_amax(const void *x, int64_t rows, int64_t cols, int had_n, uint32_t signs,
                        float *amax_row, float *amax_col, cudaStream_t s);
+// MXFP4-b32 row-wise copy -> E4M3 payload + binary32 scale per 128 elements.
+fp4_status launch_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
+                               uint8_t *q8, float *s8, cudaStream_t s);
+
 // Plain amax of n <= FP4_AMAX_MAX_JOBS BF16 tensors (n_elems[k] % 8 == 0)
 // in one launch.
 fp4_status launch_amax_many(const void *const *x, const int64_t *n_elems, float *const *amax, int n,

@@ -96,3 +96,23 @@ def down_proj_8b(seed=0, M=8192, K=14336, N=4096):
 def sweep_operand(rows, cols, seed=7):
     g = _gen(seed)
     return bf16(_scale_entries(_normal((rows, cols), 1.0, g), 0.01, 50.0, g))
+
+
+def mxfp4_copy(rows, cols, seed=11, spread=20):
+    """Random bytes in the shape of an MXFP4-b32 row-wise copy, for the FP8
+    re-encoding: payload [rows][cols/2] (uniform bytes, so every E2M1 code
+    and sign appears) and E8M0 codes [rows][cols/32].  Per 128 columns the
+    four codes are a base in [spread, 254] minus 0..spread each, so the
+    blocks of one FP8 block lie up to `spread` binades apart; a few codes are
+    pinned to the extremes 0, 254 and 255.  Returns uint8 tensors."""
+    g = _gen(seed)
+    q = torch.randint(0, 256, (rows, cols // 2), generator=g, dtype=torch.int32)
+    nb = cols // 128
+    base = torch.randint(spread, 255, (rows, nb, 1), generator=g, dtype=torch.int32)
+    off = torch.randint(0, spread + 1, (rows, nb, 4), generator=g, dtype=torch.int32)
+    sf = (base - off).reshape(rows, cols // 32)
+    if sf.numel() >= 12:
+        flat = sf.view(-1)
+        idx = torch.randperm(flat.numel(), generator=g)[:3]
+        flat[idx] = torch.tensor([0, 254, 255], dtype=torch.int32)
+    return q.to(torch.uint8), sf.to(torch.uint8)

@@ -142,6 +142,21 @@ typedef struct {
 } fp4_amax_job;
 fp4_status fp4_amax_many(const fp4_amax_job *jobs, int32_t n, void *stream);
 
+/* Direct re-encoding of an MXFP4 copy as FP8 ([HOP] Method: bit-wise
+ * FP4-to-FP8 conversion with hierarchical scale alignment, no BF16
+ * intermediate).  Input: an MXFP4_B32 row-wise copy in the plain scale
+ * layout -- q [rows][cols/2] (element 2j in the low nibble of byte j), sf
+ * [rows][cols/32] E8M0 codes.  Output: q8 [rows][cols] E4M3 codes and s8
+ * [rows][cols/128] binary32 scales, x = e4m3(q8) * s8.  Per 128 elements
+ * (four MXFP4 blocks, exponents E_i = code - 127): s8 = 2^(max E_i - 6) and
+ * q8 = the nearest-even E4M3 code of |e2m1| * 2^(E_i - max E + 6), sign
+ * copied (-0 stays -0); exact for blocks up to 14 binades below the
+ * largest, rounded into E4M3's subnormals below that.  Shapes: cols % 128
+ * == 0; rows == 0 or cols == 0 writes nothing.  Alignment: q, q8 16 bytes;
+ * sf, s8 4 bytes.  The caller owns every buffer. */
+fp4_status fp4_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows,
+                            int64_t cols, uint8_t *q8, float *s8, void *stream);
+
 /* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
  * payload, RNE or SR, zero-scale rule, 2D weight tiles):
  *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);

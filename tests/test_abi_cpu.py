@@ -99,3 +99,12 @@ def test_amax_many_argument_errors_before_any_launch(L):
     arr[0] = job(4096, 4, 16, 256)
     arr[1] = job(4096, -1, 16, 256)  # a later job is checked too
     assert L.fp4_amax_many(arr, 2, None) == 1
+
+
+def test_mxfp4_to_fp8_argument_errors_before_any_launch(L):
+    assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 96, 4096, 4096, None) == 3  # cols % 128
+    assert L.fp4_mxfp4_to_fp8(4096, 4096, -1, 128, 4096, 4096, None) == 1
+    assert L.fp4_mxfp4_to_fp8(None, 4096, 4, 128, 4096, 4096, None) == 1
+    assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 128, 4104, 4096, None) == 2  # q8 alignment
+    assert L.fp4_mxfp4_to_fp8(4096, 4098, 4, 128, 4096, 4096, None) == 2  # sf alignment
+    assert L.fp4_mxfp4_to_fp8(None, None, 0, 128, None, None, None) == 0  # empty: nothing to do
