@@ -70,6 +70,7 @@ def lib():
                                       i64p, i64p, i64, f32p, f64p, f64p]),
             "orc_canon1024": (f32, [f32]),
             "orc_mxfp4_to_fp8": (None, [u8p, u8p, i64, i64, u8p, f32p]),
+            "orc_mxfp4_to_fp8_t": (None, [u8p, u8p, i64, i64, u8p, f32p]),
             "orc_round_sum_f32": (f32, [f64p, i32, i32]),
         }
         for name, (res, args) in sig.items():
@@ -302,6 +303,20 @@ def mxfp4_to_fp8(q, sf):
     lib().orc_mxfp4_to_fp8(_p(q, ctypes.c_uint8), _p(sf, ctypes.c_uint8), R, C,
                            _p(q8, ctypes.c_uint8), _p(s8, ctypes.c_float))
     return q8, s8
+
+
+def mxfp4_to_fp8_t(q, sf):
+    """The FP8 copy of x^T from x's MXFP4-b32 copy: (E4M3 bytes [C][R],
+    binary32 scales [C][R/128]); see orc_mxfp4_to_fp8_t."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    R, C = q.shape[0], q.shape[1] * 2
+    assert R % 128 == 0 and C % 32 == 0 and sf.shape == (R, C // 32)
+    q8t = np.zeros((C, R), np.uint8)
+    s8t = np.zeros((C, R // 128), np.float32)
+    lib().orc_mxfp4_to_fp8_t(_p(q, ctypes.c_uint8), _p(sf, ctypes.c_uint8), R, C,
+                             _p(q8t, ctypes.c_uint8), _p(s8t, ctypes.c_float))
+    return q8t, s8t
 
 
 # ------------------------------------------------------------------ GEMM

@@ -710,3 +710,31 @@ void orc_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
     }
   }
 }
+
+/* Transposed re-encoding: the FP8 copy of x^T, blocks of 128 consecutive
+ * rows of x within one column.  Element (r, c) of x has the exponent of its
+ * MXFP4 block, E(r, c) = sf[r][c/32] - 127; the block of column c over rows
+ * 128b .. 128b+127 aligns to their largest E and is encoded exactly as
+ * above. */
+void orc_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
+                        uint8_t *q8t, float *s8t) {
+  const int64_t cb32 = C / 32, rb128 = R / 128;
+  for (int64_t c = 0; c < C; ++c) {
+    for (int64_t b = 0; b < rb128; ++b) {
+      int emax = -1000;
+      for (int64_t r = 128 * b; r < 128 * b + 128; ++r) {
+        int e = (int)sf[r * cb32 + c / 32] - 127;
+        if (e > emax) emax = e;
+      }
+      s8t[c * rb128 + b] = (float)ldexp(1.0, emax - 6);
+      for (int64_t r = 128 * b; r < 128 * b + 128; ++r) {
+        int e = (int)sf[r * cb32 + c / 32] - 127;
+        int nib = (q[r * (C / 2) + c / 2] >> (4 * (c & 1))) & 15;
+        double t = fabs(orc_e2m1_value(nib)) * ldexp(1.0, e - emax + 6);
+        int code = encode_rne_sat(t, 0x7E, e4m3_mag);
+        if (nib & 8) code |= 0x80;
+        q8t[c * R + r] = (uint8_t)code;
+      }
+    }
+  }
+}

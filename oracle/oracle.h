@@ -81,6 +81,10 @@ int orc_remap_ue5m3(const uint8_t *sf, const uint8_t *q, int64_t R,
  * E4M3 payload q8 [R][C] and binary32 scales s8 [R][C/128]; C % 128 == 0. */
 void orc_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
                       uint8_t *q8, float *s8);
+/* The same re-encoding of the transpose ([HOP] Method: transpose fused into
+ * the conversion): q8t [C][R] E4M3, s8t [C][R/128]; R % 128 == 0. */
+void orc_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
+                        uint8_t *q8t, float *s8t);
 
 /* ---- GEMM models ----------------------------------------------------------- */
 void orc_gemm_model(const uint8_t *qa, const uint8_t *sfa,

@@ -640,3 +640,44 @@ def test_fp8_reencode_is_exact_within_fourteen_binades(seed):
     assert np.array_equal(fp4, fp8)
     # and the signs of zeros survive
     assert np.array_equal(nib >= 8, q8 >= 0x80)
+
+
+def test_fp8_reencode_transposed_worked_example():
+    """x [128][32]: one MXFP4 block per row; row r has exponent E_r.  Column
+    c of x^T aligns its 128 rows to max E_r."""
+    R, C = 128, 32
+    nib = np.zeros((R, C), np.uint8)
+    nib[:, 0] = 7          # +6 in column 0 of every row
+    nib[:, 1] = 0xB        # -1.5 in column 1
+    sf = np.full((R, 1), 127, np.uint8)
+    sf[5, 0] = 130         # row 5: E = 3 -> the column maximum
+    sf[9, 0] = 107         # row 9: E = -20, 23 binades below
+    sf[11, 0] = 112        # row 11: E = -15, 18 binades below
+    q = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    q8t, s8t = orc.mxfp4_to_fp8_t(q, sf)
+    assert q8t.shape == (C, R) and s8t.shape == (C, 1)
+    assert (s8t == 0.125).all()                    # 2^(3 - 6) for every column
+    assert q8t[0, 5] == 0x7C                       # 6 * 2^6 = 384
+    assert q8t[0, 0] == 0x64                       # 6 * 2^(0 - 3 + 6) = 48
+    assert q8t[1, 0] == 0xD4                       # -1.5 * 8 = -12
+    assert q8t[0, 9] == 0x00 and q8t[1, 9] == 0x80  # 23 binades down: +-0
+    assert q8t[0, 11] == 0x01                      # 6 * 2^-12 = 0.75 units of 2^-9 -> 1
+    assert (q8t[2:] == 0).all()
+
+
+def test_fp8_reencode_transposed_equals_rowwise_of_the_transpose():
+    """When every element of a 128-row block shares one exponent per column
+    group, re-encoding x^T is the row-wise re-encoding of the explicitly
+    transposed MXFP4 copy (same exponent per element)."""
+    rng = np.random.default_rng(4)
+    R, C = 256, 128
+    nib = rng.integers(0, 16, size=(R, C)).astype(np.uint8)
+    e_col = rng.integers(100, 150, size=(C // 32,))
+    sf = np.tile(e_col, (R, 1)).astype(np.uint8)            # E depends on the column group only
+    q = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    q8t, s8t = orc.mxfp4_to_fp8_t(q, sf)
+    nt = np.ascontiguousarray(nib.T)                          # x^T's nibbles
+    qt = (nt[:, 0::2] | (nt[:, 1::2] << 4)).astype(np.uint8)
+    sft = np.repeat(np.repeat(e_col, 32)[:, None], R // 32, axis=1).astype(np.uint8)
+    want_q8, want_s8 = orc.mxfp4_to_fp8(qt, sft)
+    assert np.array_equal(q8t, want_q8) and np.array_equal(s8t, want_s8)
