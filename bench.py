@@ -407,14 +407,20 @@ def run_reencode(layer, flush, hbm_gbs):
     sf = mx.sf.view(M_TOK, K_FF // 32)
     q8 = torch.empty((M_TOK, K_FF), dtype=torch.uint8, device=layer.X.device)
     s8 = torch.empty((M_TOK, K_FF // 128), dtype=torch.float32, device=layer.X.device)
+    q8t = torch.empty((K_FF, M_TOK), dtype=torch.uint8, device=layer.X.device)
+    s8t = torch.empty((K_FF, M_TOK // 128), dtype=torch.float32, device=layer.X.device)
     run = lambda: fq._check(fq.fp4_mxfp4_to_fp8(mx.q, sf, M_TOK, K_FF, q8, s8), "reencode")
+    run_t = lambda: fq._check(fq.fp4_mxfp4_to_fp8_transpose(mx.q, sf, M_TOK, K_FF, q8t, s8t),
+                              "reencode_t")
     run()
-    ms = graph_ms(run, flush)
+    run_t()
     nbytes = M_TOK * K_FF * (0.5 + 1 / 32 + 1 + 4 / 128)
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"shape": [M_TOK, K_FF], "ms": round(ms, 4), "gbs": round(gbs, 1),
-            "frac": round(gbs / hbm_gbs, 4), "bytes_per_launch": int(nbytes),
-            "bound": "hbm"}
+    out = {"shape": [M_TOK, K_FF], "bytes_per_launch": int(nbytes), "bound": "hbm"}
+    for key, fn in (("row", run), ("transposed", run_t)):
+        ms = graph_ms(fn, flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[key] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)}
+    return out
 
 
 def run_linear(layer, flush, steps=10):
@@ -659,7 +665,7 @@ def run_profile(args, local):
         "dgrad": lambda: fq.gemm(layer.dyr, layer.wc, out=layer.dX),
         "wgrad": lambda: fq.gemm(layer.dyc, layer.xc, out=layer.dW),
     }
-    if args.profile == "reencode":
+    if args.profile in ("reencode", "reencode_t"):
         p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
         mx = fq.quantize(layer.X, layer.amax["X"][0], p)
         sf = mx.sf.view(M_TOK, K_FF // 32)
@@ -667,6 +673,10 @@ def run_profile(args, local):
         s8 = torch.empty((M_TOK, K_FF // 128), dtype=torch.float32, device=layer.X.device)
         ops["reencode"] = lambda: fq._check(fq.fp4_mxfp4_to_fp8(mx.q, sf, M_TOK, K_FF, q8, s8),
                                             "reencode")
+        q8t = torch.empty((K_FF, M_TOK), dtype=torch.uint8, device=layer.X.device)
+        s8t = torch.empty((K_FF, M_TOK // 128), dtype=torch.float32, device=layer.X.device)
+        ops["reencode_t"] = lambda: fq._check(
+            fq.fp4_mxfp4_to_fp8_transpose(mx.q, sf, M_TOK, K_FF, q8t, s8t), "reencode_t")
     torch.cuda.synchronize()
     for _ in range(3):
         ops[args.profile]()
@@ -686,7 +696,7 @@ def main():
                     help="launch the timed steps kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", default=None,
                     choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad",
-                             "reencode"],
+                             "reencode", "reencode_t"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     world, rank, local = dist_init()

@@ -57,7 +57,8 @@ class FP4Error(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
+EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
+           "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
            "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync", "fp4_status_string")
 
 
@@ -75,6 +76,7 @@ def lib():
         L.fp4_amax.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp]
         L.fp4_amax_many.argtypes = [ctypes.POINTER(fp4_amax_job), i32, vp]
         L.fp4_mxfp4_to_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp]
+        L.fp4_mxfp4_to_fp8_transpose.argtypes = [vp, vp, i64, i64, vp, vp, vp]
         L.fp4_quantize.argtypes = [vp, i64, i64, vp, qp, vp, vp, vp, vp, vp]
         L.fp4_quantize_transpose.argtypes = [vp, i64, i64, vp, vp, qp, vp, vp, vp, vp, vp, vp, vp,
                                              vp, vp]
@@ -87,7 +89,8 @@ def lib():
         L.fp4_status_sync.argtypes = [vp]
         L.fp4_status_string.argtypes = [i32]
         L.fp4_status_string.restype = ctypes.c_char_p
-        for f in ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
+        for f in ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
+                  "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
@@ -139,6 +142,11 @@ def fp4_amax_many(xs, outs, stream=None):
 def fp4_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, stream=None):
     return lib().fp4_mxfp4_to_fp8(_ptr(q), _ptr(sf), rows, cols, _ptr(q8), _ptr(s8),
                                   _stream(stream))
+
+
+def fp4_mxfp4_to_fp8_transpose(q, sf, rows, cols, q8t, s8t, stream=None):
+    return lib().fp4_mxfp4_to_fp8_transpose(_ptr(q), _ptr(sf), rows, cols, _ptr(q8t), _ptr(s8t),
+                                            _stream(stream))
 
 
 def fp4_quantize(x, amax, p, q, sf, s_dec, row_shift=None, stream=None):
@@ -249,6 +257,18 @@ def mxfp4_to_fp8(q, sf, stream=None):
     s8 = torch.empty((rows, cols // 128), dtype=torch.float32, device=q.device)
     _check(fp4_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, stream), "fp4_mxfp4_to_fp8")
     return q8, s8
+
+
+def mxfp4_to_fp8_transpose(q, sf, stream=None):
+    """FP8 E4M3-b128 copy of x^T (q8t uint8 [C][R], s8t float32 [C][R/128])
+    from x's MXFP4-b32 row-wise copy (payload q [R][C/2], plain E8M0 scales
+    sf [R][C/32])."""
+    rows, cols = q.shape[0], q.shape[1] * 2
+    q8t = torch.empty((cols, rows), dtype=torch.uint8, device=q.device)
+    s8t = torch.empty((cols, rows // 128), dtype=torch.float32, device=q.device)
+    _check(fp4_mxfp4_to_fp8_transpose(q, sf, rows, cols, q8t, s8t, stream),
+           "fp4_mxfp4_to_fp8_transpose")
+    return q8t, s8t
 
 
 def quantize(x, amax_dev, p, remap=True, stream=None):

@@ -110,6 +110,16 @@ fp4_status fp4_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows, i
   return launch_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, as_stream(stream));
 }
 
+fp4_status fp4_mxfp4_to_fp8_transpose(const uint8_t *q, const uint8_t *sf, int64_t rows,
+                                      int64_t cols, uint8_t *q8t, float *s8t, void *stream) {
+  if (rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
+  if (rows % 128 != 0 || cols % 32 != 0) return FP4_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return FP4_OK;
+  if (!q || !sf || !q8t || !s8t) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(q8t) || !aligned4(s8t)) return FP4_ERR_ALIGNMENT;
+  return launch_mxfp4_to_fp8_t(q, sf, rows, cols, q8t, s8t, as_stream(stream));
+}
+
 fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const float *amax_dev,
                         const fp4_quant_params *p, uint8_t *q, uint8_t *sf, float *s_dec_dev,
                         int8_t *row_shift, void *stream) {

@@ -71,6 +71,9 @@ fp4_status launch_amax(const void *x, int64_t rows, int64_t cols, int had_n, uin
 // MXFP4-b32 row-wise copy -> E4M3 payload + binary32 scale per 128 elements.
 fp4_status launch_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
                                uint8_t *q8, float *s8, cudaStream_t s);
+// ... and the FP8 copy of its transpose (FP8 blocks of 128 rows per column).
+fp4_status launch_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
+                                 uint8_t *q8t, float *s8t, cudaStream_t s);
 
 // Plain amax of n <= FP4_AMAX_MAX_JOBS BF16 tensors (n_elems[k] % 8 == 0)
 // in one launch.

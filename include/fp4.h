@@ -157,6 +157,19 @@ fp4_status fp4_amax_many(const fp4_amax_job *jobs, int32_t n, void *stream);
 fp4_status fp4_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows,
                             int64_t cols, uint8_t *q8, float *s8, void *stream);
 
+/* The same re-encoding with the transpose fused in ([HOP] Method: the
+ * layout-aware kernel fuses transposition and the conversion): from the
+ * MXFP4_B32 row-wise copy of x [rows][cols] (as above) it writes the FP8
+ * copy of x^T -- q8t [cols][rows] E4M3 codes, s8t [cols][rows/128] binary32
+ * scales.  An FP8 block is 128 consecutive rows of one column of x; its
+ * scale is 2^(max E - 6) over those rows' MXFP4 exponents (E of element
+ * (r, c) = sf[r][c/32] - 127) and each element is encoded as above.
+ * Shapes: rows % 128 == 0, cols % 32 == 0; rows == 0 or cols == 0 writes
+ * nothing.  Alignment: q, q8t 16 bytes; s8t 4 bytes. */
+fp4_status fp4_mxfp4_to_fp8_transpose(const uint8_t *q, const uint8_t *sf,
+                                      int64_t rows, int64_t cols, uint8_t *q8t,
+                                      float *s8t, void *stream);
+
 /* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
  * payload, RNE or SR, zero-scale rule, 2D weight tiles):
  *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);

@@ -108,3 +108,13 @@ def test_mxfp4_to_fp8_argument_errors_before_any_launch(L):
     assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 128, 4104, 4096, None) == 2  # q8 alignment
     assert L.fp4_mxfp4_to_fp8(4096, 4098, 4, 128, 4096, 4096, None) == 2  # sf alignment
     assert L.fp4_mxfp4_to_fp8(None, None, 0, 128, None, None, None) == 0  # empty: nothing to do
+
+
+def test_mxfp4_to_fp8_transpose_argument_errors_before_any_launch(L):
+    f = L.fp4_mxfp4_to_fp8_transpose
+    assert f(4096, 4096, 96, 128, 4096, 4096, None) == 3    # rows % 128
+    assert f(4096, 4096, 128, 48, 4096, 4096, None) == 3    # cols % 32
+    assert f(4096, 4096, -128, 128, 4096, 4096, None) == 1
+    assert f(4096, None, 128, 128, 4096, 4096, None) == 1
+    assert f(4104, 4096, 128, 128, 4096, 4096, None) == 2   # q alignment
+    assert f(None, None, 0, 64, None, None, None) == 0      # empty

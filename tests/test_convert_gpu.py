@@ -73,3 +73,38 @@ def test_reencode_empty_and_argument_errors():
     assert fq.fp4_mxfp4_to_fp8(q, sf, 4, 128, q8, s8) == fq.FP4_OK
     torch.cuda.synchronize()
     assert (q8.cpu() == 0).all() and (s8.cpu() == 2.0 ** -133).all()
+
+
+@pytest.mark.parametrize("rows,cols,spread", [(128, 32, 5), (256, 96, 20), (384, 1024, 40),
+                                              (1024, 4096, 14)])
+def test_transposed_reencode_matches_oracle(rows, cols, spread):
+    """x^T's FP8 copy (blocks of 128 rows per column, partial 128-column
+    tiles included) against the oracle, bit for bit."""
+    need_gpu()
+    g = torch.Generator().manual_seed(rows * 3 + cols)
+    q = torch.randint(0, 256, (rows, cols // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    base = torch.randint(spread, 255, (rows // 128, 1, cols // 32), generator=g)
+    off = torch.randint(0, spread + 1, (rows // 128, 128, cols // 32), generator=g)
+    sf = (base - off).reshape(rows, cols // 32).to(torch.uint8)
+    q8t, s8t = fq.mxfp4_to_fp8_transpose(q.cuda(), sf.cuda())
+    want_q8, want_s8 = orc.mxfp4_to_fp8_t(q.numpy(), sf.numpy())
+    mismatch_report(q8t.cpu().numpy(), want_q8, "q8t")
+    assert np.array_equal(s8t.cpu().numpy().view(np.uint32), want_s8.view(np.uint32)), "s8t"
+
+
+def test_transposed_reencode_full_size_sampled_columns():
+    """X's shape (8192 x 14336); the oracle checks 16 sampled columns of x
+    (16 rows of the output) on the full row range."""
+    need_gpu()
+    q, sf = inputs.mxfp4_copy(8192, 14336, seed=8, spread=16)
+    q8t, s8t = fq.mxfp4_to_fp8_transpose(q.cuda(), sf.cuda())
+    cols = np.sort(np.random.default_rng(1).choice(14336, 16, replace=False))
+    qn, sfn = q.numpy(), sf.numpy()
+    got_q8, got_s8 = q8t.cpu().numpy(), s8t.cpu().numpy()
+    for c in cols:
+        # the 32-column group of c, re-encoded alone: x[:, group] -> FP8 of its transpose
+        g0 = (c // 32) * 32
+        want_q8, want_s8 = orc.mxfp4_to_fp8_t(np.ascontiguousarray(qn[:, g0 // 2:g0 // 2 + 16]),
+                                              np.ascontiguousarray(sfn[:, c // 32:c // 32 + 1]))
+        mismatch_report(got_q8[c], want_q8[c - g0], f"q8t[{c}]")
+        assert np.array_equal(got_s8[c].view(np.uint32), want_s8[c - g0].view(np.uint32))
