@@ -243,6 +243,8 @@ def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
 
 def amax_many(xs, stream=None):
     """[amax] device float32 tensors of shape [1], one per tensor, one launch."""
+    if any(not x.is_contiguous() for x in xs):
+        raise ValueError("amax_many: tensors must be contiguous")
     outs = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
     _check(fp4_amax_many(xs, outs, stream), "fp4_amax_many")
     return outs
@@ -252,6 +254,8 @@ def mxfp4_to_fp8(q, sf, stream=None):
     """FP8 E4M3-b128 copy (q8 uint8 [R][C], s8 float32 [R][C/128]) of an
     MXFP4-b32 row-wise copy given by its payload q [R][C/2] and plain-layout
     E8M0 scales sf [R][C/32]."""
+    if not (q.is_contiguous() and sf.is_contiguous()):
+        raise ValueError("mxfp4_to_fp8: q and sf must be contiguous")
     rows, cols = q.shape[0], q.shape[1] * 2
     q8 = torch.empty((rows, cols), dtype=torch.uint8, device=q.device)
     s8 = torch.empty((rows, cols // 128), dtype=torch.float32, device=q.device)
@@ -263,6 +267,8 @@ def mxfp4_to_fp8_transpose(q, sf, stream=None):
     """FP8 E4M3-b128 copy of x^T (q8t uint8 [C][R], s8t float32 [C][R/128])
     from x's MXFP4-b32 row-wise copy (payload q [R][C/2], plain E8M0 scales
     sf [R][C/32])."""
+    if not (q.is_contiguous() and sf.is_contiguous()):
+        raise ValueError("mxfp4_to_fp8_transpose: q and sf must be contiguous")
     rows, cols = q.shape[0], q.shape[1] * 2
     q8t = torch.empty((cols, rows), dtype=torch.uint8, device=q.device)
     s8t = torch.empty((cols, rows // 128), dtype=torch.float32, device=q.device)
