@@ -258,6 +258,20 @@ def test_amax_many_matches_oracle_and_restarts_each_call():
         assert a.item() == b.item() == o.item()
 
 
+def test_amax_many_at_the_job_limit():
+    """FP4_AMAX_MAX_JOBS tensors of very different sizes in one launch."""
+    need_gpu()
+    g = torch.Generator().manual_seed(21)
+    shapes = [(1, 8), (7, 16), (64, 64), (1000, 24), (2048, 512), (3, 4096), (0, 8), (129, 136)]
+    assert len(shapes) == fq.FP4_AMAX_MAX_JOBS
+    xs = [(torch.randn(sh, generator=g) * (10.0 ** (k - 3))).to(torch.bfloat16).cuda()
+          for k, sh in enumerate(shapes)]
+    outs = fq.amax_many(xs)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    for x, o in zip(xs, outs):
+        assert o.item() == float(orc.amax(f32(x.cpu()))), x.shape
+
+
 def test_amax_many_reports_nonfinite():
     need_gpu()
     a = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
