@@ -140,17 +140,23 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
     // NSC / 4 tiles of 128 x 4 codes; 32-bit word i of a tile holds the 4
     // codes of row (i / 4) + 32 (i % 4).
     const int64_t cp4 = (copy_cb + 3) / 4;  // tiles per tile-row
+    // interior tile: a word is four consecutive codes of one staged row
+    const bool whole = !DUP && rows_valid >= 128 && cols_valid >= NSC;
     for (int idx = t; idx < 128 * (NSC / 4); idx += kThreads) {
       int atom = idx / 128, i = idx % 128;
       int64_t atom_col = c0b / 4 + atom;
       if (atom_col >= cp4) continue;
       int r = (i >> 2) + 32 * (i & 3);
       uint32_t w = 0;
+      if (whole) {
+        w = *reinterpret_cast<const uint32_t *>(&sfs[r][atom * 4]);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        int j = atom * 4 + c;
-        uint32_t code = (r < rows_valid && j < cols_valid) ? sfs[r][DUP ? j / 2 : j] : 0u;
-        w |= code << (8 * c);
+        for (int c = 0; c < 4; ++c) {
+          int j = atom * 4 + c;
+          uint32_t code = (r < rows_valid && j < cols_valid) ? sfs[r][DUP ? j / 2 : j] : 0u;
+          w |= code << (8 * c);
+        }
       }
       int64_t base = ((r0 / 128) * cp4 + atom_col) * 512;
       reinterpret_cast<uint32_t *>(sf + base)[i] = w;
@@ -528,14 +534,26 @@ __global__ void __launch_bounds__(kThreads, 4)
   if (threadIdx.x == 0 && tile + gridDim.x < ntiles) load_tile(tile + gridDim.x, buf);
 
   // ---- transposed payload: each column's 64 bytes (8 planes x 8 bytes)
-  // leave as 8 consecutive 8-byte stores
+  // leave as 16-byte stores of two adjacent planes when a row of the copy
+  // (R / 2 bytes) keeps them 16-byte aligned (R % 32 == 0), else as 8-byte
+  // stores; 8 bytes also at a ragged row end
   if (p.do_col) {
-    for (int idx = threadIdx.x; idx < kTile * 8; idx += kThreads) {
-      int col = idx >> 3, part = idx & 7;
-      int64_t gcol = C0 + col, grow = R0 + 16 * part;
+    const bool wide = (R % 32) == 0;
+    for (int idx = threadIdx.x; idx < kTile * 4; idx += kThreads) {
+      const int col = idx >> 2, part = 2 * (idx & 3);
+      const int64_t gcol = C0 + col, grow = R0 + 16 * part;
       if (gcol < C && grow < R) {
-        *reinterpret_cast<uint2 *>(p.q_col + gcol * (R / 2) + grow / 2) =
-            *reinterpret_cast<const uint2 *>(&colq[part][8 * col]);
+        const uint2 a = *reinterpret_cast<const uint2 *>(&colq[part][8 * col]);
+        uint8_t *dst = p.q_col + gcol * (R / 2) + grow / 2;
+        const bool second = grow + 16 < R;
+        if (wide && second) {
+          const uint2 b = *reinterpret_cast<const uint2 *>(&colq[part + 1][8 * col]);
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(a.x, a.y, b.x, b.y);
+        } else {
+          *reinterpret_cast<uint2 *>(dst) = a;
+          if (second)
+            *reinterpret_cast<uint2 *>(dst + 8) = *reinterpret_cast<const uint2 *>(&colq[part + 1][8 * col]);
+        }
       }
     }
   }
