@@ -23,8 +23,9 @@
 //  * the row-wise copy then encodes one block per thread from shared memory
 //    (so the 2D path can use the tile maxima of the transposed pass).
 //  * transposed payload bytes are staged in shared memory so every column
-//    segment leaves as contiguous 8-byte stores; scales leave as whole
-//    512-byte tensor-core tiles (or plain rows).
+//    segment leaves as contiguous 16-byte stores (8-byte ones when R % 32
+//    != 0); scales leave as whole 512-byte tensor-core tiles, a 32-bit word
+//    of four staged codes per store (or plain rows).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
