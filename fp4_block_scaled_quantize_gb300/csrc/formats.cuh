@@ -37,16 +37,6 @@ __device__ __forceinline__ uint32_t e2m1_rne(float v) {
   return c | ((__float_as_uint(v) >> 28) & 8u);
 }
 
-// Hardware conversion of two values (hi -> upper nibble).  Used only where
-// the self-check kernel has shown it equal to e2m1_rne on every input class.
-__device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
-  uint16_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
-      : "=h"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Eight values -> eight nibbles (value j in bits 4j..4j+3) with the same
 // hardware conversion, four conversions packed by one register move.
 __device__ __forceinline__ uint32_t e2m1x8_hw(const float *v) {
