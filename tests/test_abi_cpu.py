@@ -118,3 +118,33 @@ def test_mxfp4_to_fp8_transpose_argument_errors_before_any_launch(L):
     assert f(4096, None, 128, 128, 4096, 4096, None) == 1
     assert f(4104, 4096, 128, 128, 4096, 4096, None) == 2   # q alignment
     assert f(None, None, 0, 64, None, None, None) == 0      # empty
+
+
+def test_amax_argument_errors_before_any_launch(L):
+    f = L.fp4_amax
+    assert f(4096, 4, 16, 0, 0, None, None, None) == 1          # no output
+    assert f(4096, -4, 16, 0, 0, 256, None, None) == 1          # negative rows
+    assert f(None, 4, 16, 0, 0, 256, None, None) == 1           # data missing
+    assert f(4096, 4, 16, 8, 0, 256, 260, None) == 1            # Hadamard size not 16 / 32
+    assert f(4096, 4, 12, 0, 0, 256, None, None) == 3           # cols % 8
+    assert f(4096, 24, 16, 16, 0, 256, 260, None) == 3          # rows % hadamard_n
+    assert f(4104, 4, 16, 0, 0, 256, None, None) == 2           # x alignment
+    assert f(4096, 4, 16, 0, 0, 258, None, None) == 2           # amax alignment
+
+
+def test_quantize_transpose_argument_errors_before_any_launch(L):
+    f = L.fp4_quantize_transpose
+    ok = fq.params(format=fq.FP4_FMT_NVFP4_B16)
+    args = lambda p, rows=32, cols=32, x=4096, ar=256, ac=None, sr=None, sc=None, qr=8192, qc=12288: (
+        x, rows, cols, ar, ac, ctypes.byref(p), qr, 16384, 512, sr, qc, 20480, 516, sc, None)
+    assert f(*args(fq.params(format=7))) == 1                   # bad format
+    assert f(*args(fq.params(format=0, T=0.5))) == 1            # T below 1
+    assert f(*args(fq.params(format=0, hadamard_n=8))) == 1     # Hadamard size
+    assert f(*args(fq.params(format=0, block2d=True, round_row=1))) == 4  # 2D with SR
+    assert f(*args(ok, rows=-16)) == 1
+    assert f(*args(fq.params(format=0, hadamard_n=16))) == 1    # rotation needs amax_col
+    assert f(*args(ok, x=None)) == 1
+    assert f(*args(ok, rows=24)) == 3                           # rows % 16
+    assert f(*args(fq.params(format=2), cols=48)) == 3          # MXFP4: cols % 32
+    assert f(*args(ok, sr=1024)) == 4                           # shifts only for UE5M3 + MMA
+    assert f(*args(ok, qr=8200)) == 2                           # q_row alignment
