@@ -249,7 +249,14 @@ __global__ void __launch_bounds__(kThreads, 4)
   phase[buf] ^= 1u;
   __syncthreads();
   if (tfail) {
-    if (threadIdx.x == 0) raise_status(p.status, kStatusTimeout);
+    // The tile's copy did not land in time: report it, give the copy still
+    // in flight one more bounded wait so it does not land in shared memory
+    // after this CTA has gone, then leave.
+    if (threadIdx.x == 0) {
+      raise_status(p.status, kStatusTimeout);
+      mbar_wait_q(bar_a[buf], phase[buf] ^ 1u);
+    }
+    __syncthreads();
     return;
   }
   uint16_t(*xs)[kTile] = reinterpret_cast<uint16_t(*)[kTile]>(qsm + buf * kTileBytes);
