@@ -71,6 +71,8 @@ def lib():
             "orc_canon1024": (f32, [f32]),
             "orc_mxfp4_to_fp8": (None, [u8p, u8p, i64, i64, u8p, f32p]),
             "orc_mxfp4_to_fp8_t": (None, [u8p, u8p, i64, i64, u8p, f32p]),
+            "orc_fp8_gemm_exact": (None, [u8p, f32p, u8p, f32p, i64, i64p, i64p, i64, f64p,
+                                          f64p]),
             "orc_round_sum_f32": (f32, [f64p, i32, i32]),
         }
         for name, (res, args) in sig.items():
@@ -317,6 +319,27 @@ def mxfp4_to_fp8_t(q, sf):
     lib().orc_mxfp4_to_fp8_t(_p(q, ctypes.c_uint8), _p(sf, ctypes.c_uint8), R, C,
                              _p(q8t, ctypes.c_uint8), _p(s8t, ctypes.c_float))
     return q8t, s8t
+
+
+def fp8_gemm_exact(q8a, s8a, q8b, s8b, mi, ni):
+    """Exact D[m, n] = sum_k (e4m3(a) s8a)(e4m3(b) s8b) for K-major FP8
+    operands with binary32 scales per 128 elements, at the requested (m, n);
+    returns (y_exact, s_abs) in binary64."""
+    q8a = np.ascontiguousarray(q8a, dtype=np.uint8)
+    q8b = np.ascontiguousarray(q8b, dtype=np.uint8)
+    s8a = np.ascontiguousarray(s8a, dtype=np.float32)
+    s8b = np.ascontiguousarray(s8b, dtype=np.float32)
+    K = q8a.shape[1]
+    assert K % 128 == 0 and q8b.shape[1] == K
+    mi = np.ascontiguousarray(mi, dtype=np.int64)
+    ni = np.ascontiguousarray(ni, dtype=np.int64)
+    y = np.zeros(len(mi), np.float64)
+    s = np.zeros(len(mi), np.float64)
+    lib().orc_fp8_gemm_exact(_p(q8a, ctypes.c_uint8), _p(s8a, ctypes.c_float),
+                             _p(q8b, ctypes.c_uint8), _p(s8b, ctypes.c_float), K,
+                             _p(mi, ctypes.c_int64), _p(ni, ctypes.c_int64), len(mi),
+                             _p(y, ctypes.c_double), _p(s, ctypes.c_double))
+    return y, s
 
 
 # ------------------------------------------------------------------ GEMM

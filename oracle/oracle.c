@@ -738,3 +738,28 @@ void orc_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t 
     }
   }
 }
+
+/* FP8 exact reference: products of decoded E4M3 codes (at most 4 significant
+ * bits each) and power-of-two binary32 scales are exact in binary64; their
+ * sum is accumulated exactly and rounded once. */
+void orc_fp8_gemm_exact(const uint8_t *q8a, const float *s8a, const uint8_t *q8b,
+                        const float *s8b, int64_t K, const int64_t *mi,
+                        const int64_t *ni, int64_t count, double *y_exact,
+                        double *s_abs) {
+  const int64_t Kb = K / 128;
+  acc_t tot, absacc;
+  for (int64_t t = 0; t < count; ++t) {
+    const int64_t m = mi[t], n = ni[t];
+    acc_clear(&tot);
+    acc_clear(&absacc);
+    for (int64_t k = 0; k < K; ++k) {
+      double a = orc_e4m3_value(q8a[m * K + k]) * (double)s8a[m * Kb + k / 128];
+      double b = orc_e4m3_value(q8b[n * K + k]) * (double)s8b[n * Kb + k / 128];
+      double p = a * b;
+      acc_add_double(&tot, p);
+      acc_add_double(&absacc, fabs(p));
+    }
+    y_exact[t] = acc_to_f64(&tot);
+    s_abs[t] = acc_to_f64(&absacc);
+  }
+}

@@ -86,6 +86,16 @@ void orc_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
 void orc_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t R, int64_t C,
                         uint8_t *q8t, float *s8t);
 
+/* Exact reference of D = A * B^T for FP8 E4M3 operands with one binary32
+ * scale per 128 elements (the re-encoded copies above, K-major): for each
+ * requested (m, n), the exact sum over k of (e4m3(a) * s8a) (e4m3(b) * s8b)
+ * rounded once to binary64, and the exact sum of the magnitudes.  The FP8
+ * side of the FP4-vs-FP8 comparison ([HOP] Method); K % 128 == 0. */
+void orc_fp8_gemm_exact(const uint8_t *q8a, const float *s8a, const uint8_t *q8b,
+                        const float *s8b, int64_t K, const int64_t *mi,
+                        const int64_t *ni, int64_t count, double *y_exact,
+                        double *s_abs);
+
 /* ---- GEMM models ----------------------------------------------------------- */
 void orc_gemm_model(const uint8_t *qa, const uint8_t *sfa,
                     const uint8_t *qb, const uint8_t *sfb, int fmt, int64_t M,

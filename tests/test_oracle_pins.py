@@ -681,3 +681,40 @@ def test_fp8_reencode_transposed_equals_rowwise_of_the_transpose():
     sft = np.repeat(np.repeat(e_col, 32)[:, None], R // 32, axis=1).astype(np.uint8)
     want_q8, want_s8 = orc.mxfp4_to_fp8(qt, sft)
     assert np.array_equal(q8t, want_q8) and np.array_equal(s8t, want_s8)
+
+
+def test_fp8_gemm_exact_hand_worked():
+    # A row (scale 2^-3): 384 (0x7C) at k = 0, 12 (0x54) at k = 1;
+    # B row (scale 2^-2): 8 (0x50) at k = 0, -12 (0xD4) at k = 1
+    q8a = np.zeros((1, 128), np.uint8)
+    q8b = np.zeros((1, 128), np.uint8)
+    q8a[0, 0], q8a[0, 1] = 0x7C, 0x54
+    q8b[0, 0], q8b[0, 1] = 0x50, 0xD4     # 8 and -12
+    s8a = np.array([[0.125]], np.float32)
+    s8b = np.array([[0.25]], np.float32)
+    y, s = orc.fp8_gemm_exact(q8a, s8a, q8b, s8b, [0], [0])
+    # (384/8)(8/4) + (12/8)(-12/4) = 96 - 4.5
+    assert y[0] == 91.5 and s[0] == 100.5
+
+
+@pytest.mark.parametrize("seed", [0, 3])
+def test_fp8_gemm_of_exact_reencodings_equals_the_mxfp4_product(seed):
+    """Where the FP4 -> FP8 re-encoding is exact (blocks within 14 binades of
+    their FP8 block's largest), the FP8 operands hold the same values, so the
+    exact products agree bit for bit with the MXFP4 exact product."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 6, 5, 512
+    def operand(rows):
+        q = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+        base = rng.integers(110, 140, size=(rows, K // 128, 1))
+        sf = (base - rng.integers(0, 15, size=(rows, K // 128, 4))).reshape(rows, K // 32)
+        return q, sf.astype(np.uint8)
+    qa, sfa = operand(M)
+    qb, sfb = operand(N)
+    mi, ni = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    mi, ni = mi.ravel(), ni.ravel()
+    _, y4, s4 = orc.gemm_model(qa, sfa, qb, sfb, orc.MXFP4, K, 1.0, 1.0, mi, ni)
+    q8a, s8a = orc.mxfp4_to_fp8(qa, sfa)
+    q8b, s8b = orc.mxfp4_to_fp8(qb, sfb)
+    y8, s8 = orc.fp8_gemm_exact(q8a, s8a, q8b, s8b, mi, ni)
+    assert np.array_equal(y4, y8) and np.array_equal(s4, s8)
