@@ -23,9 +23,11 @@ FP4_FMT_UE5M3_B16, FP4_FMT_NVFP4_B16, FP4_FMT_MXFP4_B32, FP4_FMT_UE5M3_B32 = 0, 
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
 FP4_SF_PLAIN, FP4_SF_MMA = 0, 1
 FP4_OK = 0
-STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_ALIGNMENT", 3: "FP4_ERR_SHAPE",
-                4: "FP4_ERR_UNSUPPORTED", 5: "FP4_ERR_CUDA", 6: "FP4_ERR_TIMEOUT",
-                7: "FP4_ERR_NONFINITE", 8: "FP4_ERR_SCALE_WINDOW"}
+(FP4_ERR_INVALID_ARG, FP4_ERR_ALIGNMENT, FP4_ERR_UNSUPPORTED, FP4_ERR_CUDA, FP4_ERR_TIMEOUT,
+ FP4_ERR_NONFINITE, FP4_ERR_SCALE_WINDOW, FP4_ERR_SHAPE) = range(1, 9)
+STATUS_NAMES = {0: "FP4_OK", 1: "FP4_ERR_INVALID_ARG", 2: "FP4_ERR_ALIGNMENT",
+                3: "FP4_ERR_UNSUPPORTED", 4: "FP4_ERR_CUDA", 5: "FP4_ERR_TIMEOUT",
+                6: "FP4_ERR_NONFINITE", 7: "FP4_ERR_SCALE_WINDOW", 8: "FP4_ERR_SHAPE"}
 
 
 class fp4_quant_params(ctypes.Structure):
@@ -33,7 +35,7 @@ class fp4_quant_params(ctypes.Structure):
                 ("round_row", ctypes.c_int32), ("round_col", ctypes.c_int32),
                 ("sr_seed", ctypes.c_uint64), ("sr_offset", ctypes.c_uint32),
                 ("hadamard_n", ctypes.c_int32), ("hadamard_signs", ctypes.c_uint32),
-                ("sf_layout", ctypes.c_int32)]
+                ("sf_layout", ctypes.c_int32), ("T_col", ctypes.c_float)]
 
 
 class fp4_operand(ctypes.Structure):
@@ -114,10 +116,12 @@ def _check(code, where):
 
 def params(format=FP4_FMT_UE5M3_B16, T=448.0, block2d=False, round_row=FP4_ROUND_RNE,
            round_col=FP4_ROUND_RNE, sr_seed=0, sr_offset=0, hadamard_n=0, hadamard_signs=0,
-           sf_layout=FP4_SF_PLAIN):
+           sf_layout=FP4_SF_PLAIN, T_col=0.0):
+    """Producer options (fp4_quant_params); T_col = 0 gives the transposed
+    copy the same target T as the row-wise copy."""
     return fp4_quant_params(int(format), float(T), int(bool(block2d)), int(round_row),
                             int(round_col), int(sr_seed), int(sr_offset), int(hadamard_n),
-                            int(hadamard_signs), int(sf_layout))
+                            int(hadamard_signs), int(sf_layout), float(T_col))
 
 
 # ------------------------------------------------------------- raw entry points
@@ -296,10 +300,43 @@ def quantize_transpose(x, amax_row, amax_col, p, remap=True, stream=None):
     return r, c
 
 
+def _check_operands(a, b, where):
+    """The GEMM reads scales in the tensor-core tile layout only (a plain
+    [rows][k/B] buffer would be misread, and for rows % 128 != 0 read past its
+    end), and UE5M3 operands need the remap's row shifts."""
+    for name, t in (("A", a), ("B", b)):
+        if t.sf_layout != FP4_SF_MMA:
+            raise ValueError(f"{where}: operand {name} has plain-layout scales; the GEMM needs "
+                             "sf_layout=FP4_SF_MMA")
+        if t.format in (FP4_FMT_UE5M3_B16, FP4_FMT_UE5M3_B32) and t.row_shift is None:
+            raise ValueError(f"{where}: UE5M3 operand {name} has no row shifts (quantise it with "
+                             "remap=True)")
+        if not t.q.is_contiguous() or not t.sf.is_contiguous():
+            raise ValueError(f"{where}: operand {name} is not contiguous")
+    if a.format != b.format:
+        raise ValueError(f"{where}: operands have different formats")
+    if a.k != b.k:
+        raise ValueError(f"{where}: contraction lengths differ ({a.k} vs {b.k})")
+    if a.q.device != b.q.device:
+        raise ValueError(f"{where}: operands are on different devices")
+
+
 def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, stream=None):
-    """D = alpha * A B^T for two Quantized operands in the tensor-core layout."""
+    """D = alpha * A B^T for two Quantized operands in the tensor-core layout.
+    D is float32 or bfloat16 [M, N]; `out`, if given, must be a contiguous
+    tensor of that dtype and shape on the operands' device."""
+    _check_operands(a, b, "gemm")
     M, N, K = a.rows, b.rows, a.k
-    D = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.q.device)
+    if out is not None:
+        if out.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("gemm: out must be float32 or bfloat16")
+        if tuple(out.shape) != (M, N) or not out.is_contiguous() or out.device != a.q.device:
+            raise ValueError(f"gemm: out must be a contiguous [{M}, {N}] tensor on {a.q.device}")
+        D = out
+    else:
+        if out_dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("gemm: out_dtype must be float32 or bfloat16")
+        D = torch.empty((M, N), dtype=out_dtype, device=a.q.device)
     _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
                     canonicalize_1024, stream), "fp4_gemm")
     return D
@@ -308,6 +345,7 @@ def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, strea
 def gemm_quantize(a, b, amax_dev, p, remap=True, canonicalize_1024=False, stream=None):
     """Row-wise FP4 copy of y = alpha * A B^T, quantised in the GEMM epilogue
     (the product is never stored).  Returns a Quantized of y [M, N]."""
+    _check_operands(a, b, "gemm_quantize")
     M, N, K = a.rows, b.rows, a.k
     out = _alloc_copy(M, N, p, a.q.device, _want_shift(p, remap))
     _check(fp4_gemm_quantize(a.operand(), b.operand(), M, N, K, amax_dev, p, out.q, out.sf,

@@ -49,9 +49,13 @@ fp4_status check_params(const fp4_quant_params *p) {
     return FP4_ERR_INVALID_ARG;
   if (p->format != FP4_FMT_MXFP4_B32 && !(std::isfinite(p->T) && p->T >= 1.0f && p->T <= 61440.0f))
     return FP4_ERR_INVALID_ARG;
+  if (p->format != FP4_FMT_MXFP4_B32 && p->T_col != 0.0f &&
+      !(std::isfinite(p->T_col) && p->T_col >= 1.0f && p->T_col <= 61440.0f))
+    return FP4_ERR_INVALID_ARG;
   if (p->hadamard_n != 0 && p->hadamard_n != 16 && p->hadamard_n != 32) return FP4_ERR_INVALID_ARG;
   if (p->block2d && (p->round_row != FP4_ROUND_RNE || p->round_col != FP4_ROUND_RNE || p->hadamard_n))
     return FP4_ERR_UNSUPPORTED;
+  if (p->block2d && p->T_col != 0.0f && p->T_col != p->T) return FP4_ERR_UNSUPPORTED;
   return FP4_OK;
 }
 
@@ -140,6 +144,7 @@ fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const fl
   j.C = cols;
   j.amax_row = amax_dev;
   j.T = p->T;
+  j.T_col = p->T;
   j.fmt = p->format;
   j.block2d = p->block2d;
   j.had_n = 0;
@@ -184,6 +189,7 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   j.amax_row = amax_row_dev;
   j.amax_col = p->block2d ? amax_row_dev : (amax_col_dev ? amax_col_dev : amax_row_dev);
   j.T = p->T;
+  j.T_col = p->T_col != 0.0f ? p->T_col : p->T;
   j.fmt = p->format;
   j.block2d = p->block2d;
   j.had_n = p->hadamard_n;

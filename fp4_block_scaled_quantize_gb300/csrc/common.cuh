@@ -84,7 +84,7 @@ struct QuantJob {
   const uint16_t *x;
   int64_t R, C;
   const float *amax_row, *amax_col;
-  float T;
+  float T, T_col;  // scale targets of the row-wise and the transposed copy
   int fmt, block2d, had_n;
   uint32_t signs;
   int sr_row, sr_col;

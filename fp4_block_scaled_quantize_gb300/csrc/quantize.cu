@@ -53,7 +53,7 @@ struct Params {
   int64_t R, C;
   int64_t tiles_r, tiles_c;
   const float *amax_row, *amax_col;
-  float T;
+  float T, T_col;
   uint8_t *q_row, *sf_row;
   float *s_dec_row;
   uint8_t *q_col, *sf_col;
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 
   float se_r, sd_r, se_c = 1.0f, sd_c = 1.0f;
   tensor_scale<FMT>(__ldg(p.amax_row), p.T, se_r, sd_r);
-  if (p.do_col && !TWO_D) tensor_scale<FMT>(__ldg(p.amax_col), p.T, se_c, sd_c);
+  if (p.do_col && !TWO_D) tensor_scale<FMT>(__ldg(p.amax_col), p.T_col, se_c, sd_c);
   if (TWO_D) {
     se_c = se_r;
     sd_c = sd_r;
@@ -578,15 +578,15 @@ __global__ void __launch_bounds__(kThreads, 4)
 
 // s_dec only (empty tensors).
 template <int FMT>
-__global__ void k_scale_only(const float *amax_row, const float *amax_col, float T, float *sd_row,
-                             float *sd_col) {
+__global__ void k_scale_only(const float *amax_row, const float *amax_col, float T, float T_col,
+                             float *sd_row, float *sd_col) {
   float se, sd;
   if (sd_row) {
     tensor_scale<FMT>(*amax_row, T, se, sd);
     *sd_row = sd;
   }
   if (sd_col) {
-    tensor_scale<FMT>(amax_col ? *amax_col : *amax_row, T, se, sd);
+    tensor_scale<FMT>(amax_col ? *amax_col : *amax_row, T_col, se, sd);
     *sd_col = sd;
   }
 }
@@ -665,6 +665,7 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   p.amax_row = j.amax_row;
   p.amax_col = j.amax_col ? j.amax_col : j.amax_row;
   p.T = j.T;
+  p.T_col = j.T_col;
   p.q_row = j.q_row;
   p.sf_row = j.sf_row;
   p.s_dec_row = j.s_dec_row;
@@ -686,9 +687,9 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
     float *sdc = j.s_dec_col;
     switch (j.fmt) {
       case kUE5M3:
-      case kUE5M3B32: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
-      case kNVFP4: k_scale_only<kNVFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
-      default: k_scale_only<kMXFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, sdr, sdc); break;
+      case kUE5M3B32: k_scale_only<kUE5M3><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, p.T_col, sdr, sdc); break;
+      case kNVFP4: k_scale_only<kNVFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, p.T_col, sdr, sdc); break;
+      default: k_scale_only<kMXFP4><<<1, 1, 0, s>>>(p.amax_row, p.amax_col, p.T, p.T_col, sdr, sdc); break;
     }
     return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
   }

@@ -6,8 +6,8 @@ Developer view:
     refreshed by sample-and-hold every D steps (D = 50 in the recipe, D = 1 is
     "current" scaling) and deliberately not serialised in checkpoints;
   * block scale target T (448 by default) with a per-module override for the
-    upstream gradient (T = 2048 on the Wgrad-dY of the four final
-    mixer.down_proj modules);
+    upstream gradient's Wgrad copy (T = 2048 on the Wgrad-dY of the four
+    final mixer.down_proj modules); the Dgrad copy of dY keeps T;
   * nearest-even everywhere except stochastic rounding on dY (both backward
     GEMMs), 2D 16x16 weight tiles so the forward and backward views agree;
   * fprop Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X on the FP4 tensor
@@ -15,11 +15,25 @@ Developer view:
 
 Every computation runs in libfp4gb300.so; this module only allocates
 buffers, keeps the step counter and passes pointers.
+
+Device-side conditions (a bounded wait that ran out, a non-finite amax, a
+UE5M3 row outside the tensor core's scale window) are recorded in the
+library's per-device status word, which stays set until it is read.
+``FP4Linear.next_step()`` reads it once per step (outside the hot loop) and
+raises ``FP4Error`` if anything was recorded; pass ``check_status=False`` to
+leave that to the caller.
 """
+import itertools
+
 import torch
 
-from . import (FP4_FMT_UE5M3_B16, FP4_ROUND_SR, FP4_SF_MMA, _check, fp4_amax, gemm, params,
-               quantize_transpose)
+from . import (FP4_FMT_UE5M3_B16, FP4_OK, FP4_ROUND_SR, FP4_SF_MMA, FP4Error, _check, fp4_amax,
+               fp4_status_sync, gemm, params, quantize_transpose)
+
+# Distinct stochastic-rounding streams per module: the default Philox key of
+# the k-th FP4Linear built in this process is (42 << 32) | k, so two layers
+# never draw the same random bits at the same element positions.
+_module_index = itertools.count()
 
 
 class AmaxCache:
@@ -81,13 +95,19 @@ class FP4Linear(torch.nn.Module):
     in_features, out_features and the number of tokens per call must be
     multiples of 64 (the K dimension of every one of the three GEMMs).
     ``format`` is one of the library's FP4 formats (UE5M3 block 16 by
-    default); ``T_dy`` is the per-module target for the upstream gradient.
+    default); ``T_dy`` is the per-module target for the upstream gradient's
+    transposed (Wgrad) copy; ``sr_seed`` (default: distinct per module) keys
+    the stochastic rounding of dY.
     Call ``next_step()`` once per optimizer step to advance the
     sample-and-hold clock."""
 
     def __init__(self, in_features, out_features, D=50, T=448.0, T_dy=None,
-                 format=FP4_FMT_UE5M3_B16, sr_seed=42, device="cuda", dtype=torch.bfloat16):
+                 format=FP4_FMT_UE5M3_B16, sr_seed=None, device="cuda", dtype=torch.bfloat16,
+                 check_status=True):
         super().__init__()
+        if sr_seed is None:
+            sr_seed = (42 << 32) | next(_module_index)
+        self.check_status = bool(check_status)
         self.in_features, self.out_features = in_features, out_features
         self.weight = torch.nn.Parameter(
             torch.empty(out_features, in_features, device=device, dtype=dtype))
@@ -98,11 +118,20 @@ class FP4Linear(torch.nn.Module):
         self.cache_dy = AmaxCache(D, device)
         self.p_x = params(format=format, T=T, sf_layout=FP4_SF_MMA)
         self.p_w = params(format=format, T=T, block2d=True, sf_layout=FP4_SF_MMA)
-        self.p_dy = params(format=format, T=T_dy if T_dy is not None else T,
+        # the override applies to the transposed (Wgrad) copy of dY only
+        self.p_dy = params(format=format, T=T, T_col=T_dy if T_dy is not None else 0.0,
                            round_row=FP4_ROUND_SR, round_col=FP4_ROUND_SR, sr_seed=sr_seed,
                            sf_layout=FP4_SF_MMA)
 
     def next_step(self):
+        """Advance the sample-and-hold clock; with check_status, first read
+        (and clear) the device status word and raise FP4Error if a kernel
+        recorded a condition since the last read.  Reading it waits for the
+        current stream."""
+        if self.check_status:
+            st = fp4_status_sync()
+            if st != FP4_OK:
+                raise FP4Error(st, f"FP4Linear step {self.step}")
         self.step += 1
 
     def forward(self, x):

@@ -49,12 +49,12 @@ typedef enum {
   FP4_OK = 0,
   FP4_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum      */
   FP4_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned                */
-  FP4_ERR_SHAPE = 3,        /* size not a multiple the layout needs       */
-  FP4_ERR_UNSUPPORTED = 4,  /* valid but unsupported option combination   */
-  FP4_ERR_CUDA = 5,         /* a CUDA runtime call failed                 */
-  FP4_ERR_TIMEOUT = 6,      /* a bounded device wait ran out              */
-  FP4_ERR_NONFINITE = 7,    /* amax saw Inf or NaN                        */
-  FP4_ERR_SCALE_WINDOW = 8  /* a UE5M3 row spans more than E4M3 can hold  */
+  FP4_ERR_UNSUPPORTED = 3,  /* valid but unsupported option combination   */
+  FP4_ERR_CUDA = 4,         /* a CUDA runtime call failed                 */
+  FP4_ERR_TIMEOUT = 5,      /* a bounded device wait ran out              */
+  FP4_ERR_NONFINITE = 6,    /* amax saw Inf or NaN                        */
+  FP4_ERR_SCALE_WINDOW = 7, /* a UE5M3 row spans more than E4M3 can hold  */
+  FP4_ERR_SHAPE = 8         /* size not a multiple the layout needs       */
 } fp4_status;
 
 /* Payload is always E2M1.  Block scale and block size per format:
@@ -97,6 +97,11 @@ typedef struct {
   int32_t hadamard_n;      /* 0, 16 or 32: rotation of the transposed copy   */
   uint32_t hadamard_signs; /* bit j set: input lane j of each group negated  */
   int32_t sf_layout;       /* fp4_sf_layout of every scale output            */
+  float T_col;             /* scale target of the transposed copy; 0: T.
+                              [UE5M3] Approach applies the T = 2048 override
+                              to the Wgrad-dY (transposed) copy only.  With
+                              block2d both copies share the tile scales, so
+                              T_col must be 0 or T                           */
 } fp4_quant_params;
 
 /* One quantised GEMM operand: `rows` rows of `k` elements, K-major. */

@@ -8,6 +8,7 @@ import subprocess
 import tempfile
 
 import pytest
+import torch
 
 import fp4_block_scaled_quantize_gb300 as fq
 from fp4_block_scaled_quantize_gb300 import build as fbuild
@@ -42,9 +43,9 @@ def test_struct_layout_matches_header():
 #include <stddef.h>
 #include "fp4.h"
 int main(void){
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(fp4_quant_params), offsetof(fp4_quant_params, sr_seed),
-         offsetof(fp4_quant_params, sf_layout), sizeof(fp4_operand), offsetof(fp4_operand, format),
-         offsetof(fp4_operand, k));
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(fp4_quant_params), offsetof(fp4_quant_params, sr_seed),
+         offsetof(fp4_quant_params, sf_layout), offsetof(fp4_quant_params, T_col),
+         sizeof(fp4_operand), offsetof(fp4_operand, format), offsetof(fp4_operand, k));
   return 0; }
 """
     with tempfile.TemporaryDirectory() as d:
@@ -55,8 +56,21 @@ int main(void){
         got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True,
                                               check=True).stdout.split()]
     P, O = fq.fp4_quant_params, fq.fp4_operand
-    assert got == [ctypes.sizeof(P), P.sr_seed.offset, P.sf_layout.offset, ctypes.sizeof(O),
-                   O.format.offset, O.k.offset]
+    assert got == [ctypes.sizeof(P), P.sr_seed.offset, P.sf_layout.offset, P.T_col.offset,
+                   ctypes.sizeof(O), O.format.offset, O.k.offset]
+
+
+def test_status_codes_match_header_and_contract():
+    # the numbering of the boundary's contract: UNSUPPORTED 3 ... SCALE_WINDOW 7,
+    # SHAPE appended after it
+    src = open(HEADER).read()
+    vals = dict((k, int(v)) for k, v in re.findall(r"(FP4_(?:OK|ERR_\w+))\s*=\s*(\d+)", src))
+    want = dict(FP4_OK=0, FP4_ERR_INVALID_ARG=1, FP4_ERR_ALIGNMENT=2, FP4_ERR_UNSUPPORTED=3,
+                FP4_ERR_CUDA=4, FP4_ERR_TIMEOUT=5, FP4_ERR_NONFINITE=6, FP4_ERR_SCALE_WINDOW=7,
+                FP4_ERR_SHAPE=8)
+    assert vals == want
+    for k, v in want.items():
+        assert getattr(fq, k) == v and fq.STATUS_NAMES[v] == k
 
 
 def test_host_helpers(L):
@@ -91,7 +105,7 @@ def test_amax_many_argument_errors_before_any_launch(L):
     arr[0] = job(None, 4, 16, 256)  # data missing for a non-empty tensor
     assert L.fp4_amax_many(arr, 1, None) == 1
     arr[0] = job(4096, 4, 12, 256)  # cols % 8
-    assert L.fp4_amax_many(arr, 1, None) == 3
+    assert L.fp4_amax_many(arr, 1, None) == fq.FP4_ERR_SHAPE
     arr[0] = job(4104, 4, 16, 256)  # x not 16-byte aligned
     assert L.fp4_amax_many(arr, 1, None) == 2
     arr[0] = job(4096, 4, 16, 258)  # output not 4-byte aligned
@@ -102,7 +116,7 @@ def test_amax_many_argument_errors_before_any_launch(L):
 
 
 def test_mxfp4_to_fp8_argument_errors_before_any_launch(L):
-    assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 96, 4096, 4096, None) == 3  # cols % 128
+    assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 96, 4096, 4096, None) == fq.FP4_ERR_SHAPE  # cols % 128
     assert L.fp4_mxfp4_to_fp8(4096, 4096, -1, 128, 4096, 4096, None) == 1
     assert L.fp4_mxfp4_to_fp8(None, 4096, 4, 128, 4096, 4096, None) == 1
     assert L.fp4_mxfp4_to_fp8(4096, 4096, 4, 128, 4104, 4096, None) == 2  # q8 alignment
@@ -112,8 +126,8 @@ def test_mxfp4_to_fp8_argument_errors_before_any_launch(L):
 
 def test_mxfp4_to_fp8_transpose_argument_errors_before_any_launch(L):
     f = L.fp4_mxfp4_to_fp8_transpose
-    assert f(4096, 4096, 96, 128, 4096, 4096, None) == 3    # rows % 128
-    assert f(4096, 4096, 128, 48, 4096, 4096, None) == 3    # cols % 32
+    assert f(4096, 4096, 96, 128, 4096, 4096, None) == fq.FP4_ERR_SHAPE    # rows % 128
+    assert f(4096, 4096, 128, 48, 4096, 4096, None) == fq.FP4_ERR_SHAPE    # cols % 32
     assert f(4096, 4096, -128, 128, 4096, 4096, None) == 1
     assert f(4096, None, 128, 128, 4096, 4096, None) == 1
     assert f(4104, 4096, 128, 128, 4096, 4096, None) == 2   # q alignment
@@ -126,8 +140,8 @@ def test_amax_argument_errors_before_any_launch(L):
     assert f(4096, -4, 16, 0, 0, 256, None, None) == 1          # negative rows
     assert f(None, 4, 16, 0, 0, 256, None, None) == 1           # data missing
     assert f(4096, 4, 16, 8, 0, 256, 260, None) == 1            # Hadamard size not 16 / 32
-    assert f(4096, 4, 12, 0, 0, 256, None, None) == 3           # cols % 8
-    assert f(4096, 24, 16, 16, 0, 256, 260, None) == 3          # rows % hadamard_n
+    assert f(4096, 4, 12, 0, 0, 256, None, None) == fq.FP4_ERR_SHAPE           # cols % 8
+    assert f(4096, 24, 16, 16, 0, 256, 260, None) == fq.FP4_ERR_SHAPE          # rows % hadamard_n
     assert f(4104, 4, 16, 0, 0, 256, None, None) == 2           # x alignment
     assert f(4096, 4, 16, 0, 0, 258, None, None) == 2           # amax alignment
 
@@ -140,11 +154,52 @@ def test_quantize_transpose_argument_errors_before_any_launch(L):
     assert f(*args(fq.params(format=7))) == 1                   # bad format
     assert f(*args(fq.params(format=0, T=0.5))) == 1            # T below 1
     assert f(*args(fq.params(format=0, hadamard_n=8))) == 1     # Hadamard size
-    assert f(*args(fq.params(format=0, block2d=True, round_row=1))) == 4  # 2D with SR
+    assert f(*args(fq.params(format=0, block2d=True, round_row=1))) == fq.FP4_ERR_UNSUPPORTED  # 2D with SR
     assert f(*args(ok, rows=-16)) == 1
     assert f(*args(fq.params(format=0, hadamard_n=16))) == 1    # rotation needs amax_col
     assert f(*args(ok, x=None)) == 1
-    assert f(*args(ok, rows=24)) == 3                           # rows % 16
-    assert f(*args(fq.params(format=2), cols=48)) == 3          # MXFP4: cols % 32
-    assert f(*args(ok, sr=1024)) == 4                           # shifts only for UE5M3 + MMA
+    assert f(*args(ok, rows=24)) == fq.FP4_ERR_SHAPE                           # rows % 16
+    assert f(*args(fq.params(format=2), cols=48)) == fq.FP4_ERR_SHAPE          # MXFP4: cols % 32
+    assert f(*args(ok, sr=1024)) == fq.FP4_ERR_UNSUPPORTED                           # shifts only for UE5M3 + MMA
     assert f(*args(ok, qr=8200)) == 2                           # q_row alignment
+
+
+def test_t_col_argument_checks(L):
+    f = L.fp4_quantize_transpose
+    args = lambda p: (4096, 32, 32, 256, None, ctypes.byref(p), 8192, 16384, 512, None, 12288,
+                      20480, 516, None, None)
+    assert f(*args(fq.params(format=0, T_col=0.5))) == fq.FP4_ERR_INVALID_ARG
+    assert f(*args(fq.params(format=0, T_col=70000.0))) == fq.FP4_ERR_INVALID_ARG
+    # 2D weight tiles share one scale between the copies: one target only
+    assert f(*args(fq.params(format=0, block2d=True, T_col=2048.0))) == fq.FP4_ERR_UNSUPPORTED
+
+
+def _cpu_operand(rows, k, fmt=fq.FP4_FMT_NVFP4_B16, layout=fq.FP4_SF_MMA, shift=False):
+    q = torch.zeros((rows, k // 2), dtype=torch.uint8)
+    sf = torch.zeros(max(fq.fp4_sf_bytes(fmt, rows, k, layout), 16), dtype=torch.uint8)
+    sh = torch.zeros(rows, dtype=torch.int8) if shift else None
+    return fq.Quantized(q, sf, torch.ones(1), sh, fmt, layout)
+
+
+def test_gemm_wrapper_rejects_bad_operands_before_any_launch(L):
+    # plain-layout scales, missing UE5M3 shifts, bad out tensors: ValueError
+    # before the library is called (the operands here live on the CPU)
+    a, b = _cpu_operand(64, 128), _cpu_operand(32, 128)
+    with pytest.raises(ValueError, match="plain-layout"):
+        fq.gemm(_cpu_operand(64, 128, layout=fq.FP4_SF_PLAIN), b)
+    with pytest.raises(ValueError, match="plain-layout"):
+        fq.gemm_quantize(a, _cpu_operand(32, 128, layout=fq.FP4_SF_PLAIN), torch.ones(1),
+                         fq.params())
+    with pytest.raises(ValueError, match="row shifts"):
+        fq.gemm(_cpu_operand(64, 128, fmt=fq.FP4_FMT_UE5M3_B16),
+                _cpu_operand(32, 128, fmt=fq.FP4_FMT_UE5M3_B16, shift=True))
+    with pytest.raises(ValueError, match="formats"):
+        fq.gemm(a, _cpu_operand(32, 128, fmt=fq.FP4_FMT_MXFP4_B32))
+    with pytest.raises(ValueError, match="contraction"):
+        fq.gemm(a, _cpu_operand(32, 256))
+    for bad in (torch.empty((64, 32), dtype=torch.float16), torch.empty((64, 16)),
+                torch.empty((32, 64)).t()):
+        with pytest.raises(ValueError, match="out"):
+            fq.gemm(a, b, out=bad)
+    with pytest.raises(ValueError, match="out_dtype"):
+        fq.gemm(a, b, out_dtype=torch.float16)

@@ -66,7 +66,7 @@ def test_reencode_empty_and_argument_errors():
     s8 = torch.empty((4, 1), dtype=torch.float32, device="cuda")
     assert fq.fp4_mxfp4_to_fp8(q, sf, 0, 128, q8, s8) == fq.FP4_OK
     assert fq.fp4_mxfp4_to_fp8(q, sf, 4, 0, q8, s8) == fq.FP4_OK
-    assert fq.fp4_mxfp4_to_fp8(q, sf, 4, 96, q8, s8) == 3   # cols % 128
+    assert fq.fp4_mxfp4_to_fp8(q, sf, 4, 96, q8, s8) == fq.FP4_ERR_SHAPE   # cols % 128
     assert fq.fp4_mxfp4_to_fp8(q, sf, -1, 128, q8, s8) == 1
     assert fq.fp4_mxfp4_to_fp8(q, sf, 4, 128, q8, None) == 1
     assert fq.fp4_mxfp4_to_fp8(q[:, 1:], sf, 4, 128, q8, s8) == 2  # q not 16-byte aligned

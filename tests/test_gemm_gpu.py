@@ -134,7 +134,7 @@ def test_gemm_k_zero_and_empty():
     assert fq.fp4_gemm(A, B, 64, 32, 0, D, 0) == fq.FP4_OK
     torch.cuda.synchronize()
     assert torch.all(D == 0)
-    assert fq.fp4_gemm(A, B, 64, 32, 32, D, 0) == 3  # K % 64 != 0
+    assert fq.fp4_gemm(A, B, 64, 32, 32, D, 0) == fq.FP4_ERR_SHAPE  # K % 64 != 0
 
 
 def test_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
@@ -150,7 +150,7 @@ def test_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
     A, B = upload(a, NV), upload(b, NV)
     monkeypatch.setenv("FP4_TEST_STALL_PRODUCER", "1")
     fq.gemm(A, B)
-    assert fq.fp4_status_sync() == 6  # FP4_ERR_TIMEOUT
+    assert fq.fp4_status_sync() == fq.FP4_ERR_TIMEOUT
     monkeypatch.delenv("FP4_TEST_STALL_PRODUCER")
     assert fq.fp4_status_sync() == fq.FP4_OK  # cleared
     y = fq.gemm(A, B)
@@ -170,7 +170,7 @@ def test_gemm_shape_errors():
     assert fq.fp4_gemm(A, B, 128, 128, 128, D, 0) == 1  # mixed formats
     A2 = fq.fp4_operand(q.data_ptr(), sf.data_ptr(), sd.data_ptr(), None, UE, 128, 128)
     assert fq.fp4_gemm(A2, A2, 128, 128, 128, D, 0) == 1  # UE5M3 needs row shifts
-    assert fq.fp4_gemm(A, A, 128, 124, 128, D, 0) == 3  # N % 8
+    assert fq.fp4_gemm(A, A, 128, 124, 128, D, 0) == fq.FP4_ERR_SHAPE  # N % 8
 
 
 @pytest.mark.parametrize("fmt", [UE, NV, MX, U32])
@@ -211,3 +211,34 @@ def test_end_to_end_layer_small(fmt):
         Mo, No = yg.shape
         mm, nn = np.meshgrid(np.arange(Mo), np.arange(No), indexing="ij")
         check(yg, oa, ob, fmt, kk, mm.ravel(), nn.ravel(), name=f"{name} fmt{fmt}")
+
+
+def test_config_tiny_ue5m3_layer_seed0():
+    """The tiny configuration as stated: X 256x256 ~ N(0,1) with 0.1% of
+    entries x50, W 256x256 ~ N(0, 0.02) with 2D 16x16 tiles, UE5M3 block 16,
+    T = 448, nearest-even, amax fresh from each tensor, seed 0; both copies
+    of each operand emitted, and Y = X W^T in full against the probe-matched
+    model and the exact reference."""
+    need_gpu()
+    d = inputs.tiny(seed=0)
+    X, W = d["X"], d["W"]
+    assert X.shape == (256, 256) and W.shape == (256, 256)
+    P = lambda **kw: fq.params(format=UE, T=448.0, sf_layout=fq.FP4_SF_MMA, **kw)
+    xg, wg = X.cuda(), W.cuda()
+    ax, _ = fq.amax(xg)
+    aw, _ = fq.amax(wg)
+    x_r, x_c = fq.quantize_transpose(xg, ax, ax, P())
+    w_r, w_c = fq.quantize_transpose(wg, aw, aw, P(block2d=True))
+    y = fq.gemm(x_r, w_r)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    x32, w32 = f32(X), f32(W)
+    assert ax.item() == orc.amax(x32) and aw.item() == orc.amax(w32)
+    ox_r, ox_c = orc.quantize_transpose(x32, orc.amax(x32), orc.amax(x32), orc.UE5M3, T=448.0)
+    ow_r, ow_c = orc.quantize_transpose(w32, orc.amax(w32), orc.amax(w32), orc.UE5M3, T=448.0,
+                                        block2d=True)
+    for name, gq, oq in (("X.row", x_r, ox_r), ("X.col", x_c, ox_c), ("W.row", w_r, ow_r),
+                         ("W.col", w_c, ow_c)):
+        assert np.array_equal(gq.q.cpu().numpy(), oq["q"]), name
+        assert gq.s_dec.item() == np.float32(oq["s_dec"]), name
+    mm, nn = np.meshgrid(np.arange(256), np.arange(256), indexing="ij")
+    check(y, ox_r, ow_r, UE, 256, mm.ravel(), nn.ravel(), name="tiny fprop")

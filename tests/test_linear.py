@@ -33,21 +33,35 @@ def test_amax_cache_not_in_state_dict():
     assert set(m.state_dict().keys()) == {"weight"}
     assert m.p_w.block2d == 1 and m.p_x.block2d == 0
     assert m.p_dy.round_row == fq.FP4_ROUND_SR and m.p_dy.round_col == fq.FP4_ROUND_SR
-    m2 = FP4Linear(128, 64, T_dy=2048.0, device="cpu")
-    assert m2.p_dy.T == 2048.0 and m2.p_x.T == 448.0
+    m2 = FP4Linear(128, 64, T_dy=2048.0, device="cpu", check_status=False)
+    # the override reaches the Wgrad (transposed) copy of dY only
+    assert m2.p_dy.T == 448.0 and m2.p_dy.T_col == 2048.0 and m2.p_x.T == 448.0
+    assert m.p_dy.sr_seed != m2.p_dy.sr_seed     # distinct SR streams per module
+    m2.next_step()
+    assert m2.step == 1
+
+
+def test_next_step_raises_on_a_recorded_device_condition(monkeypatch):
+    import fp4_block_scaled_quantize_gb300.linear as L
+    m = FP4Linear(128, 64, device="cpu")
+    monkeypatch.setattr(L, "fp4_status_sync", lambda: fq.FP4_ERR_NONFINITE)
+    with pytest.raises(fq.FP4Error):
+        m.next_step()
+    assert m.step == 0
+    monkeypatch.setattr(L, "fp4_status_sync", lambda: fq.FP4_OK)
     m.next_step()
     assert m.step == 1
 
 
 # ----------------------------------------------------------------- GPU parity
 
-def _oracle_layer(X, W, dY, fmt, amax_x, amax_w, amax_dy, T_dy, offset):
+def _oracle_layer(X, W, dY, fmt, amax_x, amax_w, amax_dy, T_dy, offset, seed=42):
     of = ORC_FMT[fmt]
     x32, w32, dy32 = f32(X), f32(W), f32(dY)
     ox_r, ox_c = orc.quantize_transpose(x32, amax_x, amax_x, of)
     ow_r, ow_c = orc.quantize_transpose(w32, amax_w, amax_w, of, block2d=True)
-    ody_r, ody_c = orc.quantize_transpose(dy32, amax_dy, amax_dy, of, T=T_dy, sr_row=True,
-                                          sr_col=True, seed=42, offset=offset)
+    ody_r, ody_c = orc.quantize_transpose(dy32, amax_dy, amax_dy, of, T=448.0, T_col=T_dy,
+                                          sr_row=True, sr_col=True, seed=seed, offset=offset)
     return (ox_r, ow_r), (ody_r, ow_c), (ody_c, ox_c)
 
 
@@ -82,7 +96,8 @@ def test_linear_forward_backward_matches_oracle(fmt):
     assert fq.fp4_status_sync() == fq.FP4_OK
     assert y.dtype == torch.bfloat16 and x.grad.dtype == torch.bfloat16
     a32 = lambda t: float(np.max(np.abs(f32(t))))
-    fp, dg, wg = _oracle_layer(X, W, dY, fmt, a32(X), a32(W), a32(dY), T_dy, offset=0)
+    fp, dg, wg = _oracle_layer(X, W, dY, fmt, a32(X), a32(W), a32(dY), T_dy, offset=0,
+                               seed=lin.p_dy.sr_seed)
     _check_bf16(y, *fp, fmt, K, "fprop")
     _check_bf16(x.grad, *dg, fmt, N, "dgrad")
     _check_bf16(lin.weight.grad, *wg, fmt, M, "wgrad")

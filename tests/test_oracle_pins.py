@@ -718,3 +718,113 @@ def test_fp8_gemm_of_exact_reencodings_equals_the_mxfp4_product(seed):
     q8b, s8b = orc.mxfp4_to_fp8(qb, sfb)
     y8, s8 = orc.fp8_gemm_exact(q8a, s8a, q8b, s8b, mi, ni)
     assert np.array_equal(y4, y8) and np.array_equal(s4, s8)
+
+
+# -------------------------------------------------------------- amax (A1)
+
+def test_amax_is_the_largest_magnitude():
+    # numpy's own max of |x| is the independent reference; the cases are
+    # chosen so that a max without |.|, or a start value taken from x[0],
+    # gives a different answer
+    rng = np.random.default_rng(21)
+    cases = [
+        -(np.abs(rng.standard_normal(100)) + 0.5),                  # all negative
+        np.concatenate([[-9.0], rng.uniform(-1, 1, 50)]),           # largest first, negative
+        np.concatenate([rng.uniform(0, 1, 30), [-3.0], rng.uniform(0, 1, 30)]),
+        np.concatenate([[2.0], rng.uniform(-1, 1, 20), [-2.5]]),    # x[0] positive, larger |.| later
+        np.zeros(17), np.array([-0.0, 0.0, -0.0]),
+        rng.standard_normal(1000) * 1e-40,                           # binary32 subnormals
+        torch.randn(4096, generator=torch.Generator().manual_seed(3)).bfloat16().float().numpy(),
+    ]
+    for x in cases:
+        x = x.astype(F32)
+        got = orc.amax(x)
+        assert got == float(np.abs(x).max()), (got, np.abs(x).max())
+        assert got >= 0.0 and math.copysign(1.0, got) == 1.0
+    assert orc.amax(np.zeros(0, F32)) == 0.0
+
+
+@pytest.mark.parametrize("n,signs", [(16, 0), (16, 0x9A5C), (32, 0), (32, 0x9A5C3E71)])
+def test_amax_pair_rotated_view_against_sylvester_matrix(n, signs):
+    # The transposed view is x^T, rotated along its rows in aligned groups of
+    # n, i.e. down each column of x.  With small integers every butterfly sum
+    # is exact in binary32, so each rotated value is the exact integer
+    # H diag(s) x_group (scipy's Sylvester matrix, in float64) times the
+    # normaliser, rounded once: exact for n = 16 (0.25), one rounding of the
+    # product for n = 32 (RN32(1/sqrt 32) = 0x3E3504F3).
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(n + signs)
+    R, C = 4 * n, 24
+    x = rng.integers(-8, 9, size=(R, C)).astype(F32)
+    x[n:2 * n, 5] = 7.0          # a constant group: rotation piles it into one value
+    H = scipy_linalg.hadamard(n).astype(np.float64)
+    s = np.array([-1.0 if (signs >> j) & 1 else 1.0 for j in range(n)])
+    c = bits_to_f32(0x3E800000 if n == 16 else 0x3E3504F3)
+    ys = []
+    for col in range(C):
+        for g in range(R // n):
+            exact = H @ (s * x[g * n:(g + 1) * n, col].astype(np.float64))
+            ys.append(np.float32(exact).astype(F32) * F32(c))
+    want = float(np.max(np.abs(np.concatenate(ys))))
+    a_row, a_col = orc.amax_pair(x, n, signs)
+    assert a_row == float(np.abs(x).max())
+    assert a_col == want
+    assert a_col != a_row            # the unrotated transpose would give max |x|
+    assert orc.amax_pair(x, 0, 0) == (a_row, a_row)
+
+
+# ------------------------------------------------- 2D tile maximum (A3/A6)
+
+def test_2d_tile_scale_takes_the_max_over_the_whole_tile_ue5m3():
+    # One 16 x 16 tile, hand-worked.  The largest magnitude sits at row 5,
+    # column 11 (not in the first row or column, off the diagonal) and is
+    # negative; row 0 holds 1.0, everything else 0.5.  With the held amax at
+    # that element (7.5) and T = 448 the tile's scale is T itself (code 0xBE)
+    # and the element multiplier is 448 / 7.5 * (1/448) ... = 0.8 up to
+    # rounding: 1.0 -> 0.8 -> E2M1 1.0 (code 2), 0.5 -> 0.4 -> 0.5 (code 1),
+    # -7.5 -> -6 (code 0xF).  A tile max over row 0 alone (1.0) would give a
+    # scale ~7.5x smaller and encode the 1.0 entries as 6 (code 7).
+    x = np.full((16, 16), 0.5, F32)
+    x[0, :] = 1.0
+    x[5, 11] = -7.5
+    out_r, out_c = orc.quantize_transpose(x, 7.5, 7.5, orc.UE5M3, T=448.0, block2d=True)
+    assert orc.ue5m3_value(0xBE) == 448.0
+    assert (out_r["sf"] == 0xBE).all() and (out_c["sf"] == 0xBE).all()
+    nib = np.stack([out_r["q"] & 15, out_r["q"] >> 4], -1).reshape(16, 16)
+    want = np.full((16, 16), 1, np.uint8)
+    want[0, :] = 2
+    want[5, 11] = 0xF
+    np.testing.assert_array_equal(nib, want)
+    nib_c = np.stack([out_c["q"] & 15, out_c["q"] >> 4], -1).reshape(16, 16)
+    np.testing.assert_array_equal(nib_c, want.T)
+
+
+def test_2d_tile_scale_takes_the_max_over_the_whole_tile_mxfp4():
+    # 32 x 32 MXFP4 tile (reading: B x B tiles).  Max |x| = 24 at (13, 27):
+    # E = floor(log2 24) - 2 = 2, code 129; -24 * 2^-2 = -6 (code 0xF); the
+    # 0.25 entries become 0.0625 -> 0 (code 0).  A max over row 0 alone
+    # (0.25) would give E = -4 and encode 0.25 as 4 (code 6).
+    x = np.full((32, 32), 0.25, F32)
+    x[13, 27] = -24.0
+    out_r, out_c = orc.quantize_transpose(x, 24.0, 24.0, orc.MXFP4, block2d=True)
+    assert orc.e8m0_value(129) == 4.0
+    assert (out_r["sf"] == 129).all() and (out_c["sf"] == 129).all()
+    nib = np.stack([out_r["q"] & 15, out_r["q"] >> 4], -1).reshape(32, 32)
+    want = np.zeros((32, 32), np.uint8)
+    want[13, 27] = 0xF
+    np.testing.assert_array_equal(nib, want)
+
+
+def test_transposed_copy_target_t_col():
+    # The T override on the transposed copy only: the row-wise copy is what
+    # T gives alone, the transposed copy what T_col gives alone.
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((64, 64)) * 1e-4).astype(F32)
+    a = orc.amax(x)
+    r1, c1 = orc.quantize_transpose(x, a, a, orc.UE5M3, T=448.0, T_col=2048.0)
+    r0, _ = orc.quantize_transpose(x, a, a, orc.UE5M3, T=448.0)
+    _, c2 = orc.quantize_transpose(x, a, a, orc.UE5M3, T=2048.0)
+    np.testing.assert_array_equal(r1["sf"], r0["sf"])
+    np.testing.assert_array_equal(c1["sf"], c2["sf"])
+    np.testing.assert_array_equal(c1["q"], c2["q"])
+    assert c1["s_dec"] == c2["s_dec"] and r1["s_dec"] == r0["s_dec"]

@@ -54,7 +54,7 @@ def _check_copy(name, got, want, fmt, layout, remap):
 def _expect_status(st, fails):
     """The device reports FP4_ERR_SCALE_WINDOW exactly when the oracle's remap
     finds a block with no exact E4M3 image (planted outlier rows do)."""
-    assert st == (8 if fails else fq.FP4_OK), (fq.STATUS_NAMES.get(st), fails)
+    assert st == (fq.FP4_ERR_SCALE_WINDOW if fails else fq.FP4_OK), (fq.STATUS_NAMES.get(st), fails)
 
 
 CASES = [
@@ -278,7 +278,7 @@ def test_amax_many_reports_nonfinite():
     b = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
     b[7, 9] = float("nan")
     fq.amax_many([a, b])
-    assert fq.fp4_status_sync() == 7  # FP4_ERR_NONFINITE
+    assert fq.fp4_status_sync() == fq.FP4_ERR_NONFINITE
     assert fq.fp4_status_sync() == fq.FP4_OK
 
 
@@ -287,7 +287,7 @@ def test_nonfinite_amax_is_reported():
     x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
     x[3, 5] = float("inf")
     fq.amax(x)
-    assert fq.fp4_status_sync() == 7  # FP4_ERR_NONFINITE
+    assert fq.fp4_status_sync() == fq.FP4_ERR_NONFINITE
     assert fq.fp4_status_sync() == fq.FP4_OK  # cleared
 
 
@@ -301,7 +301,7 @@ def test_scale_window_is_reported():
     a = set_device_scalar(2688.0)  # s_enc = 1
     p = fq.params(format=UE, sf_layout=fq.FP4_SF_MMA)
     out = fq.quantize(xg, a, p)
-    assert fq.fp4_status_sync() == 8  # FP4_ERR_SCALE_WINDOW
+    assert fq.fp4_status_sync() == fq.FP4_ERR_SCALE_WINDOW
     want = orc.quantize(f32(xg.cpu()), 2688.0, orc.UE5M3)
     e4, shift, fails = orc.remap_ue5m3(want["sf"], want["q"])
     # 2^14 / 6 gives scale 2816 (shift 11 - 7 = 4): the 2^-14 block and the
@@ -319,12 +319,37 @@ def test_argument_errors_are_synchronous():
     q = torch.empty((64, 20), dtype=torch.uint8, device="cuda")
     sf = torch.empty(64 * 3, dtype=torch.uint8, device="cuda")
     sd = torch.empty(1, dtype=torch.float32, device="cuda")
-    assert fq.fp4_quantize(x, a, p, q, sf, sd) == 3  # FP4_ERR_SHAPE
+    assert fq.fp4_quantize(x, a, p, q, sf, sd) == fq.FP4_ERR_SHAPE
     x2 = torch.zeros((64, 48), dtype=torch.bfloat16, device="cuda")
     bad = fq.params(format=7)
     assert fq.fp4_quantize(x2, a, bad, q, sf, sd) == 1
     p2d = fq.params(format=UE, block2d=True, round_row=fq.FP4_ROUND_SR)
-    assert fq.fp4_quantize(x2, a, p2d, q, sf, sd) == 4
+    assert fq.fp4_quantize(x2, a, p2d, q, sf, sd) == fq.FP4_ERR_UNSUPPORTED
     big = torch.zeros(64 * 48 + 8, dtype=torch.bfloat16, device="cuda")
     xs = big[1:1 + 64 * 48].view(64, 48)  # 2-byte offset: misaligned
     assert fq.fp4_quantize(xs, a, p, q, sf, sd) == 2
+
+
+@pytest.mark.parametrize("fmt,sr,had", [(UE, True, 0), (NV, False, 16), (U32, True, 32)])
+def test_transposed_copy_target_override(fmt, sr, had):
+    """T_col (the Wgrad-dY override of the UE5M3 recipe) changes only the
+    transposed copy: each copy bit-exact against the oracle with its own
+    target."""
+    need_gpu()
+    g = torch.Generator().manual_seed(77)
+    x = (torch.randn((256, 384), generator=g) * 1e-4).to(torch.bfloat16)
+    xg = x.cuda()
+    ar, ac = fq.amax(xg, had, 0x1357 if had else 0)
+    p = fq.params(format=fmt, T=448.0, T_col=2048.0, round_row=int(sr), round_col=int(sr),
+                  sr_seed=5, hadamard_n=had, hadamard_signs=0x1357 if had else 0,
+                  sf_layout=fq.FP4_SF_MMA)
+    r, c = fq.quantize_transpose(xg, ar, ac, p)
+    st = fq.fp4_status_sync()
+    x32 = f32(x)
+    a_r, a_c = orc.amax_pair(x32, had, 0x1357 if had else 0)
+    want_r, want_c = orc.quantize_transpose(x32, a_r, a_c, ORC_FMT[fmt], T=448.0, T_col=2048.0,
+                                            sr_row=sr, sr_col=sr, seed=5, hadamard_n=had,
+                                            signs=0x1357 if had else 0)
+    fails = _check_copy("row", r, want_r, fmt, fq.FP4_SF_MMA, True)
+    fails += _check_copy("col", c, want_c, fmt, fq.FP4_SF_MMA, True)
+    _expect_status(st, fails)
