@@ -10,8 +10,9 @@ and backward pass through the FP4 path on the 8B MLP down_proj shapes:
          dgrad dX = dY W (8192 x 14336 x 4096, BF16 out),
          wgrad dW = dY^T X (4096 x 14336 x 8192, FP32 out).
 Inputs are seeded synthetic tensors with the workload's distributions,
-resident in HBM when the timed region starts; L2 is flushed (256 MB write)
-before every timed step.
+resident in HBM when the timed region starts; L2 is flushed (a read of a
+clean buffer twice its size) before every timed step.  Step times are the
+median over the timed steps.
 
 `value` is the step's roofline-normalised throughput: the time the step's
 kernels would take at the roofline (quantizer and amax bytes at the measured
@@ -39,6 +40,14 @@ M_TOK, K_FF, N_MODEL = 8192, 14336, 4096
 WORKLOAD = "8B MLP down_proj fwd+bwd (refresh step), UE5M3-b16"
 FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32", 3: "UE5M3-b32"}
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor ratio on GB300
+UNIT = "% of one GB300 roofline (step ideal time / step time, summed over GPUs)"
+L2_FLUSH_BYTES = 2 * 129 * 1000 * 1000  # twice the L2
+
+
+def flush_l2(buf):
+    """Evict L2 by reading a clean buffer twice its size (a read leaves no
+    dirty lines whose write-back would land in the next timed kernel)."""
+    torch.amax(buf)
 
 
 def peaks():
@@ -230,7 +239,7 @@ def run_gpu(args, world, rank, local):
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     layer = Layer(args.format, seed=args.seed + rank, device=dev)
     amax_b, qbytes, gemms, flops = work_model(args.format)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device=dev)
     names = ["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad", "end"]
 
     for _ in range(args.warmup):
@@ -249,10 +258,10 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
 
-    total_ms = 0.0
+    step_ms = []
     with Clocks(local) as clk:
         for _ in range(args.steps):
-            flush.fill_(1)
+            flush_l2(flush)
             s_ev = torch.cuda.Event(enable_timing=True)
             e_ev = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
@@ -263,29 +272,29 @@ def run_gpu(args, world, rank, local):
                 layer.step()
             e_ev.record()
             torch.cuda.synchronize()
-            total_ms += s_ev.elapsed_time(e_ev)
+            step_ms.append(s_ev.elapsed_time(e_ev))
     barrier(world)
     # per-kernel breakdown: the same steps launched one kernel at a time,
-    # each bracketed by events on the launching stream
-    per_kernel = {n: 0.0 for n in names[:-1]}
-    for _ in range(args.steps):
-        flush.fill_(1)
+    # each bracketed by events on the launching stream; median per kernel
+    per_kernel = {n: [] for n in names[:-1]}
+    for _ in range(min(args.steps, 50)):
+        flush_l2(flush)
         ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
         torch.cuda.synchronize()
         layer.step(ev)
         torch.cuda.synchronize()
         for a, b in zip(names, names[1:]):
-            per_kernel[a] += ev[a].elapsed_time(ev[b])
+            per_kernel[a].append(ev[a].elapsed_time(ev[b]))
     st = fq.fp4_status_sync()
     if st != fq.FP4_OK:
         raise RuntimeError("device status after timed steps: " + fq.STATUS_NAMES[st])
-    ms_step = reduce_max(total_ms / args.steps, world)
+    ms_step = reduce_max(statistics.median(step_ms), world)
 
     # roofline-ideal time of one step (seconds)
     hbm = pk["hbm_gbs"] * 1e9
     ideal = amax_b / hbm + sum(qbytes.values()) / hbm + sum(flops.values()) / (fp4_peak * 1e12)
     value = 100.0 * ideal / (ms_step * 1e-3) * world
-    avg = {k: v / args.steps for k, v in per_kernel.items()}
+    avg = {k: statistics.median(v) for k, v in per_kernel.items()}
     q_ms = avg["quant_X"] + avg["quant_W"] + avg["quant_dY"]
     g_ms = avg["fprop"] + avg["dgrad"] + avg["wgrad"]
     quant_gbs = sum(qbytes.values()) / (q_ms * 1e-3) / 1e9
@@ -304,14 +313,16 @@ def run_gpu(args, world, rank, local):
     out = {
         "metric": "quantize GB/s and FP4 block-scaled GEMM TFLOP/s, each as % of GB300 roofline",
         "value": round(value, 3),
-        "unit": "% of one GB300 roofline (step ideal time / step time, summed over GPUs)",
+        "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e2m1 payload x fp32 accumulate (u8 codes)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "format": FMT_NAMES[args.format],
                    "X": [M_TOK, K_FF], "W": [N_MODEL, K_FF], "dY": [M_TOK, N_MODEL],
-                   "amax": "current (D=1 refresh step)", "l2": "flushed before each step",
+                   "amax": "current (D=1 refresh step)",
+                   "l2": "flushed before each step (read of a clean 258 MB buffer)",
+                   "timing": "median of the timed steps",
                    "launch": "CUDA graph of the whole step" if graph is not None else "eager",
                    "parallelism": f"replicas x{world}"},
         "quantize": {"gbs": round(quant_gbs, 1), "frac": round(quant_gbs / pk["hbm_gbs"], 4),
@@ -344,7 +355,7 @@ def graph_ms(fn, flush, reps=20):
     def cap(with_fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            flush.fill_(1)
+            flush_l2(flush)
             if with_fn:
                 fn()
         return g
@@ -449,7 +460,7 @@ def run_linear(layer, flush, steps=10):
         tot = 0.0
         for _ in range(steps):
             lin.step = step
-            flush.fill_(1)
+            flush_l2(flush)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
@@ -533,7 +544,7 @@ def run_e2e(layer, args, world, ideal, graph=None):
     ms = reduce_max(s.elapsed_time(e) / steps, world)
     fq._check(fq.fp4_status_sync(), "e2e")
     return {"value": round(100.0 * ideal / (ms * 1e-3) * world, 3),
-            "unit": "% of one GB300 roofline (summed over GPUs)", "ms_per_step": round(ms, 4),
+            "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "uploads, compute and downloads of consecutive steps overlap "
                        "(two device buffer sets, one copy stream per direction)"}
@@ -543,9 +554,11 @@ def gemm_source_digest():
     """Short digest of the GEMM kernel source: a traffic figure measured on
     another version of the kernel is stale."""
     import hashlib
-    path = os.path.join(ROOT, "fp4_block_scaled_quantize_gb300", "csrc", "gemm.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "gemm2.cu", "tcgen05.cuh"):
+        with open(os.path.join(ROOT, "fp4_block_scaled_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(kernel):
@@ -575,7 +588,7 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
 
     import oracle as orc
     from fp4_block_scaled_quantize_gb300 import inputs
-    fmt = {0: orc.UE5M3, 1: orc.NVFP4, 2: orc.MXFP4}[args.format]
+    fmt = {0: orc.UE5M3, 1: orc.NVFP4, 2: orc.MXFP4, 3: orc.UE5M3_B32}[args.format]
     R = sample_rows
     g = inputs.down_proj_8b(seed=args.seed, M=R * 2, K=K_FF, N=N_MODEL)
     threads = os.cpu_count() or 1
@@ -612,7 +625,7 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
 
 def cpu_baseline(args, ideal):
     secs, threads, desc = oracle_step_seconds(args)
-    return {"value": 100.0 * ideal / secs, "unit": "% of one GB300 roofline", "cores": threads,
+    return {"value": 100.0 * ideal / secs, "unit": UNIT, "cores": threads,
             "kind": "oracle", "sample": desc, "seconds_per_step_extrapolated": round(secs, 1)}
 
 
@@ -632,20 +645,23 @@ def run_reference(args, world, rank):
         times.append(s)
         if time.time() - t_start > 90.0:
             break
-    secs = statistics.mean(times)
+    secs = statistics.median(times)
     value = 100.0 * ideal / secs
     out = {"impl": "reference",
            "metric": "quantize GB/s and FP4 block-scaled GEMM TFLOP/s, each as % of GB300 roofline",
-           "value": value, "unit": "% of one GB300 roofline", "n_gpus": world,
+           "value": value, "unit": UNIT, "n_gpus": world,
            "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,
-           "ms_per_step": secs * 1e3,
+           "ms_per_step": secs * 1e3, "ms_per_step_extrapolated": True,
+           "timing": "each step times the oracle on a bounded sample of the step (rows of each "
+                     "producer, sampled GEMM outputs) and extrapolates to the full step; median "
+                     "over steps",
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "e2m1 payload x exact accumulate (u8 codes)", "data": "synthetic",
            "config": {"workload": WORKLOAD, "format": FMT_NAMES[args.format],
                       "X": [M_TOK, K_FF], "W": [N_MODEL, K_FF], "dY": [M_TOK, N_MODEL]},
-           "cpu_baseline": {"value": value, "unit": "% of one GB300 roofline", "kind": "oracle",
+           "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                             "cores": threads, "sample": desc},
-           "e2e": {"value": value, "unit": "% of one GB300 roofline", "h2d_bytes_per_step": 0,
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
@@ -699,7 +715,16 @@ def main():
                              "reencode", "reencode_t"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch this command under torchrun
+        port = os.environ.get("MASTER_PORT", "29500")
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr=127.0.0.1",
+               f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
     world, rank, local = dist_init()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.profile:
         run_profile(args, local)
     elif args.impl == "reference":

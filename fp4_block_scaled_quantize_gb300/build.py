@@ -28,6 +28,7 @@ UNITS = {
     "remap.cu": ["-fmad=false"],
     "convert.cu": ["-fmad=false"],
     "gemm.cu": [],
+    "gemm2.cu": [],
 }
 
 

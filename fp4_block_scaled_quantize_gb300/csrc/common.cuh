@@ -131,5 +131,7 @@ struct GemmJob {
   uint32_t offset_out;
 };
 fp4_status launch_gemm(const GemmJob &j, cudaStream_t s);
+// Plain GEMM on SM pairs (tcgen05 cta_group::2); K > 0, no fused output.
+fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s);
 
 }  // namespace fp4

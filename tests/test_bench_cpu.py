@@ -63,3 +63,18 @@ dist.destroy_process_group()
                         "--nproc-per-node=2", "--master-addr=127.0.0.1", "--master-port=29733",
                         path], cwd=ROOT, capture_output=True, text=True, timeout=300, env=_env())
     assert r.returncode == 0, r.stderr[-3000:]
+
+
+def test_gpus_flag_spawns_ranks_without_torchrun():
+    # --gpus 2 outside torchrun relaunches itself with two ranks
+    env = _env()
+    env["MASTER_PORT"] = "29737"
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--gpus", "2", "--format", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["config"]["format"] == "UE5M3-b32"
+    assert d["ms_per_step_extrapolated"] is True

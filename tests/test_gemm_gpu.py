@@ -137,13 +137,16 @@ def test_gemm_k_zero_and_empty():
     assert fq.fp4_gemm(A, B, 64, 32, 32, D, 0) == fq.FP4_ERR_SHAPE  # K % 64 != 0
 
 
-def test_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
+@pytest.mark.parametrize("M", [128, 384])
+def test_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch, M):
     """Failure detection without a GPU fault: with the producer stalled by the
     test switch, the MMA and epilogue waits run out after about a second, the
     kernel returns, fp4_status_sync reports FP4_ERR_TIMEOUT, and the next
-    GEMM on the same context is correct."""
+    GEMM on the same context is correct.  M = 128 runs the one-SM kernel,
+    M = 384 the SM-pair kernel (both CTAs of every pair time out and leave
+    through the final cluster barrier)."""
     need_gpu()
-    M, N, K = 128, 256, 256
+    N, K = 256, 256
     d = inputs.sweep_operand(M + N, K, seed=1)
     a = oracle_operand(d[:M], NV)
     b = oracle_operand(d[M:], NV)
