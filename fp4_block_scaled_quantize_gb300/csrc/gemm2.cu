@@ -30,10 +30,16 @@
 //           peer's arrival ~200 ns, so a lockstep hand-off per stage (as a
 //           named barrier with the MMA warp would impose) tripled the time
 //           of a stage;
-//   warp 1  MMA issuer (leader CTA only): waits for the stage's ready
-//           barrier, issues four tcgen05.mma.cta_group::2 (M256 N256 K64),
-//           commits multicast to both CTAs' empty barriers, and at the end
-//           of a tile to both CTAs' accumulator barriers;
+//   warp 14 waiter (leader CTA only): polls the stage's ready barrier (and,
+//           at the start of a tile, the accumulator-empty barrier) and hands
+//           the stage to the MMA warp through a named barrier.  Measured on
+//           this part, a shared-memory barrier poll by the thread that
+//           issues the MMAs waits behind that thread's MMAs in flight and
+//           drains the tensor pipe every stage;
+//   warp 1  MMA issuer (leader CTA only): per stage handed over, four
+//           tcgen05.mma.cta_group::2 (M256 N256 K64) from one thread, a
+//           commit multicast to both CTAs' empty barriers, and at the end of
+//           a tile to both CTAs' accumulator barriers;
 //   warps 6-13 epilogue (both CTAs): each CTA drains its own 128 x 256
 //           accumulator, releases it to the leader, then scales and stores.
 // Every wait is bounded (about one second); on expiry the CTA raises the
@@ -71,7 +77,10 @@ constexpr int NBARS = 3 * STAGES + 3;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 8 * NBARS + 16;
 constexpr int EPI_WARPS = 8;
 constexpr int SF_WARPS = 4;
-constexpr int THREADS = 64 + 32 * SF_WARPS + 32 * EPI_WARPS;
+constexpr int WAITER_WARP = 2 + SF_WARPS + EPI_WARPS;  // the last warp
+constexpr int THREADS = 32 * (WAITER_WARP + 1);
+constexpr uint32_t kHandoffBar = 2;   // leader: MMA warp + waiter warp
+constexpr uint32_t kHandoffThreads = 64;
 constexpr uint32_t kScaleBar = 1;     // the scale warps of a CTA among themselves
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;       // 256 binary32 columns
@@ -134,14 +143,19 @@ __device__ __forceinline__ void mbar_arrive_local_relaxed(uint32_t addr) {
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
-// Bounded wait on a barrier that the peer CTA arrives on (acquire at cluster
-// scope); polls with test_wait like the MMA issuer's wait.
+// Bounded wait of the waiter warp on a barrier that both CTAs arrive on (the
+// stage-ready and accumulator-empty barriers); polls with test_wait.
+// Relaxed: the arrivals only publish completed work (landed TMA copies,
+// tensor-memory stores and loads waited for), and the tcgen05 fence after
+// the wait orders the MMAs behind it.  Measured on this part, an acquire at
+// cluster scope made each poll take ~200 ns, nearly the time of the stage's
+// MMAs.
 __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                volatile int *abort_flag, uint32_t *status) {
   auto test = [&]() {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], "
         "%2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -318,51 +332,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (issued_parity >> s) & 1u);
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    // One thread of the leader issues every MMA of the pair.
-    if (leader && lane == 0) {
+    // One thread of the leader issues every MMA of the pair; the whole warp
+    // meets the waiter warp at the hand-off barrier once per stage.
+    if (leader) {
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool any = false;
-      for (int tile = cid; tile < ntiles; tile += ncl) {
-        bool good = mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag, p.status);
-        for (int kt = 0; good && kt < p.k_tiles; ++kt) {
-          // both CTAs' operands landed and scales staged
-          if (!mbar_wait_cluster(ready_bar(stage), phase, abort_flag, p.status)) {
-            good = false;
+      bool abort_seen = false, any = false;
+      for (int tile = cid; !abort_seen && tile < ntiles; tile += ncl) {
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          // both CTAs' operands landed and scales staged (or abort)
+          if (bar_red_or(kHandoffBar, kHandoffThreads, false)) {
+            abort_seen = true;
             break;
           }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
-          const int nks = min(4, p.k_steps - 4 * kt);
-          const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
-          const uint32_t sfb_t = sfa_t + 16;
-          const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
-          for (int kk = 0; kk < nks; ++kk) {
-            const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
-            const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
-            tc_mma_pair<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc_pair<FMT>(id, id),
-                             sfa_t + 4 * a, sfb_t + 8 * a, (kt | kk) != 0);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + stage * STAGE_BYTES);
+            const int nks = min(4, p.k_steps - 4 * kt);
+            const uint32_t sfa_t = tmem + SF_COL0 + SF_SLOT * (uint32_t)stage;
+            const uint32_t sfb_t = sfa_t + 16;
+            const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
+            for (int kk = 0; kk < nks; ++kk) {
+              const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
+              const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
+              tc_mma_pair<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc_pair<FMT>(id, id),
+                               sfa_t + 4 * a, sfb_t + 8 * a, (kt | kk) != 0);
+            }
+            tc_commit_pair(empty_bar(stage));
+            any = true;
           }
-          tc_commit_pair(empty_bar(stage));
-          any = true;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          __syncwarp();
+          if (++stage == STAGES) stage = 0;
         }
-        if (!good) {
-          abort_both();
-          break;
-        }
-        tc_commit_pair(acc_full);
-        acc_phase ^= 1u;
+        if (abort_seen) break;
+        if (lane == 0) tc_commit_pair(acc_full);
       }
-      if (any) {  // every MMA this thread issued has completed
+      if (lane == 0 && any) {  // every MMA this thread issued has completed
         tc_commit_local(drain);
         mbar_wait_drain(drain, 0);
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp >= 2 && warp < 2 + SF_WARPS) {
     // ------------------------------------------------- scale-factor warps
     // Warp w writes tensor-memory lanes 32 (w % 4) .. +31 of the stage's
@@ -421,6 +430,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           stage = 0;
           phase ^= 1u;
         }
+      }
+    }
+  } else if (warp == WAITER_WARP) {
+    // ---------------------------------------------------------------- waiter
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < ntiles; tile += ncl) {
+        int good = 1;
+        if (lane == 0)
+          good = mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (good && lane == 0)
+            good = mbar_wait_cluster(ready_bar(stage), phase, abort_flag, p.status) ? 1 : 0;
+          good = __shfl_sync(0xFFFFFFFFu, good, 0);
+          if (!good && lane == 0) abort_both();
+          if (bar_red_or(kHandoffBar, kHandoffThreads, !good)) {
+            ok = false;
+            break;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        acc_phase ^= 1u;
       }
     }
   } else if (warp >= 2 + SF_WARPS) {
