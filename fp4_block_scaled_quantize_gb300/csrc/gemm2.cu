@@ -74,7 +74,7 @@ constexpr int SFA_BYTES = 4 * 512;         // up to 4 scale tiles (block 16)
 constexpr int SFB_BYTES = 2 * 4 * 512;     // both 128-row groups of the pair's B rows
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
 constexpr int NBARS = 3 * STAGES + 3;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 8 * NBARS + 16;  // + flag, tmem, 2 words
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 8 * NBARS + 16;  // + flag, tmem
 constexpr int EPI_WARPS = 8;
 constexpr int SF_WARPS = 4;
 constexpr int WAITER_WARP = 2 + SF_WARPS + EPI_WARPS;  // the last warp
@@ -136,11 +136,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-// Plain named barrier over `nthreads` threads (whole warps); the per-stage
-// hand-off from the waiter warp to the MMA warp.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_local_relaxed(uint32_t addr) {
   asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
@@ -241,15 +236,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
   // bars: full[S], empty[S], ready[S] (leader: both CTAs' scales staged),
   // acc_full, acc_empty, drain;
-  // then the abort flag, the tensor-memory address and the hand-off word
+  // then the abort flag and the tensor-memory address
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + NBARS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS) + 1;
-  // the waiter's go / stop decision for the k-th stage it hands over, in
-  // slot k % 2: written before the hand-off barrier and read by the MMA warp
-  // after it, so both leave together (the abort flag itself may change
-  // between two reads).  The waiter reaches hand-off k + 2, which reuses the
-  // slot, only after the MMA warp has joined hand-off k + 1.
-  volatile int *handoff_stop = reinterpret_cast<volatile int *>(bars + NBARS) + 2;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -348,13 +337,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // meets the waiter warp at the hand-off barrier once per stage.
     if (leader) {
       int stage = 0;
-      uint32_t hk = 0;  // hand-offs so far
       bool abort_seen = false, any = false;
       for (int tile = cid; !abort_seen && tile < ntiles; tile += ncl) {
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          // both CTAs' operands landed and scales staged (or stop)
-          named_bar_sync(kHandoffBar, kHandoffThreads);
-          if (handoff_stop[hk++ & 1]) {
+          // both CTAs' operands landed and scales staged (or abort: the
+          // barrier ORs the waiter's flag, so both warps leave together)
+          if (bar_red_or(kHandoffBar, kHandoffThreads, false)) {
             abort_seen = true;
             break;
           }
@@ -450,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- waiter
     if (leader) {
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0, hk = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < ntiles; tile += ncl) {
         int good = 1;
@@ -459,14 +447,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (good && lane == 0)
             good = mbar_wait_cluster(ready_bar(stage), phase, abort_flag, p.status) ? 1 : 0;
-          if (lane == 0) {
-            if (!good) abort_both();
-            handoff_stop[hk & 1] = good ? 0 : 1;
-          }
           good = __shfl_sync(0xFFFFFFFFu, good, 0);
-          named_bar_sync(kHandoffBar, kHandoffThreads);
-          ++hk;
-          if (!good) {
+          if (!good && lane == 0) abort_both();
+          if (bar_red_or(kHandoffBar, kHandoffThreads, !good)) {
             ok = false;
             break;
           }
