@@ -69,29 +69,6 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
 __device__ __forceinline__ float f32x2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
 __device__ __forceinline__ float f32x2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
 
-// Stochastic rounding with 16 random bits r16: between the neighbouring
-// codebook values lo <= |v| < hi, round up iff r16 < 65536 (|v|-lo)/(hi-lo).
-// For |v| in [1, 6) the value sits in a binade with one kept mantissa bit,
-// so (|v|-lo)/(hi-lo) is the dropped 22-bit mantissa tail over 2^22 and the
-// test is the integer comparison r16 * 64 < tail.  Below 1 the codebook step
-// is 0.5: t = 2|v|, and the fraction is t - floor(t), exact.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-  const float a = fabsf(v);
-  const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-  // [1, 6): adding 2^22 - 1 - 64 r16 to the bit pattern carries into the kept
-  // mantissa bit exactly when tail > 64 r16; the code is then the pattern's
-  // top bits (1.0 = 0x3F800000 -> 254 -> code 2).
-  const uint32_t u = __float_as_uint(a) + (0x3FFFFFu - (r16 << 6));
-  const uint32_t c_hi = (u >> 22) - 252u;
-  // [0, 1): step 0.5, t = 2|v|, fraction t - floor(t) exact.
-  const float t = __fmul_rn(a, 2.0f);
-  const float c = (t >= 1.0f) ? 1.0f : 0.0f;
-  const float f = __fmul_rn(__fsub_rn(t, c), 65536.0f);
-  const uint32_t c_lo = (uint32_t)c + (uint32_t)(__uint2float_rn(r16) < f);
-  const uint32_t code = (a >= 6.0f) ? 7u : ((a >= 1.0f) ? c_hi : c_lo);
-  return code | sign;
-}
-
 // --------------------------------------------------------------- UE5M3
 // Unsigned E5M3, bias 15, exponent 31 reserved: normal (8+m) 2^(e-18),
 // subnormal m 2^-17, largest 0xF7 = 61,440.
@@ -323,26 +300,44 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Random bits for the 8-element group g of copy `copy`: element j of the
-// group uses bits [16 (j&1), +16) of word j>>1.
-__device__ __forceinline__ uint4 sr_group_bits(uint64_t seed, uint32_t offset, uint32_t copy,
-                                               uint64_t g) {
-  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), copy, offset), (uint32_t)seed,
-                       (uint32_t)(seed >> 32));
+// Stochastic rounding ("UE5M3 FP4 Block Scaling for Stable Language Model
+// Pretraining", Approach: SR on the upstream gradient).  The random bits of
+// a copy come in groups of 16 consecutive elements: group g draws one
+// Philox4x32-10 block with counter (g_lo, g_hi, copy, offset) and key
+// (seed_lo, seed_hi); word i of it serves elements 4i .. 4i + 3.  Within a
+// word w the four elements take 16 bits each -- element 0 (w[23:16] << 8) |
+// w[7:0], element 2 (w[31:24] << 8) | w[15:8], elements 1 and 3 the bit
+// reversals of those -- and each rounds up iff the floor of 2^16 times its
+// fraction between the neighbouring codes, plus its 16 bits, reaches 2^16.
+// That is exactly what the hardware conversion cvt.rs.satfinite.e2m1x4.f32
+// does with the word (its first operand lands in the top nibble, so the
+// elements are passed in reverse order); it saturates at 6, keeps the sign
+// and maps -0 to 8 like the nearest-even encoder.
+__device__ __forceinline__ uint32_t e2m1x4_sr(const float *v, uint32_t w) {
+  uint16_t r;
+  asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=h"(r)
+      : "f"(v[3]), "f"(v[2]), "f"(v[1]), "f"(v[0]), "r"(w));
+  return r;
 }
-
-__device__ __forceinline__ uint32_t sr_r16(const uint4 &w, int j) {
-  uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
-  return (word >> (16 * (j & 1))) & 0xFFFFu;
+// The four random words of the copy's 16-element group g16: word i serves
+// elements 4i .. 4i + 3 of the group.
+__device__ __forceinline__ uint4 sr_words16(uint64_t seed, uint32_t offset, uint32_t copy,
+                                            uint64_t g16) {
+  return philox4x32_10(make_uint4((uint32_t)g16, (uint32_t)(g16 >> 32), copy, offset),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
 }
-
-// Eight stochastically rounded E2M1 codes (value j in bits 4j..4j+3) from
-// the group's random bits.
-__device__ __forceinline__ uint32_t encode8_sr(const float *v, const uint4 &bits) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) w |= e2m1_sr(v[j], sr_r16(bits, j)) << (4 * j);
-  return w;
+// Eight stochastically rounded codes (element j in bits 4j .. 4j + 3) from
+// the two words of their half of a 16-element group.
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float *v, uint32_t w0, uint32_t w1) {
+  return e2m1x4_sr(v, w0) | (e2m1x4_sr(v + 4, w1) << 16);
+}
+// Sixteen stochastically rounded codes (element j in bits 4j .. 4j + 3 of
+// word j / 8) of the copy's 16-element group g16.
+__device__ __forceinline__ uint2 encode16_sr(const float *v, uint64_t seed, uint32_t offset,
+                                             uint32_t copy, uint64_t g16) {
+  const uint4 w = sr_words16(seed, offset, copy, g16);
+  return make_uint2(e2m1x8_sr(v, w.x, w.y), e2m1x8_sr(v + 8, w.z, w.w));
 }
 
 // Scale 8 values of a block by mult (0 * inf read as 0; zero payload -> 0).

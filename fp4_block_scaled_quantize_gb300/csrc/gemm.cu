@@ -413,16 +413,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             float mult;
             bool zp;
             code = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
-            for (int h = 0; h < QB / 8; ++h) {
-              float v[8];
+            for (int g = 0; g < QB / 16; ++g) {
+              float v[16];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
+              for (int j = 0; j < 16; ++j) v[j] = y[o + 16 * g + j];
               scale8(v, mult, zp);
-              const int64_t n = n0 + o + 8 * h;
-              qacc[4 * q + 2 * blk + h] =
-                  p.sr_out ? encode8_sr(v, sr_group_bits(p.seed_out, p.offset_out, 0u,
-                                                         ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 3))
-                           : e2m1x8_hw(v);
+              scale8(v + 8, mult, zp);
+              const int64_t n = n0 + o + 16 * g;
+              if (p.sr_out) {
+                // one Philox block per 16 elements of the output row
+                const uint2 qq = encode16_sr(v, p.seed_out, p.offset_out, 0u,
+                                             ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 4);
+                qacc[4 * q + 2 * blk + 2 * g] = qq.x;
+                qacc[4 * q + 2 * blk + 2 * g + 1] = qq.y;
+              } else {
+                qacc[4 * q + 2 * blk + 2 * g] = e2m1x8_hw(v);
+                qacc[4 * q + 2 * blk + 2 * g + 1] = e2m1x8_hw(v + 8);
+              }
             }
           }
           // code of scale column (q * nb + blk) of this lane's 128 columns

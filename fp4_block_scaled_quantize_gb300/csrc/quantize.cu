@@ -296,40 +296,41 @@ __global__ void __launch_bounds__(kThreads, 4)
       float mult;
       bool zp;
       const uint32_t code = block_scale_bf16<FMT>(b, se_r, ctab_r, mtab_r, mult, zp);
+      // 16 elements at a time: under SR one Philox block covers 16 elements
+      // of the copy row
+      const bool careful = __any_sync(0xFFFFFFFFu, zp || isinf(mult));
+      const uint64_t mm = pack_f32x2(mult, mult);
       uint32_t out[B / 8];
-      if (__any_sync(0xFFFFFFFFu, zp || isinf(mult))) {
-        // a zero-payload block or an infinite multiplier somewhere in the
-        // warp: the careful path (0 * inf read as 0)
 #pragma unroll
-        for (int h = 0; h < B / 8; ++h) {
-          float v[8];
+      for (int g = 0; g < B / 16; ++g) {
+        float v[16];
+        if (careful) {
+          // a zero-payload block or an infinite multiplier somewhere in the
+          // warp: the careful path (0 * inf read as 0)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[2 * k] = bf16_lo(w[4 * h + k]);
-            v[2 * k + 1] = bf16_hi(w[4 * h + k]);
+          for (int k = 0; k < 8; ++k) {
+            v[2 * k] = bf16_lo(w[8 * g + k]);
+            v[2 * k + 1] = bf16_hi(w[8 * g + k]);
           }
           scale8(v, mult, zp);
-          out[h] = (SR && p.sr_row) ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
-                                                          ((uint64_t)gr * (uint64_t)C +
-                                                           (uint64_t)(gc + 8 * h)) >> 3))
-                            : e2m1x8_hw(v);
-        }
-      } else {
-        // v = RN32(x * mult), two products per packed multiply
-        const uint64_t mm = pack_f32x2(mult, mult);
+          scale8(v + 8, mult, zp);
+        } else {
+          // v = RN32(x * mult), two products per packed multiply
 #pragma unroll
-        for (int h = 0; h < B / 8; ++h) {
-          float v[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(w[4 * h + k]), mm);
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t r2 = mul_f32x2(bf16x2_to_f32x2(w[8 * g + k]), mm);
             v[2 * k] = f32x2_lo(r2);
             v[2 * k + 1] = f32x2_hi(r2);
           }
-          out[h] = (SR && p.sr_row) ? encode8_sr(v, sr_group_bits(p.seed, p.offset, 0u,
-                                                          ((uint64_t)gr * (uint64_t)C +
-                                                           (uint64_t)(gc + 8 * h)) >> 3))
-                            : e2m1x8_hw(v);
+        }
+        if (SR && p.sr_row) {
+          const uint2 q = encode16_sr(v, p.seed, p.offset, 0u,
+                                      ((uint64_t)gr * (uint64_t)C + (uint64_t)(gc + 16 * g)) >> 4);
+          out[2 * g] = q.x;
+          out[2 * g + 1] = q.y;
+        } else {
+          out[2 * g] = e2m1x8_hw(v);
+          out[2 * g + 1] = e2m1x8_hw(v + 8);
         }
       }
       if (gr < R && gc < C) {
@@ -359,21 +360,25 @@ __global__ void __launch_bounds__(kThreads, 4)
       const uint32_t code = block_scale_tab<FMT>(bmax, se_c, mtab_c, mult, zp);
       const int tcol = col0 + c;
       const int64_t gcol = C0 + tcol;
+      // 16 rows at a time: under SR one Philox block covers 16 elements of
+      // the transposed copy's row
 #pragma unroll
-      for (int h8 = 0; h8 < B / 8; ++h8) {
-        float e[8];
+      for (int g = 0; g < B / 16; ++g) {
+        float e[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) e[j] = value(rb + 8 * h8 + j);
+        for (int j = 0; j < 16; ++j) e[j] = value(rb + 16 * g + j);
         scale8(e, mult, zp);
-        uint32_t word;
-        const int trow = row0 + rb + 8 * h8;
+        scale8(e + 8, mult, zp);
         if (SR && p.sr_col) {
-          uint64_t g = ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
-          word = encode8_sr(e, sr_group_bits(p.seed, p.offset, 1u, g));
+          const uint64_t g16 =
+              ((uint64_t)gcol * (uint64_t)R + (uint64_t)(R0 + row0 + rb + 16 * g)) >> 4;
+          const uint2 q = encode16_sr(e, p.seed, p.offset, 1u, g16);
+          cw[c][(rb >> 3) + 2 * g] = q.x;
+          cw[c][(rb >> 3) + 2 * g + 1] = q.y;
         } else {
-          word = e2m1x8_hw(e);
+          cw[c][(rb >> 3) + 2 * g] = e2m1x8_hw(e);
+          cw[c][(rb >> 3) + 2 * g + 1] = e2m1x8_hw(e + 8);
         }
-        cw[c][(rb >> 3) + h8] = word;
       }
       sfc[tcol][(row0 + rb) / B] = (uint8_t)code;
     };
@@ -443,6 +448,9 @@ __global__ void __launch_bounds__(kThreads, 4)
           const uint32_t code1 = block_scale_bf16<FMT>(bmax[2 * k + 1], se_c, ctab_c, mtab_c, m1, z1);
           const bool fast = !__any_sync(0xFFFFFFFFu, z0 || z1 || isinf(m0) || isinf(m1));
           const uint64_t mm = pack_f32x2(m0, m1);
+          // 8 rows of both columns at a time; under SR one Philox block
+          // per column covers 16 rows of the transposed copy
+          uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
 #pragma unroll
           for (int h8 = 0; h8 < B / 8; ++h8) {
             float v0[8], v1[8];
@@ -458,12 +466,15 @@ __global__ void __launch_bounds__(kThreads, 4)
                 v1[j] = z1 ? 0.0f : scale_elem(bf16_hi(x), m1);
               }
             }
-            const int trow = row0 + 8 * h8;
             if (SR && p.sr_col) {
-              const uint64_t g0 = ((uint64_t)(C0 + col0 + 2 * k) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
-              const uint64_t g1 = ((uint64_t)(C0 + col0 + 2 * k + 1) * (uint64_t)R + (uint64_t)(R0 + trow)) >> 3;
-              cw[2 * k][h8] = encode8_sr(v0, sr_group_bits(p.seed, p.offset, 1u, g0));
-              cw[2 * k + 1][h8] = encode8_sr(v1, sr_group_bits(p.seed, p.offset, 1u, g1));
+              if ((h8 & 1) == 0) {
+                const uint64_t r16 = (uint64_t)(R0 + row0 + 8 * h8);
+                r0 = sr_words16(p.seed, p.offset, 1u, ((uint64_t)(C0 + col0 + 2 * k) * (uint64_t)R + r16) >> 4);
+                r1 = sr_words16(p.seed, p.offset, 1u,
+                                ((uint64_t)(C0 + col0 + 2 * k + 1) * (uint64_t)R + r16) >> 4);
+              }
+              cw[2 * k][h8] = (h8 & 1) ? e2m1x8_sr(v0, r0.z, r0.w) : e2m1x8_sr(v0, r0.x, r0.y);
+              cw[2 * k + 1][h8] = (h8 & 1) ? e2m1x8_sr(v1, r1.z, r1.w) : e2m1x8_sr(v1, r1.x, r1.y);
             } else {
               cw[2 * k][h8] = e2m1x8_hw(v0);
               cw[2 * k + 1][h8] = e2m1x8_hw(v1);

@@ -203,9 +203,13 @@ fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols,
  * of every n consecutive elements of its rows (butterflies of span 1, 2, 4,
  * ... in binary32, then the normaliser).  With block2d both copies share
  * the B x B tile scales and the transposed payload is the nibble transpose.
- * SR draws Philox4x32-10 with key sr_seed and counter (g_lo, g_hi, copy,
- * sr_offset), g = (row * cols_of_copy + col) >> 3, copy 0 row-wise / 1
- * transposed, 16 bits per element.
+ * SR draws one Philox4x32-10 block per 16 consecutive elements of a copy
+ * row: key sr_seed, counter (g_lo, g_hi, copy, sr_offset),
+ * g = (row * cols_of_copy + col) >> 4, copy 0 row-wise / 1 transposed.
+ * Word (col & 15) >> 2 of the block serves four elements, 16 bits each:
+ * e0 = (w[23:16] << 8) | w[7:0], e1 = e0 bit-reversed, e2 = (w[31:24] << 8)
+ * | w[15:8], e3 = e2 bit-reversed; a scaled value rounds away from zero
+ * iff floor(65536 frac) + r >= 65536, frac its position in its E2M1 gap.
  * Outputs: q_row [rows][cols/2], sf_row, s_dec_row, shift_row (as in
  * fp4_quantize); q_col [cols][rows/2], sf_col, s_dec_col, shift_col.
  * Shapes: rows % B == 0, cols % B == 0, rows % hadamard_n == 0. */
@@ -239,7 +243,7 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M,
  * its row-wise copy is quantised exactly as fp4_quantize quantises a
  * binary32 input: tensor scale from the held amax *amax_dev and p->T, one
  * scale per p->format block along N, RNE or (p->round_row == SR) Philox
- * stochastic rounding with counter group (m N + n) >> 3 and copy 0,
+ * stochastic rounding with counter group (m N + n) >> 4 and copy 0,
  * zero-scale rule, scales in p->sf_layout; UE5M3 with the MMA layout and a
  * non-NULL row_shift is remapped onto E4M3 as in fp4_quantize.  Only the
  * row-wise copy is produced (block2d, hadamard_n and round_col must be 0).

@@ -56,6 +56,7 @@ def lib():
             "orc_scale_value": (ctypes.c_double, [i32, i32]),
             "orc_philox4x32_10": (None, [u32p, u32p, u32p]),
             "orc_e2m1_sr": (i32, [f32, u32]),
+            "orc_sr_r16": (u32, [u64, u32, u32, i64, i64, i64]),
             "orc_hadamard": (None, [f32p, i32, u32]),
             "orc_hadamard_rows": (None, [f32p, i64, i64, i32, u32]),
             "orc_tensor_scale": (None, [i32, f32, f32, f32p, f32p]),
@@ -107,6 +108,12 @@ def e2m1_rne(v):
 
 def e2m1_sr(v, r16):
     return lib().orc_e2m1_sr(float(v), int(r16))
+
+
+def sr_r16(seed, offset, copy_id, row, cols, col):
+    """The 16 random bits stochastic rounding uses for element (row, col)
+    of a copy with `cols` columns (see orc_sr_r16)."""
+    return lib().orc_sr_r16(int(seed), int(offset), int(copy_id), int(row), int(cols), int(col))
 
 
 def ue5m3_value(code):

@@ -162,33 +162,58 @@ void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
 
 /* Stochastic rounding of v to E2M1 with 16 random bits ([UE5M3] Approach:
  * SR on the upstream-gradient payload only).  Between the neighbouring code
- * magnitudes lo <= |v| < hi the value rounds up with probability
- * ceil(65536 * (|v|-lo)/(hi-lo)) / 65536.  |v| >= 6 saturates; the sign is
- * taken from v. */
+ * magnitudes lo <= |v| < hi, with f = (|v|-lo)/(hi-lo), the 16 random bits
+ * are added to the top 16 bits of the fraction being dropped and the sum is
+ * truncated: the value rounds up iff floor(65536 f) + r16 >= 65536, i.e.
+ * with probability floor(65536 f) / 65536 (low by less than 2^-16 of the
+ * gap).  |v| >= 6 saturates; the sign is taken from v.  (f * 65536 is exact
+ * in binary64: |v| has 24 significant bits and the gap is a power of two.) */
 int orc_e2m1_sr(float v, uint32_t r16) {
   int sign = signbit(v) ? 8 : 0;
   double a = fabs((double)v);
-  if (a >= 6.0) return sign | 7;
+  if (!(a < 6.0)) return sign | 7;
   int lo = 0;
   for (int c = 1; c < 8; ++c)
     if (e2m1_mag(c) <= a) lo = c;
   if (e2m1_mag(lo) == a) return sign | lo;
   double frac = (a - e2m1_mag(lo)) / (e2m1_mag(lo + 1) - e2m1_mag(lo));
-  int up = (double)r16 < frac * 65536.0;
+  uint32_t top16 = (uint32_t)floor(frac * 65536.0);
+  int up = top16 + (r16 & 0xFFFFu) >= 65536u;
   return sign | (lo + up);
 }
 
+static uint32_t bitrev16(uint32_t x) {
+  uint32_t r = 0;
+  for (int b = 0; b < 16; ++b)
+    if ((x >> b) & 1u) r |= 1u << (15 - b);
+  return r;
+}
+
 /* 16 random bits for element `col` of row `row` of a copy with `cols`
- * columns: one Philox call per 8 consecutive elements of the copy. */
-static uint32_t sr_bits(uint64_t seed, uint32_t offset, uint32_t copy_id,
-                        int64_t row, int64_t cols, int64_t col) {
-  uint64_t g = ((uint64_t)row * (uint64_t)cols + (uint64_t)col) >> 3;
+ * columns (cols a multiple of 16).  One Philox4x32-10 call per 16
+ * consecutive elements of the copy: counter (g_lo, g_hi, copy_id, offset)
+ * with g = (row * cols + col) >> 4, key (seed_lo, seed_hi).  Output word
+ * w = out[(col & 15) >> 2] serves four consecutive elements e0..e3
+ * (i = col & 3), 16 bits each:
+ *   e0: (w[23:16] << 8) | w[7:0]     e1: e0's 16 bits in reverse order
+ *   e2: (w[31:24] << 8) | w[15:8]    e3: e2's 16 bits in reverse order
+ * Every element's value is uniform on [0, 2^16). */
+uint32_t orc_sr_r16(uint64_t seed, uint32_t offset, uint32_t copy_id, int64_t row,
+                    int64_t cols, int64_t col) {
+  uint64_t g = ((uint64_t)row * (uint64_t)cols + (uint64_t)col) >> 4;
   uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), copy_id, offset};
   uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
   uint32_t out[4];
   orc_philox4x32_10(ctr, key, out);
-  int j = (int)(col & 7);
-  return (out[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+  uint32_t w = out[(col & 15) >> 2];
+  uint32_t even = (((w >> 16) & 0xFFu) << 8) | (w & 0xFFu);
+  uint32_t odd = ((w >> 24) << 8) | ((w >> 8) & 0xFFu);
+  switch ((int)(col & 3)) {
+    case 0: return even;
+    case 1: return bitrev16(even);
+    case 2: return odd;
+    default: return bitrev16(odd);
+  }
 }
 
 /* Fixed-sign Hadamard on n = 16 or 32 consecutive values ([MXH] Method and
@@ -340,8 +365,8 @@ void orc_quantize_rows(const float *x, int64_t R, int64_t C, int fmt,
         float v = scaled(xb[i], mult, zp);
         int e;
         if (sr)
-          e = orc_e2m1_sr(v, sr_bits(seed, offset, copy_id, row_base + r, C,
-                                     col));
+          e = orc_e2m1_sr(v, orc_sr_r16(seed, offset, copy_id, row_base + r, C,
+                                        col));
         else
           e = orc_e2m1_rne(v);
         put_nibble(q + r * (C / 2), col, e);

@@ -52,6 +52,9 @@ double orc_scale_value(int fmt, int code);
 void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
                        uint32_t out[4]);
 int orc_e2m1_sr(float v, uint32_t r16);
+/* 16 random bits of element (row, col) of a copy with `cols` columns. */
+uint32_t orc_sr_r16(uint64_t seed, uint32_t offset, uint32_t copy_id, int64_t row,
+                    int64_t cols, int64_t col);
 void orc_hadamard(float *x, int n, uint32_t signs);
 void orc_hadamard_rows(float *x, int64_t R, int64_t C, int n, uint32_t signs);
 

@@ -155,20 +155,16 @@ def test_philox_known_answers():
 # ------------------------------------------------------- stochastic rounding
 
 def test_sr_unbiased_and_neighbour_valued():
-    # 2^17 independent 16-bit draws per value from the Philox stream
+    # 2^17 16-bit draws per value: the per-element values the quantiser uses
+    # along the first 2^17 elements of one copy row
     n = 1 << 17
-    key = [42, 0]
-    draws = []
-    for g in range(n // 8):
-        o = orc.philox4x32_10([g, 0, 0, 0], key)
-        for j in range(8):
-            draws.append((int(o[j >> 1]) >> (16 * (j & 1))) & 0xFFFF)
-    draws = np.array(draws[:n], dtype=np.int64)
+    draws = np.array([orc.sr_r16(42, 0, 0, 0, n, c) for c in range(n)], dtype=np.int64)
+    assert abs(draws.mean() - 32767.5) < 4 * 18918.6 / math.sqrt(n)   # uniform on [0, 2^16)
     book = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
     for v in (0.1, 0.3, 0.77, 1.1, 1.6, 2.2, 2.9, 3.3, 4.5, 5.9, -0.6, -2.7, 0.0078125):
         lo = book[book <= abs(v)].max()
         hi = book[book > abs(v)].min()
-        # P(up) = ceil(65536 frac)/65536 with frac = (|v|-lo)/(hi-lo)
+        # P(up) = floor(65536 frac)/65536 with frac = (|v|-lo)/(hi-lo)
         frac = (abs(f32(v)) - lo) / (hi - lo)
         codes = np.array([orc.e2m1_sr(v, int(r)) for r in draws])
         dec = np.array([orc.e2m1_value(int(c)) for c in codes])
@@ -177,6 +173,48 @@ def test_sr_unbiased_and_neighbour_valued():
         sigma = (hi - lo) * math.sqrt(frac * (1 - frac) / n)
         assert abs(mean - abs(f32(v))) <= 4 * sigma + (hi - lo) * 2.0 ** -16, (v, mean)
     assert orc.e2m1_sr(6.5, 0) == 7 and orc.e2m1_sr(1.5, 0) == 3 and orc.e2m1_sr(1.5, 65535) == 3
+
+
+def test_sr_rule_adds_the_draw_to_the_dropped_fraction():
+    # frac = 1/2 (1.25 between 1 and 1.5): up iff 32768 + r >= 65536
+    assert orc.e2m1_sr(1.25, 32767) == 2 and orc.e2m1_sr(1.25, 32768) == 3
+    assert orc.e2m1_sr(-1.25, 32768) == 11 and orc.e2m1_sr(-1.25, 32767) == 10
+    # frac = 1/4 (2.25 between 2 and 3): up iff r >= 49152
+    assert orc.e2m1_sr(2.25, 49151) == 4 and orc.e2m1_sr(2.25, 49152) == 5
+    # frac = 3/4 in the gap 4..6 (5.5): up iff r >= 16384
+    assert orc.e2m1_sr(5.5, 16383) == 6 and orc.e2m1_sr(5.5, 16384) == 7
+    # below 0.5 (step 0.5): 0.125 has frac 1/4
+    assert orc.e2m1_sr(0.125, 49151) == 0 and orc.e2m1_sr(0.125, 49152) == 1
+    # a fraction below 2^-16 never rounds up; one just below 1 always does
+    # unless the draw is 0
+    tiny = 1.0 + 2.0 ** -20
+    assert all(orc.e2m1_sr(tiny, r) == 2 for r in (0, 1, 65534, 65535))
+    near = float(np.float32(1.5) - np.float32(2.0 ** -23))
+    assert orc.e2m1_sr(near, 0) == 2 and orc.e2m1_sr(near, 1) == 3
+    # exact codebook values and zeros never move; the sign of zero is kept
+    for c, m in enumerate([0, .5, 1, 1.5, 2, 3, 4, 6]):
+        assert orc.e2m1_sr(m, 65535) == c
+    assert orc.e2m1_sr(-0.0, 65535) == 8
+
+
+def _rev16(x):
+    return int(format(x, "016b")[::-1], 2)
+
+
+def test_sr_random_bits_come_from_one_philox_call_per_16_elements():
+    # element c of row r in a copy with C columns: group g = (r C + c) >> 4,
+    # word out[(c & 15) >> 2]; even lanes of a word take bytes 2 and 0, odd
+    # lanes bytes 3 and 1, and lanes 1 and 3 the bit reversals of 0 and 2
+    seed, offset, copy, C = 0x1234_5678_9ABC_DEF0, 7, 1, 96
+    for r, c in ((0, 0), (0, 5), (2, 17), (3, 95), (1, 42)):
+        g = (r * C + c) >> 4
+        out = orc.philox4x32_10([g & 0xFFFFFFFF, g >> 32, copy, offset],
+                                [seed & 0xFFFFFFFF, seed >> 32])
+        w = int(out[(c & 15) >> 2])
+        even = (((w >> 16) & 0xFF) << 8) | (w & 0xFF)
+        odd = ((w >> 24) << 8) | ((w >> 8) & 0xFF)
+        want = {0: even, 1: _rev16(even), 2: odd, 3: _rev16(odd)}[c & 3]
+        assert orc.sr_r16(seed, offset, copy, r, C, c) == want, (r, c)
 
 
 def test_sr_quantizer_deterministic_and_unbiased():
