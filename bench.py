@@ -191,9 +191,6 @@ class Layer:
         self.Y = torch.empty((M_TOK, N_MODEL), dtype=torch.bfloat16, device=device)
         self.dX = torch.empty((M_TOK, K_FF), dtype=torch.bfloat16, device=device)
         self.dW = torch.empty((N_MODEL, K_FF), dtype=torch.float32, device=device)
-        # amax (zeroing + one batched launch), producers x3, GEMMs x3, one
-        # remap per UE5M3 producer
-        self.launches_per_step = 2 + 3 + 3 + (3 if fmt in (0, 3) else 0)
 
     def refresh_amax(self):
         fq = self.fq
@@ -231,6 +228,95 @@ class Layer:
         mark("end")
 
 
+def measure_layer(layer, args, world, flush):
+    """Warm-up, one CUDA graph of the whole step, the timed steps (median,
+    L2 flushed before each) and a per-kernel breakdown of the same step
+    launched kernel by kernel between events on the launching stream."""
+    fq = layer.fq
+    names = ["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad", "end"]
+    for _ in range(args.warmup):
+        layer.step()
+    st = fq.fp4_status_sync()
+    if st != fq.FP4_OK:
+        raise RuntimeError("device status after warm-up: " + fq.STATUS_NAMES[st])
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.step()
+        graph.replay()
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = []
+    for _ in range(args.steps):
+        flush_l2(flush)
+        s_ev = torch.cuda.Event(enable_timing=True)
+        e_ev = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_ev.record()
+        if graph is not None:
+            graph.replay()
+        else:
+            layer.step()
+        e_ev.record()
+        torch.cuda.synchronize()
+        step_ms.append(s_ev.elapsed_time(e_ev))
+    barrier(world)
+    per_kernel = {n: [] for n in names[:-1]}
+    for _ in range(min(args.steps, 50)):
+        flush_l2(flush)
+        ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
+        torch.cuda.synchronize()
+        layer.step(ev)
+        torch.cuda.synchronize()
+        for a_, b_ in zip(names, names[1:]):
+            per_kernel[a_].append(ev[a_].elapsed_time(ev[b_]))
+    st = fq.fp4_status_sync()
+    if st != fq.FP4_OK:
+        raise RuntimeError("device status after timed steps: " + fq.STATUS_NAMES[st])
+    return {"step_ms": reduce_max(statistics.median(step_ms), world),
+            "kernel_ms": {k: statistics.median(v) for k, v in per_kernel.items()},
+            "graph": graph}
+
+
+def summarize_layer(fmt, m, pk, world):
+    """Step value, producer GB/s and GEMM TFLOP/s of one measured layer."""
+    amax_b, qbytes, gemms, flops = work_model(fmt)
+    hbm = pk["hbm_gbs"] * 1e9
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    ideal = amax_b / hbm + sum(qbytes.values()) / hbm + sum(flops.values()) / (fp4_peak * 1e12)
+    avg = m["kernel_ms"]
+    q_ms = avg["quant_X"] + avg["quant_W"] + avg["quant_dY"]
+    g_ms = avg["fprop"] + avg["dgrad"] + avg["wgrad"]
+    quant_gbs = sum(qbytes.values()) / (q_ms * 1e-3) / 1e9
+    gemm_tflops = sum(flops.values()) / (g_ms * 1e-3) / 1e12
+    per_producer = {}
+    for k in ("X", "W", "dY"):
+        ms = avg["quant_" + k]
+        gbs = qbytes[k] / (ms * 1e-3) / 1e9
+        per_producer[k] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                           "frac": round(gbs / pk["hbm_gbs"], 4)}
+    per_gemm = {}
+    for k in ("fprop", "dgrad", "wgrad"):
+        tf = flops[k] / (avg[k] * 1e-3) / 1e12
+        per_gemm[k] = {"ms": round(avg[k], 4), "tflops": round(tf, 1),
+                       "frac": round(tf / fp4_peak, 4)}
+    return {
+        "ideal_s": ideal,
+        "value": 100.0 * ideal / (m["step_ms"] * 1e-3) * world,
+        "quantize": {"gbs": round(quant_gbs, 1), "frac": round(quant_gbs / pk["hbm_gbs"], 4),
+                     "ms": round(q_ms, 4), "per_producer": per_producer,
+                     "note": "UE5M3 producers include the scale remap launch"
+                             if fmt in (0, 3) else "one launch per producer"},
+        "amax": {"gbs": round(amax_b / (avg["amax"] * 1e-3) / 1e9, 1),
+                 "ms": round(avg["amax"], 4)},
+        "gemm": {"tflops": round(gemm_tflops, 1), "frac": round(gemm_tflops / fp4_peak, 4),
+                 "ms": {k: round(avg[k], 4) for k in ("fprop", "dgrad", "wgrad")},
+                 "per_gemm": per_gemm},
+    }
+
+
 def run_gpu(args, world, rank, local):
     import fp4_block_scaled_quantize_gb300 as fq
     torch.cuda.set_device(local)
@@ -240,65 +326,13 @@ def run_gpu(args, world, rank, local):
     layer = Layer(args.format, seed=args.seed + rank, device=dev)
     amax_b, qbytes, gemms, flops = work_model(args.format)
     flush = torch.zeros(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device=dev)
-    names = ["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad", "end"]
 
-    for _ in range(args.warmup):
-        layer.step()
-    st = fq.fp4_status_sync()
-    if st != fq.FP4_OK:
-        raise RuntimeError("device status after warm-up: " + fq.STATUS_NAMES[st])
-    torch.cuda.synchronize()
-    # the whole step captured once as a CUDA graph and replayed
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            layer.step()
-        graph.replay()
-        torch.cuda.synchronize()
-    barrier(world)
-
-    step_ms = []
     with Clocks(local) as clk:
-        for _ in range(args.steps):
-            flush_l2(flush)
-            s_ev = torch.cuda.Event(enable_timing=True)
-            e_ev = torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            s_ev.record()
-            if graph is not None:
-                graph.replay()
-            else:
-                layer.step()
-            e_ev.record()
-            torch.cuda.synchronize()
-            step_ms.append(s_ev.elapsed_time(e_ev))
-    barrier(world)
-    # per-kernel breakdown: the same steps launched one kernel at a time,
-    # each bracketed by events on the launching stream; median per kernel
-    per_kernel = {n: [] for n in names[:-1]}
-    for _ in range(min(args.steps, 50)):
-        flush_l2(flush)
-        ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
-        torch.cuda.synchronize()
-        layer.step(ev)
-        torch.cuda.synchronize()
-        for a, b in zip(names, names[1:]):
-            per_kernel[a].append(ev[a].elapsed_time(ev[b]))
-    st = fq.fp4_status_sync()
-    if st != fq.FP4_OK:
-        raise RuntimeError("device status after timed steps: " + fq.STATUS_NAMES[st])
-    ms_step = reduce_max(statistics.median(step_ms), world)
-
-    # roofline-ideal time of one step (seconds)
-    hbm = pk["hbm_gbs"] * 1e9
-    ideal = amax_b / hbm + sum(qbytes.values()) / hbm + sum(flops.values()) / (fp4_peak * 1e12)
-    value = 100.0 * ideal / (ms_step * 1e-3) * world
-    avg = {k: statistics.median(v) for k, v in per_kernel.items()}
-    q_ms = avg["quant_X"] + avg["quant_W"] + avg["quant_dY"]
-    g_ms = avg["fprop"] + avg["dgrad"] + avg["wgrad"]
-    quant_gbs = sum(qbytes.values()) / (q_ms * 1e-3) / 1e9
-    gemm_tflops = sum(flops.values()) / (g_ms * 1e-3) / 1e12
+        m = measure_layer(layer, args, world, flush)
+    graph = m["graph"]
+    ms_step = m["step_ms"]
+    summ = summarize_layer(args.format, m, pk, world)
+    ideal, value, avg = summ["ideal_s"], summ["value"], m["kernel_ms"]
     dominant = max(("fprop", "dgrad", "wgrad"), key=lambda k: avg[k])
     dom_tflops = flops[dominant] / (avg[dominant] * 1e-3) / 1e12
     traffic = load_traffic(dominant)
@@ -308,6 +342,14 @@ def run_gpu(args, world, rank, local):
     reencode = run_reencode(layer, flush, pk["hbm_gbs"])
     linear = run_linear(layer, flush)
     e2e = run_e2e(layer, args, world, ideal, graph)
+    out_dtypes = run_out_dtypes(layer, flush, flops, fp4_peak)
+    host = layer.host
+    graphed = graph is not None
+    del layer, graph, m
+    torch.cuda.empty_cache()
+    per_format = run_per_format(args, world, host, dev, flush, pk)
+    del host
+    configs = run_configs(dev, flush, pk)
 
     clocks = clk.summary()
     out = {
@@ -323,14 +365,11 @@ def run_gpu(args, world, rank, local):
                    "amax": "current (D=1 refresh step)",
                    "l2": "flushed before each step (read of a clean 258 MB buffer)",
                    "timing": "median of the timed steps",
-                   "launch": "CUDA graph of the whole step" if graph is not None else "eager",
+                   "launch": "CUDA graph of the whole step" if graphed else "eager",
                    "parallelism": f"replicas x{world}"},
-        "quantize": {"gbs": round(quant_gbs, 1), "frac": round(quant_gbs / pk["hbm_gbs"], 4),
-                     "ms": round(q_ms, 4)},
-        "amax": {"gbs": round(amax_b / (avg["amax"] * 1e-3) / 1e9, 1),
-                 "ms": round(avg["amax"], 4)},
-        "gemm": {"tflops": round(gemm_tflops, 1), "frac": round(gemm_tflops / fp4_peak, 4),
-                 "ms": {k: round(avg[k], 4) for k in ("fprop", "dgrad", "wgrad")}},
+        "quantize": summ["quantize"],
+        "amax": summ["amax"],
+        "gemm": summ["gemm"],
         "roofline": {"kernel": "k_gemm (" + dominant + ")", "bound": "tensor",
                      "achieved": round(dom_tflops, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(dom_tflops / fp4_peak, 4),
@@ -338,8 +377,11 @@ def run_gpu(args, world, rank, local):
                      "peak_source": f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal "
                                     "FP4/BF16 dense ratio)"},
         "clocks": clocks,
-        "gpu_launches": layer.launches_per_step * args.steps,
+        "gpu_launches": layer_launches(args.format) * args.steps,
         "e2e": e2e,
+        "gemm_out_dtypes": out_dtypes,
+        "per_format": per_format,
+        "configs": configs,
         "epilogue_fused_producer": fused,
         "mxfp4_to_fp8": reencode,
         "linear_layer": linear,
@@ -347,6 +389,319 @@ def run_gpu(args, world, rank, local):
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(args, ideal)
         print(json.dumps(out))
+
+
+def layer_launches(fmt):
+    """Kernel launches of one step: amax (zeroing + one batched launch),
+    producers x3, GEMMs x3, one remap per UE5M3 producer."""
+    return 2 + 3 + 3 + (3 if fmt in (0, 3) else 0)
+
+
+def median_ms(fn, flush, reps=20):
+    """Median device time of fn() over `reps` runs, each after an L2 flush:
+    fn is captured once as a CUDA graph, and events on the launching stream
+    bracket each replay."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(reps):
+        flush_l2(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_out_dtypes(layer, flush, flops, fp4_peak):
+    """The three GEMMs of the step with the other output type: fprop and dgrad
+    to binary32, wgrad to BF16 (the step itself writes BF16, BF16, binary32)."""
+    fq = layer.fq
+    dev = layer.X.device
+    y32 = torch.empty((M_TOK, N_MODEL), dtype=torch.float32, device=dev)
+    dx32 = torch.empty((M_TOK, K_FF), dtype=torch.float32, device=dev)
+    dw16 = torch.empty((N_MODEL, K_FF), dtype=torch.bfloat16, device=dev)
+    runs = {"fprop_f32": ("fprop", lambda: fq.gemm(layer.xr, layer.wr, out=y32)),
+            "dgrad_f32": ("dgrad", lambda: fq.gemm(layer.dyr, layer.wc, out=dx32)),
+            "wgrad_bf16": ("wgrad", lambda: fq.gemm(layer.dyc, layer.xc, out=dw16))}
+    out = {}
+    for key, (g, fn) in runs.items():
+        ms = median_ms(fn, flush)
+        tf = flops[g] / (ms * 1e-3) / 1e12
+        out[key] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / fp4_peak, 4)}
+    fq._check(fq.fp4_status_sync(), "out dtypes")
+    return out
+
+
+def run_per_format(args, world, host, dev, flush, pk):
+    """The same step under the comparison formats (NVFP4-b16, MXFP4-b32) and
+    the UE5M3-b32 control, measured exactly as the headline format."""
+    out = {}
+    for fmt in (0, 1, 2, 3):
+        if fmt == args.format:
+            continue
+        layer = Layer(fmt, seed=0, device=dev, host=host)
+        m = measure_layer(layer, args, world, flush)
+        summ = summarize_layer(fmt, m, pk, world)
+        out[FMT_NAMES[fmt]] = {"value": round(summ["value"], 3), "unit": UNIT,
+                               "ms_per_step": round(m["step_ms"], 4),
+                               "quantize": summ["quantize"], "amax": summ["amax"],
+                               "gemm": summ["gemm"]}
+        del layer, m
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------ other configs
+
+SWEEP_SIZES = (2048, 4096, 8192, 16384)
+HAD32_SIGNS = 0x5A5AF00F  # fixed sign vector of the 32-point rotation
+
+
+def _qt(fq, x, a_r, a_c, p, r, c):
+    fq._check(fq.fp4_quantize_transpose(x, a_r, a_c, p, r.q, r.sf, r.s_dec, r.row_shift,
+                                        c.q, c.sf, c.s_dec, c.row_shift), "quantize_transpose")
+
+
+def _q(fq, x, a, p, r):
+    fq._check(fq.fp4_quantize(x, a, p, r.q, r.sf, r.s_dec, r.row_shift), "quantize")
+
+
+def producer_bytes(fmt, elems, copies):
+    """Algorithmic bytes of a producer: 2 B read per element, per copy 0.5 B
+    of payload and 1/B of scale bytes, 4 B of s_dec."""
+    B = 32 if fmt in (2, 3) else 16
+    return elems * (2.0 + copies * (0.5 + 1.0 / B)) + 4 * copies
+
+
+def _rate(nbytes=None, flop=None, ms=None, pk=None):
+    if flop is not None:
+        tf = flop / (ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"] * FP4_OVER_BF16
+        return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+
+
+def config_tiny(fq, dev, flush):
+    """Tiny UE5M3-b16 layer (X, W 256 x 256, seed 0): fresh amax of both, the
+    X producer (row + transposed), the 2D W producer (row + transposed) and
+    Y = X W^T.  Launch-bound: latency only."""
+    from fp4_block_scaled_quantize_gb300 import inputs
+    d = inputs.tiny(seed=0)
+    X, W = d["X"].to(dev), d["W"].to(dev)
+    mma = fq.FP4_SF_MMA
+    px = fq.params(format=0, T=448.0, sf_layout=mma)
+    pw = fq.params(format=0, T=448.0, block2d=True, sf_layout=mma)
+    ax = torch.zeros(1, dtype=torch.float32, device=dev)
+    aw = torch.zeros(1, dtype=torch.float32, device=dev)
+    fq._check(fq.fp4_amax_many([X, W], [ax, aw]), "amax")
+    xr, xc = fq.quantize_transpose(X, ax, ax, px)
+    wr, wc = fq.quantize_transpose(W, aw, aw, pw)
+    Y = torch.empty((256, 256), dtype=torch.float32, device=dev)
+
+    def step():
+        fq._check(fq.fp4_amax_many([X, W], [ax, aw]), "amax")
+        _qt(fq, X, ax, ax, px, xr, xc)
+        _qt(fq, W, aw, aw, pw, wr, wc)
+        fq.gemm(xr, wr, out=Y)
+
+    dev_ms = median_ms(step, flush, reps=50)
+    step()
+    torch.cuda.synchronize()
+    host = []
+    for _ in range(50):
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        host.append(time.perf_counter() - t0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    replay = []
+    for _ in range(50):
+        t0 = time.perf_counter()
+        g.replay()
+        torch.cuda.synchronize()
+        replay.append(time.perf_counter() - t0)
+    fq._check(fq.fp4_status_sync(), "tiny")
+    return {"shape": "X [256, 256], W [256, 256], Y = X W^T (binary32)", "format": "UE5M3-b16",
+            "launches": 2 + 2 + 2 + 1,
+            "device_us": round(dev_ms * 1e3, 2),
+            "host_eager_us": round(statistics.median(host) * 1e6, 1),
+            "host_graph_replay_us": round(statistics.median(replay) * 1e6, 1),
+            "note": "launch-bound; latency only, no roofline claim"}
+
+
+def config_forward(fq, dev, flush, pk):
+    """Forward layer: X [8192, 4096] N(0,1) with 1% of channels scaled by
+    LogNormal(0,1), W [4096, 4096] N(0, 0.02) with 2D tiles; row-wise
+    producers, fprop M=8192 N=4096 K=4096, UE5M3-b16 and NVFP4-b16, RNE."""
+    from fp4_block_scaled_quantize_gb300 import inputs
+    d = inputs.forward_layer(seed=0)
+    X, W = d["X"].to(dev), d["W"].to(dev)
+    M, K, N = X.shape[0], X.shape[1], W.shape[0]
+    out = {"shapes": {"X": [M, K], "W": [N, K]}}
+    ax, aw = fq.amax_many([X, W])
+    Y16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Y32 = torch.empty((M, N), dtype=torch.float32, device=dev)
+    for fmt in (0, 1):
+        mma = fq.FP4_SF_MMA
+        px = fq.params(format=fmt, T=448.0, sf_layout=mma)
+        pw = fq.params(format=fmt, T=448.0, block2d=True, sf_layout=mma)
+        xr, wr = fq.quantize(X, ax, px), fq.quantize(W, aw, pw)
+        flop = 2.0 * M * N * K
+        out[FMT_NAMES[fmt]] = {
+            "quant_X_row": _rate(producer_bytes(fmt, M * K, 1),
+                                 ms=median_ms(lambda: _q(fq, X, ax, px, xr), flush), pk=pk),
+            "quant_W_2d_row": _rate(producer_bytes(fmt, N * K, 1),
+                                    ms=median_ms(lambda: _q(fq, W, aw, pw, wr), flush), pk=pk),
+            "fprop_bf16": _rate(flop=flop, ms=median_ms(lambda: fq.gemm(xr, wr, out=Y16), flush),
+                                pk=pk),
+            "fprop_f32": _rate(flop=flop, ms=median_ms(lambda: fq.gemm(xr, wr, out=Y32), flush),
+                               pk=pk),
+        }
+        del xr, wr
+    out["amax_ms"] = round(median_ms(lambda: fq.amax_many([X, W]), flush), 4)
+    fq._check(fq.fp4_status_sync(), "forward config")
+    return out
+
+
+def config_backward_sr(fq, dev, flush, pk):
+    """Backward with SR: dY [8192, 4096] Student-t(3) * 1e-4 quantised with a
+    stale held amax (half the true one), UE5M3-b16 T=2048, Philox SR seed 42
+    on both copies; X [8192, 4096] (N(0,1), 0.1% x50) row + transposed, RNE,
+    T=448, fresh amax; W [4096, 4096] 2D; dgrad dX = dY W, wgrad dW = dY^T X."""
+    from fp4_block_scaled_quantize_gb300 import inputs
+    d = inputs.backward_sr(seed=0)
+    dY, X, W = d["dY"].to(dev), d["X"].to(dev), d["W"].to(dev)
+    M, N = dY.shape
+    K_in = X.shape[1]
+    mma = fq.FP4_SF_MMA
+    ady, ax, aw = fq.amax_many([dY, X, W])
+    ady_held = ady * 0.5
+    pdy = fq.params(format=0, T=2048.0, round_row=fq.FP4_ROUND_SR, round_col=fq.FP4_ROUND_SR,
+                    sr_seed=42, sf_layout=mma)
+    px = fq.params(format=0, T=448.0, sf_layout=mma)
+    pw = fq.params(format=0, T=448.0, block2d=True, sf_layout=mma)
+    dyr, dyc = fq.quantize_transpose(dY, ady_held, ady_held, pdy)
+    xr, xc = fq.quantize_transpose(X, ax, ax, px)
+    wr, wc = fq.quantize_transpose(W, aw, aw, pw)
+    dX16 = torch.empty((M, K_in), dtype=torch.bfloat16, device=dev)
+    dX32 = torch.empty((M, K_in), dtype=torch.float32, device=dev)
+    dW32 = torch.empty((N, K_in), dtype=torch.float32, device=dev)
+    dW16 = torch.empty((N, K_in), dtype=torch.bfloat16, device=dev)
+    f_dgrad = 2.0 * M * K_in * N
+    f_wgrad = 2.0 * N * K_in * M
+    out = {"shapes": {"dY": [M, N], "X": [M, K_in], "W": [N, K_in]},
+           "dgrad": [M, K_in, N], "wgrad": [N, K_in, M],
+           "quant_dY_sr_row_col": _rate(producer_bytes(0, M * N, 2), ms=median_ms(
+               lambda: _qt(fq, dY, ady_held, ady_held, pdy, dyr, dyc), flush), pk=pk),
+           "quant_X_row_col": _rate(producer_bytes(0, M * K_in, 2), ms=median_ms(
+               lambda: _qt(fq, X, ax, ax, px, xr, xc), flush), pk=pk),
+           "quant_W_2d_row_col": _rate(producer_bytes(0, N * K_in, 2), ms=median_ms(
+               lambda: _qt(fq, W, aw, aw, pw, wr, wc), flush), pk=pk),
+           "dgrad_bf16": _rate(flop=f_dgrad, ms=median_ms(lambda: fq.gemm(dyr, wc, out=dX16),
+                                                          flush), pk=pk),
+           "dgrad_f32": _rate(flop=f_dgrad, ms=median_ms(lambda: fq.gemm(dyr, wc, out=dX32),
+                                                         flush), pk=pk),
+           "wgrad_f32": _rate(flop=f_wgrad, ms=median_ms(lambda: fq.gemm(dyc, xc, out=dW32),
+                                                         flush), pk=pk),
+           "wgrad_bf16": _rate(flop=f_wgrad, ms=median_ms(lambda: fq.gemm(dyc, xc, out=dW16),
+                                                          flush), pk=pk),
+           "format": "UE5M3-b16 (dY T=2048 SR, X and W T=448 RNE)"}
+    fq._check(fq.fp4_status_sync(), "backward config")
+    return out
+
+
+def config_sweep(fq, dev, flush, pk):
+    """GEMM sweep: (M, N, K) in {2048, 4096, 8192, 16384}^3 plus
+    (8192, 14336, 4096) and (14336, 8192, 4096); A [M, K] and B [N, K] are
+    N(0,1) with 1% of entries x50 (seeds 7 and 8, drawn on the device),
+    quantised row-wise to UE5M3-b16; BF16 output.  Then the three producer
+    variants on a [8192, 8192] operand pair: MXFP4-b32 with the fixed-sign
+    32-point rotation on the transposed (wgrad) copies, UE5M3-b16 with H16,
+    UE5M3-b16 without rotation, each with its wgrad GEMM on those copies."""
+    from fp4_block_scaled_quantize_gb300 import inputs
+    mma = fq.FP4_SF_MMA
+    p = fq.params(format=0, T=448.0, sf_layout=mma)
+    cache = {}
+
+    def operand(role, rows, k):
+        key = (role, rows, k)
+        if key not in cache:
+            x = inputs.sweep_operand(rows, k, seed=7 if role == "A" else 8, device=dev)
+            (a,) = fq.amax_many([x])
+            cache[key] = fq.quantize(x, a, p)
+            del x
+        return cache[key]
+
+    shapes = [(m, n, k) for m in SWEEP_SIZES for n in SWEEP_SIZES for k in SWEEP_SIZES]
+    shapes += [(8192, 14336, 4096), (14336, 8192, 4096)]
+    tflops = {}
+    fracs = []
+    for m, n, k in shapes:
+        A, B = operand("A", m, k), operand("B", n, k)
+        D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms = median_ms(lambda: fq.gemm(A, B, out=D), flush, reps=10)
+        r = _rate(flop=2.0 * m * n * k, ms=ms, pk=pk)
+        tflops[f"{m}x{n}x{k}"] = r["tflops"]
+        fracs.append(r["frac"])
+        del D
+    fq._check(fq.fp4_status_sync(), "sweep")
+    cache.clear()
+    torch.cuda.empty_cache()
+    variants = {}
+    R = 8192
+    xa = inputs.sweep_operand(R, R, seed=7, device=dev)
+    xb = inputs.sweep_operand(R, R, seed=8, device=dev)
+    for name, fmt, had, signs in (("MXFP4-b32 + H32", 2, 32, HAD32_SIGNS),
+                                  ("UE5M3-b16 + H16", 0, 16, 0),
+                                  ("UE5M3-b16", 0, 0, 0)):
+        pv = fq.params(format=fmt, T=448.0, hadamard_n=had, hadamard_signs=signs, sf_layout=mma)
+        copies = []
+        for x in (xa, xb):
+            ar, ac = fq.amax(x, had, signs)
+            r_, c_ = fq.quantize_transpose(x, ar, ac, pv)
+            copies.append((x, ar, ac, r_, c_))
+        x, ar, ac, r_, c_ = copies[0]
+        amax_ms = median_ms(lambda: fq.amax(x, had, signs), flush)
+        q_ms = median_ms(lambda: _qt(fq, x, ar, ac, pv, r_, c_), flush)
+        D = torch.empty((R, R), dtype=torch.float32, device=dev)
+        ca, cb = copies[0][4], copies[1][4]
+        g_ms = median_ms(lambda: fq.gemm(ca, cb, out=D), flush)
+        variants[name] = {"amax_view": _rate(2.0 * R * R, ms=amax_ms, pk=pk),
+                          "producer_row_col": _rate(producer_bytes(fmt, R * R, 2), ms=q_ms, pk=pk),
+                          "wgrad_gemm_f32": _rate(flop=2.0 * R ** 3, ms=g_ms, pk=pk)}
+        del copies, D
+    fq._check(fq.fp4_status_sync(), "sweep variants")
+    fs = sorted(fracs)
+    return {"format": "UE5M3-b16", "out": "bf16", "shapes": len(shapes),
+            "inputs": "N(0,1), 1% of entries x50, drawn on the device (seeds 7, 8)",
+            "tflops": tflops,
+            "frac": {"min": fs[0], "median": fs[len(fs) // 2], "max": fs[-1]},
+            "producer_variants": {"shape": [R, R], "variants": variants}}
+
+
+def run_configs(dev, flush, pk):
+    import fp4_block_scaled_quantize_gb300 as fq
+    out = {"tiny_256": config_tiny(fq, dev, flush)}
+    torch.cuda.empty_cache()
+    out["forward_8192x4096"] = config_forward(fq, dev, flush, pk)
+    torch.cuda.empty_cache()
+    out["backward_sr_8192x4096"] = config_backward_sr(fq, dev, flush, pk)
+    torch.cuda.empty_cache()
+    out["sweep"] = config_sweep(fq, dev, flush, pk)
+    torch.cuda.empty_cache()
+    return out
 
 
 def graph_ms(fn, flush, reps=20):
@@ -581,7 +936,7 @@ def load_traffic(kernel):
 
 # ------------------------------------------------------------ CPU oracle arm
 
-def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
+def oracle_step_seconds(args, sample_rows=64, sample_outputs=24, threads=None):
     """Time the oracle on a bounded sample of one step and extrapolate.
     Returns (seconds per full step, threads used, description)."""
     import numpy as np
@@ -591,7 +946,7 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
     fmt = {0: orc.UE5M3, 1: orc.NVFP4, 2: orc.MXFP4, 3: orc.UE5M3_B32}[args.format]
     R = sample_rows
     g = inputs.down_proj_8b(seed=args.seed, M=R * 2, K=K_FF, N=N_MODEL)
-    threads = os.cpu_count() or 1
+    threads = threads or min(16, os.cpu_count() or 1)
     t_quant = 0.0
     elems_done = 0
     for name, x in (("X", g["X"][:R]), ("W", g["W"][:R]), ("dY", g["dY"][:R])):
@@ -599,7 +954,7 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
         t0 = time.perf_counter()
         a = orc.amax(x32)
         orc.quantize_transpose(x32, a, a, fmt, block2d=(name == "W"), sr_row=(name == "dY"),
-                               sr_col=(name == "dY"), seed=42)
+                               sr_col=(name == "dY"), seed=42, threads=threads)
         t_quant += time.perf_counter() - t0
         elems_done += x32.size
     total_elems = M_TOK * K_FF + N_MODEL * K_FF + M_TOK * N_MODEL
@@ -614,7 +969,8 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
         mi = np.arange(sample_outputs) % 4
         ni = (np.arange(sample_outputs) // 4) % 4
         t0 = time.perf_counter()
-        orc.gemm_model(a["q"], a["sf"], b["q"], b["sf"], fmt, K, a["s_dec"], b["s_dec"], mi, ni)
+        orc.gemm_model(a["q"], a["sf"], b["q"], b["sf"], fmt, K, a["s_dec"], b["s_dec"], mi, ni,
+                       threads=threads)
         dt = time.perf_counter() - t0
         gemm_s += dt / sample_outputs * M * N
         gemm_desc.append(f"{name} {sample_outputs} outputs")
@@ -624,9 +980,15 @@ def oracle_step_seconds(args, sample_rows=64, sample_outputs=24):
 
 
 def cpu_baseline(args, ideal):
-    secs, threads, desc = oracle_step_seconds(args)
+    """The oracle on all host cores (up to 16 threads) and on one thread."""
+    secs, threads, desc = oracle_step_seconds(args, sample_rows=256, sample_outputs=128)
+    secs1, _, _ = oracle_step_seconds(args, sample_rows=32, sample_outputs=16, threads=1)
     return {"value": 100.0 * ideal / secs, "unit": UNIT, "cores": threads,
-            "kind": "oracle", "sample": desc, "seconds_per_step_extrapolated": round(secs, 1)}
+            "kind": "oracle", "sample": desc, "seconds_per_step_extrapolated": round(secs, 1),
+            "host_cpus": os.cpu_count(),
+            "single_thread": {"value": 100.0 * ideal / secs1, "cores": 1,
+                              "seconds_per_step_extrapolated": round(secs1, 1),
+                              "sample": "32 rows of each producer, 16 outputs per GEMM"}}
 
 
 def run_reference(args, world, rank):

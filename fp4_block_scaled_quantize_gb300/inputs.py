@@ -17,25 +17,27 @@ with the same distributions):
 * ``sweep_operand``   N(0,1) with 1% of entries x50.
 
 Draw order within a workload is fixed as listed; outlier positions come from
-``randperm`` on the same generator.
+``randperm`` on the same generator.  ``sweep_operand`` can also draw on a CUDA
+device (its own seeded generator there): the same distribution, other values,
+for timing runs whose operands are too large to draw on the host quickly.
 """
 import torch
 
 
-def _gen(seed):
-    g = torch.Generator(device="cpu")
+def _gen(seed, device="cpu"):
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
 
 
 def _normal(shape, std, g):
-    return torch.randn(shape, generator=g, dtype=torch.float32) * std
+    return torch.randn(shape, generator=g, dtype=torch.float32, device=g.device) * std
 
 
 def _scale_entries(x, frac, factor, g):
     n = int(round(frac * x.numel()))
     if n:
-        idx = torch.randperm(x.numel(), generator=g)[:n]
+        idx = torch.randperm(x.numel(), generator=g, device=g.device)[:n]
         x.view(-1)[idx] *= factor
     return x
 
@@ -93,8 +95,8 @@ def down_proj_8b(seed=0, M=8192, K=14336, N=4096):
     return dict(X=bf16(x), W=bf16(w), dY=bf16(dy))
 
 
-def sweep_operand(rows, cols, seed=7):
-    g = _gen(seed)
+def sweep_operand(rows, cols, seed=7, device="cpu"):
+    g = _gen(seed, device)
     return bf16(_scale_entries(_normal((rows, cols), 1.0, g), 0.01, 50.0, g))
 
 

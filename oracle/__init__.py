@@ -253,7 +253,8 @@ def quantize(x, amax_held, fmt, T=448.0, block2d=False, sr=False, seed=0, offset
 
 
 def quantize_transpose(x, amax_row, amax_col, fmt, T=448.0, block2d=False, sr_row=False,
-                       sr_col=False, seed=0, offset=0, hadamard_n=0, signs=0, T_col=None):
+                       sr_col=False, seed=0, offset=0, hadamard_n=0, signs=0, T_col=None,
+                       threads=None):
     """Row-wise copy and transposed copy (what fp4_quantize_transpose emits).
     The transposed copy quantises x^T (rotated by the fixed-sign Hadamard along
     its rows when hadamard_n is 16 or 32) with its own held amax and its own
@@ -264,13 +265,13 @@ def quantize_transpose(x, amax_row, amax_col, fmt, T=448.0, block2d=False, sr_ro
         q_r, sf_r, q_c, sf_c = quantize_2d(x, fmt, s_enc_r, s_dec_r)
         return (dict(q=q_r, sf=sf_r, s_dec=s_dec_r), dict(q=q_c, sf=sf_c, s_dec=s_dec_r))
     q_r, sf_r = quantize_rows(x, fmt, s_enc_r, s_dec_r, sr=sr_row, seed=seed, offset=offset,
-                              copy_id=0)
+                              copy_id=0, threads=threads)
     xt = np.ascontiguousarray(np.asarray(x, dtype=np.float32).T)
     if hadamard_n:
         xt = hadamard_rows(xt, hadamard_n, signs)
     s_enc_c, s_dec_c = tensor_scale(fmt, T if T_col is None else T_col, amax_col)
     q_c, sf_c = quantize_rows(xt, fmt, s_enc_c, s_dec_c, sr=sr_col, seed=seed, offset=offset,
-                              copy_id=1)
+                              copy_id=1, threads=threads)
     return dict(q=q_r, sf=sf_r, s_dec=s_dec_r), dict(q=q_c, sf=sf_c, s_dec=s_dec_c)
 
 
