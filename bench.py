@@ -42,6 +42,7 @@ FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32", 3: "UE5M3-b32"}
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor ratio on GB300
 UNIT = "% of one GB300 roofline (step ideal time / step time, summed over GPUs)"
 L2_FLUSH_BYTES = 2 * 129 * 1000 * 1000  # twice the L2
+SLEEP_CYCLES = 100_000  # ~50 us of device-side wait before a timed region
 
 
 def flush_l2(buf):
@@ -254,6 +255,9 @@ def measure_layer(layer, args, world, flush):
         s_ev = torch.cuda.Event(enable_timing=True)
         e_ev = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        # a short device-side wait lets the host enqueue the step before the
+        # start event fires, so host launch latency stays out of the step
+        torch.cuda._sleep(SLEEP_CYCLES)
         s_ev.record()
         if graph is not None:
             graph.replay()
@@ -268,6 +272,7 @@ def measure_layer(layer, args, world, flush):
         flush_l2(flush)
         ev = {n: torch.cuda.Event(enable_timing=True) for n in names}
         torch.cuda.synchronize()
+        torch.cuda._sleep(4 * SLEEP_CYCLES)
         layer.step(ev)
         torch.cuda.synchronize()
         for a_, b_ in zip(names, names[1:]):
@@ -348,6 +353,8 @@ def run_gpu(args, world, rank, local):
     del layer, graph, m
     torch.cuda.empty_cache()
     per_format = run_per_format(args, world, host, dev, flush, pk)
+    fp8_vs_fp4 = run_fp8_vs_fp4(host, dev, flush, pk,
+                                dict(per_format, **{FMT_NAMES[args.format]: summ}))
     del host
     configs = run_configs(dev, flush, pk)
 
@@ -381,6 +388,7 @@ def run_gpu(args, world, rank, local):
         "e2e": e2e,
         "gemm_out_dtypes": out_dtypes,
         "per_format": per_format,
+        "fp8_vs_fp4": fp8_vs_fp4,
         "configs": configs,
         "epilogue_fused_producer": fused,
         "mxfp4_to_fp8": reencode,
@@ -457,6 +465,55 @@ def run_per_format(args, world, host, dev, flush, pk):
                                "gemm": summ["gemm"]}
         del layer, m
         torch.cuda.empty_cache()
+    return out
+
+
+def run_fp8_vs_fp4(host, dev, flush, pk, per_format):
+    """The step's three GEMMs in FP8 on the re-encoded MXFP4 copies
+    (fp4_mxfp4_to_fp8 for row-wise operands, fp4_mxfp4_to_fp8_transpose for
+    the transposed ones) against the same GEMMs in FP4 (MXFP4-b32 and
+    UE5M3-b16, from the step measurements).  FP8 peak: the measured BF16
+    burst x 2 (nominal FP8 / BF16 dense ratio)."""
+    import fp4_block_scaled_quantize_gb300 as fq
+    X, W, dY = (host[k].to(dev) for k in ("X", "W", "dY"))
+    p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
+    fp8 = {}
+    for name, x in (("X", X), ("W", W), ("dY", dY)):
+        (a,) = fq.amax_many([x])
+        c = fq.quantize(x, a, p)
+        sf = c.sf.view(x.shape[0], x.shape[1] // 32)
+        fp8[name] = fq.mxfp4_to_fp8(c.q, sf)
+        fp8[name + "t"] = fq.mxfp4_to_fp8_transpose(c.q, sf)
+        del c, sf
+    del X, W, dY
+    torch.cuda.empty_cache()
+    gemms = {"fprop": ("X", "W", torch.bfloat16), "dgrad": ("dY", "Wt", torch.bfloat16),
+             "wgrad": ("dYt", "Xt", torch.float32)}
+    fp8_peak = pk["bf16_tflops"] * 2.0
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    out = {"operands": "MXFP4-b32 copies of the step's X, W, dY re-encoded to E4M3-b128",
+           "fp8_peak_tflops": round(fp8_peak, 1),
+           "fp8_peak_source": f"{pk['source']} bf16 burst x 2 (nominal FP8/BF16 dense ratio)"}
+    for g, (a, b, dt) in gemms.items():
+        qa, sa = fp8[a]
+        qb, sb = fp8[b]
+        D = torch.empty((qa.shape[0], qb.shape[0]), dtype=dt, device=dev)
+        ms = median_ms(lambda: fq.fp8_gemm(qa, sa, qb, sb, out=D), flush)
+        flop = 2.0 * qa.shape[0] * qb.shape[0] * qa.shape[1]
+        tf = flop / (ms * 1e-3) / 1e12
+        row = {"shape": [qa.shape[0], qb.shape[0], qa.shape[1]], "fp8_ms": round(ms, 4),
+               "fp8_tflops": round(tf, 1), "fp8_frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        for fmt_name in ("MXFP4-b32", "UE5M3-b16"):
+            pf = per_format.get(fmt_name)
+            if pf is not None:
+                g4 = pf["gemm"]["per_gemm"][g]
+                row[fmt_name + "_ms"] = g4["ms"]
+                row[fmt_name + "_tflops"] = g4["tflops"]
+        out[g] = row
+        del D
+    fq._check(fq.fp4_status_sync(), "fp8 gemm")
+    out["note"] = "FP4 figures are the step's GEMMs (frac of FP4 peak " + \
+                  f"{round(fp4_peak, 1)} TFLOP/s in per_format)"
     return out
 
 
@@ -1043,6 +1100,19 @@ def run_profile(args, local):
         "dgrad": lambda: fq.gemm(layer.dyr, layer.wc, out=layer.dX),
         "wgrad": lambda: fq.gemm(layer.dyc, layer.xc, out=layer.dW),
     }
+    if args.profile.startswith("fp8_"):
+        # the step's operands as FP8 copies (MXFP4-b32 re-encoded), one GEMM
+        p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
+        f8 = {}
+        for name, x in (("X", layer.X), ("W", layer.W), ("dY", layer.dY)):
+            c = fq.quantize(x, layer.amax[name][0], p)
+            sf = c.sf.view(x.shape[0], x.shape[1] // 32)
+            f8[name] = fq.mxfp4_to_fp8(c.q, sf)
+            f8[name + "t"] = fq.mxfp4_to_fp8_transpose(c.q, sf)
+        a, b, dt = {"fp8_fprop": ("X", "W", torch.bfloat16), "fp8_dgrad": ("dY", "Wt", torch.bfloat16),
+                    "fp8_wgrad": ("dYt", "Xt", torch.float32)}[args.profile]
+        D = torch.empty((f8[a][0].shape[0], f8[b][0].shape[0]), dtype=dt, device=layer.X.device)
+        ops[args.profile] = lambda: fq.fp8_gemm(*f8[a], *f8[b], out=D)
     if args.profile in ("reencode", "reencode_t"):
         p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
         mx = fq.quantize(layer.X, layer.amax["X"][0], p)
@@ -1074,7 +1144,7 @@ def main():
                     help="launch the timed steps kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", default=None,
                     choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad",
-                             "reencode", "reencode_t"],
+                             "reencode", "reencode_t", "fp8_fprop", "fp8_dgrad", "fp8_wgrad"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

@@ -61,7 +61,8 @@ class FP4Error(RuntimeError):
 _lib = None
 EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
            "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
-           "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync", "fp4_status_string")
+           "fp4_fp8_gemm", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
+           "fp4_status_string")
 
 
 def lib():
@@ -84,6 +85,7 @@ def lib():
                                              vp, vp]
         L.fp4_gemm.argtypes = [op, op, i64, i64, i64, vp, i32, i32, vp]
         L.fp4_gemm_quantize.argtypes = [op, op, i64, i64, i64, vp, qp, vp, vp, vp, vp, i32, vp]
+        L.fp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, vp]
         L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
         L.fp4_sf_bytes.restype = i64
         L.fp4_block_size.argtypes = [i32]
@@ -93,7 +95,7 @@ def lib():
         L.fp4_status_string.restype = ctypes.c_char_p
         for f in ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
                   "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
-                  "fp4_gemm_quantize", "fp4_status_sync"):
+                  "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -178,6 +180,11 @@ def fp4_gemm_quantize(A, B, M, N, K, amax, p, q, sf, s_dec, row_shift=None, cano
     return lib().fp4_gemm_quantize(ctypes.byref(A), ctypes.byref(B), M, N, K, _ptr(amax),
                                    ctypes.byref(p), _ptr(q), _ptr(sf), _ptr(s_dec), _ptr(row_shift),
                                    int(canonicalize_1024), _stream(stream))
+
+
+def fp4_fp8_gemm(q8a, s8a, q8b, s8b, M, N, K, D, d_is_bf16, stream=None):
+    return lib().fp4_fp8_gemm(_ptr(q8a), _ptr(s8a), _ptr(q8b), _ptr(s8b), M, N, K, _ptr(D),
+                              int(bool(d_is_bf16)), _stream(stream))
 
 
 def fp4_sf_bytes(format, rows, cols, layout):
@@ -339,6 +346,34 @@ def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, strea
         D = torch.empty((M, N), dtype=out_dtype, device=a.q.device)
     _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
                     canonicalize_1024, stream), "fp4_gemm")
+    return D
+
+
+def fp8_gemm(q8a, s8a, q8b, s8b, out_dtype=torch.float32, out=None, stream=None):
+    """D = A B^T for two FP8 copies as the MXFP4 -> FP8 re-encoding emits them:
+    E4M3 codes q8 [rows, K] uint8 and binary32 scales s8 [rows, K / 128]."""
+    for t, name in ((q8a, "q8a"), (q8b, "q8b")):
+        if t.dtype != torch.uint8 or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"fp8_gemm: {name} must be a contiguous 2-D uint8 tensor")
+    for t, name in ((s8a, "s8a"), (s8b, "s8b")):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"fp8_gemm: {name} must be a contiguous float32 tensor")
+    M, K = q8a.shape
+    N = q8b.shape[0]
+    if q8b.shape[1] != K or s8a.numel() != M * (K // 128) or s8b.numel() != N * (K // 128):
+        raise ValueError("fp8_gemm: operand shapes disagree")
+    if out is not None:
+        if out.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("fp8_gemm: out must be float32 or bfloat16")
+        if tuple(out.shape) != (M, N) or not out.is_contiguous() or out.device != q8a.device:
+            raise ValueError(f"fp8_gemm: out must be a contiguous [{M}, {N}] tensor on {q8a.device}")
+        D = out
+    else:
+        if out_dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("fp8_gemm: out_dtype must be float32 or bfloat16")
+        D = torch.empty((M, N), dtype=out_dtype, device=q8a.device)
+    _check(fp4_fp8_gemm(q8a, s8a, q8b, s8b, M, N, K, D, D.dtype == torch.bfloat16, stream),
+           "fp4_fp8_gemm")
     return D
 
 

@@ -124,6 +124,32 @@ fp4_status fp4_mxfp4_to_fp8_transpose(const uint8_t *q, const uint8_t *sf, int64
   return launch_mxfp4_to_fp8_t(q, sf, rows, cols, q8t, s8t, as_stream(stream));
 }
 
+fp4_status fp4_fp8_gemm(const uint8_t *q8a, const float *s8a, const uint8_t *q8b,
+                        const float *s8b, int64_t M, int64_t N, int64_t K, void *D,
+                        int32_t d_is_bf16, void *stream) {
+  if (M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 8 != 0) return FP4_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!D) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(D)) return FP4_ERR_ALIGNMENT;
+  if (K > 0) {
+    if (!q8a || !s8a || !q8b || !s8b) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(q8a) || !aligned16(q8b) || !aligned4(s8a) || !aligned4(s8b))
+      return FP4_ERR_ALIGNMENT;
+  }
+  Fp8GemmJob j{};
+  j.qa = q8a;
+  j.qb = q8b;
+  j.sa = s8a;
+  j.sb = s8b;
+  j.M = M;
+  j.N = N;
+  j.K = K;
+  j.D = D;
+  j.d_bf16 = d_is_bf16 != 0;
+  return launch_gemm_fp8(j, as_stream(stream));
+}
+
 fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const float *amax_dev,
                         const fp4_quant_params *p, uint8_t *q, uint8_t *sf, float *s_dec_dev,
                         int8_t *row_shift, void *stream) {

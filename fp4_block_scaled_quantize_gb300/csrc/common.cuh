@@ -131,6 +131,15 @@ struct GemmJob {
   uint32_t offset_out;
 };
 fp4_status launch_gemm(const GemmJob &j, cudaStream_t s);
+// FP8 GEMM on E4M3 copies with per-(row, 128-column) power-of-two scales.
+struct Fp8GemmJob {
+  const uint8_t *qa, *qb;
+  const float *sa, *sb;
+  int64_t M, N, K;
+  void *D;
+  int d_bf16;
+};
+fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s);
 // Plain GEMM on SM pairs (tcgen05 cta_group::2); K > 0, no fused output.
 fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s);
 

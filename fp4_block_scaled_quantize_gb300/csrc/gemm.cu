@@ -37,6 +37,19 @@
 // Every mbarrier wait is bounded (about one second): on expiry the CTA
 // raises the timeout status bit, drains its own copies and MMAs (again
 // bounded), frees its tensor memory and returns.
+//
+// The same kernel, instantiated for kFP8, multiplies FP8 copies: E4M3
+// payloads (one byte per element, 128 elements per stage) with one binary32
+// power-of-two scale per row and 128 columns, the output of the direct
+// MXFP4 -> FP8 re-encoding ("Practical FP4 Training for Large-Scale MoE
+// Models on Hopper GPUs", Method: FP8 blocks of 128 elements).  The MMA is
+// tcgen05.mma.kind::mxf8f6f4 with one E8M0 scale per 32 elements
+// (scale_vec::1X); a 128-element block's code is the same for its four
+// 32-element MMA steps.  The scale warps read the binary32 scales from
+// global memory and write their E8M0 codes (exponent field) into the
+// stage's tensor-memory slot (four stages' scales of a row are one 16-byte
+// load, issued a group of stages ahead); a scale that is not a power of two
+// in [2^-127, 2^127] raises the scale-window status bit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,6 +66,7 @@ namespace fp4 {
 
 namespace {
 
+constexpr int kFP8 = 8;  // FP8 operand kind of this kernel (not a producer format)
 constexpr int BM = 128, BN = 256;
 constexpr int BK_BYTES = 128;  // 256 FP4 elements per stage
 constexpr int STAGES = 4;
@@ -77,6 +91,9 @@ constexpr uint32_t SF_SLOT = 48;     // 256 + 4 x 48 = 448 <= 512
 
 struct Params {
   const uint8_t *sfa, *sfb;
+  const float *s8a, *s8b;  // FP8: binary32 scales [rows][K / 128]
+  int64_t kb8;             // FP8: scale columns per row
+  int fp8_tma_scales;      // FP8: scales by tensor TMA (K % 512 == 0, 16-byte aligned)
   const float *sda, *sdb;
   const int8_t *sha, *shb;
   void *D;
@@ -106,7 +123,14 @@ constexpr uint32_t kHandoffBar = 1;  // barrier 0 is __syncthreads
 template <int FMT>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  if (FMT == kMXFP4) {
+  if (FMT == kFP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  } else if (FMT == kMXFP4) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
@@ -141,14 +165,17 @@ __device__ __forceinline__ uint32_t block_scale_rt(int fmt, float b, float se, f
 
 // Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, K-major A and B,
 // M = 128, N = 256; scale type E4M3 (block 16) or E8M0 (block 32).
+// kind::mxf8f6f4 (kFP8): E4M3 x E4M3 (type code 0), E8M0 scales.
 template <int FMT>
 __device__ __forceinline__ uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
   uint32_t d = 0;
   d |= (b_sf_id & 3u) << 4;
-  d |= 1u << 7;   // A: E2M1
-  d |= 1u << 10;  // B: E2M1
+  if (FMT != kFP8) {
+    d |= 1u << 7;   // A: E2M1
+    d |= 1u << 10;  // B: E2M1
+  }
   d |= (uint32_t)(BN >> 3) << 17;
-  d |= (FMT == kMXFP4 ? 1u : 0u) << 23;
+  d |= (FMT == kMXFP4 || FMT == kFP8 ? 1u : 0u) << 23;
   d |= (uint32_t)(BM >> 4) << 24;
   d |= (a_sf_id & 3u) << 29;
   return d;
@@ -157,6 +184,7 @@ __device__ __forceinline__ uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
 template <int FMT, bool QOUT>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+           const __grid_constant__ CUtensorMap tma_sa, const __grid_constant__ CUtensorMap tma_sb,
            const Params p) {
   constexpr int APK = (FMT == kMXFP4) ? 2 : 4;  // scale tiles per stage per 128 rows
   extern __shared__ uint8_t smem_raw[];
@@ -205,6 +233,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
+    uint32_t groups = 0;  // FP8 scale groups issued (buffer = groups & 1)
     bool ok = !p.stall_producer;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
@@ -215,12 +244,35 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         uint8_t *st = smem + stage * STAGE_BYTES;
+        const uint32_t fb = full_bar(stage);
+        if (FMT == kFP8) {
+          // FP8: operand tiles; with TMA scales, every fourth stage also
+          // brings the binary32 scales of its group of four stages (4
+          // columns x 128 A rows, 4 x 256 B rows) into the group buffer
+          // (the unused scale area of stage slot (group & 1))
+          const bool sg = p.fp8_tma_scales && (kt & 3) == 0;
+          mbar_expect_tx(fb, A_BYTES + B_BYTES + (sg ? (uint32_t)(SFA_BYTES + SFB_BYTES) : 0u));
+          tma_load_2d(smem_u32(st), &tma_a, fb, kt * BK_BYTES, mt * BM);
+          tma_load_2d(smem_u32(st + A_BYTES), &tma_b, fb, kt * BK_BYTES, nt * BN);
+          if (sg) {
+            const uint32_t gb = smem_u32(smem + (groups & 1u) * STAGE_BYTES + A_BYTES + B_BYTES);
+            tma_load_2d(gb, &tma_sa, fb, kt, mt * BM);
+            tma_load_2d(gb + SFA_BYTES, &tma_sb, fb, kt, nt * BN);
+            ++groups;
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         const int64_t atoms = min((int64_t)APK, p.cp4 - (int64_t)kt * APK);
         uint32_t bytes = A_BYTES + B_BYTES + (uint32_t)atoms * 512u;
         const bool g1 = (2 * (int64_t)nt + 1) < p.ngrp_b;
         if (g1) bytes += (uint32_t)atoms * 512u;
         bytes += (uint32_t)atoms * 512u;  // group 0 of B always exists
-        const uint32_t fb = full_bar(stage);
         mbar_expect_tx(fb, bytes);
         tma_load_2d(smem_u32(st), &tma_a, fb, kt * BK_BYTES, mt * BM);
         tma_load_2d(smem_u32(st + A_BYTES), &tma_b, fb, kt * BK_BYTES, nt * BN);
@@ -269,8 +321,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sfb_t = sfa_t + 16;
           const uint64_t da = desc_sw128(st), db = desc_sw128(st + A_BYTES);
           for (int kk = 0; kk < nks; ++kk) {
-            const int a = (FMT == kMXFP4) ? kk >> 1 : kk;
-            const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : 0u;
+            // scale atom of this MMA and byte of its 32-bit words: block 16
+            // one atom per MMA; MXFP4 two MMAs per atom; FP8 one atom per
+            // stage, byte kk (the four bytes hold the same code)
+            const int a = (FMT == kMXFP4) ? kk >> 1 : (FMT == kFP8 ? 0 : kk);
+            const uint32_t id = (FMT == kMXFP4) ? 2u * (kk & 1) : (FMT == kFP8 ? (uint32_t)kk : 0u);
             tc_mma<FMT>(tmem + ACC_COL, da + 2 * kk, db + 2 * kk, idesc<FMT>(id, id),
                         sfa_t + 4 * a, sfb_t + 8 * a, (kt | kk) != 0);
           }
@@ -303,6 +358,165 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    if (FMT == kFP8 && p.fp8_tma_scales) {
+      // FP8, TMA scales: the stage's column (kt & 3) of its group buffer,
+      // landed with the group's first stage.  The conversion is branch-free:
+      // it sits on the path from a landed stage to its MMAs.  Rows past M or
+      // N (zero fill) are written as code 127.
+      uint32_t bad = 0u;
+      uint32_t groups = 0;
+      int tile = blockIdx.x, kt = 0;
+      int64_t left_a = 0, left_b = 0;  // rows of this tile inside A and B
+      while (tile < ntiles) {
+        if (kt == 0) {
+          const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
+          const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
+          left_a = p.M - (int64_t)mt * BM;
+          left_b = p.N - (int64_t)nt * BN;
+        }
+        if (!mbar_wait_issuer(full_bar(stage), phase, abort_flag, p.status)) {
+          bar_red_or(kHandoffBar, kHandoffThreads, true);
+          break;
+        }
+        tc_fence_after();
+        if ((kt & 3) == 0) ++groups;
+        const float *gbuf = reinterpret_cast<const float *>(smem + ((groups - 1u) & 1u) * STAGE_BYTES +
+                                                            A_BYTES + B_BYTES);
+        // E8M0 code of a power of two in [2^-127, 2^127], four copies
+        auto code = [&](float sc, bool valid) -> uint32_t {
+          const uint32_t b = __float_as_uint(sc);
+          const uint32_t c = b >> 23;
+          const bool normal = (b & 0x807FFFFFu) == 0u && c - 1u < 254u;
+          const bool tiny = b == 0x00400000u;  // 2^-127, a binary32 subnormal
+          bad |= (valid && !normal && !tiny) ? 1u : 0u;
+          return (valid ? (normal ? c : (tiny ? 0u : 127u)) : 127u) * 0x01010101u;
+        };
+        uint32_t wa[4], wb[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          wa[j] = code(gbuf[4 * r + (kt & 3)], r < left_a);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = 128 * (j >> 2) + lane + 32 * (j & 3);
+          wb[j] = code(gbuf[SFA_BYTES / 4 + 4 * r + (kt & 3)], r < left_b);
+        }
+        const uint32_t sfa_t = tmem + lane_base + SF_COL0 + SF_SLOT * (uint32_t)stage;
+        tc_st_4cols(sfa_t, wa);
+        tc_st_8cols(sfa_t + 16, wb);
+        tc_wait_st();
+        tc_fence_before();
+        if (bar_red_or(kHandoffBar, kHandoffThreads, false)) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++kt == p.k_tiles) {
+          kt = 0;
+          tile += gridDim.x;
+        }
+      }
+      if (bad) raise_status(p.status, kStatusScaleWindow);
+      ok = false;
+    } else if (FMT == kFP8) {
+      // FP8: the binary32 scales of four consecutive stages of a row are one
+      // 16-byte load (columns 4g .. 4g + 3); the loads of the next group of
+      // stages are in flight while the current group is written.  Lane l
+      // writes rows l + 32 j of each 128-row group as 32-bit words of four
+      // equal E8M0 codes, the image the block-16 path leaves for one
+      // 512-byte scale tile.
+      float4 nxa[4], nxb[8];   // next group, in flight
+      uint32_t cda[4], cdb[8];  // current group: code of stage 4g + c in byte c
+      const bool vec = (p.kb8 & 3) == 0;  // rows 16-byte aligned
+      auto load4 = [&](const float *sc, int64_t r, int64_t rows, int g) -> float4 {
+        float4 v = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+        if (r < rows) {
+          const float *row = sc + r * p.kb8;
+          if (vec) {
+            v = __ldg(reinterpret_cast<const float4 *>(row) + g);
+          } else {
+            const int64_t c = 4 * (int64_t)g;
+            v.x = __ldg(row + c);
+            if (c + 1 < p.kb8) v.y = __ldg(row + c + 1);
+            if (c + 2 < p.kb8) v.z = __ldg(row + c + 2);
+            if (c + 3 < p.kb8) v.w = __ldg(row + c + 3);
+          }
+        }
+        return v;
+      };
+      auto fetch = [&](int tile, int g) {
+        const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
+        const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) nxa[j] = load4(p.s8a, (int64_t)mt * BM + lane + 32 * j, p.M, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          nxb[j] = load4(p.s8b, (int64_t)nt * BN + 128 * (j >> 2) + lane + 32 * (j & 3), p.N, g);
+      };
+      bool bad = false;
+      // E8M0 code of a power-of-two scale in [2^-127, 2^127]
+      auto code1 = [&](float sc) -> uint32_t {
+        const uint32_t b = __float_as_uint(sc);
+        uint32_t c = b >> 23;
+        if (b == 0x00400000u) {
+          c = 0u;  // 2^-127, a binary32 subnormal
+        } else if ((b & 0x807FFFFFu) != 0u || c == 0u || c == 255u) {
+          bad = true;
+          c = 127u;
+        }
+        return c;
+      };
+      auto codes4 = [&](float4 v) {
+        return code1(v.x) | (code1(v.y) << 8) | (code1(v.z) << 16) | (code1(v.w) << 24);
+      };
+      int tile = blockIdx.x, kt = 0;
+      if (tile < ntiles) fetch(tile, 0);
+      while (tile < ntiles) {
+        if ((kt & 3) == 0) {
+          // this group's loads were issued a group of stages ago
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cda[j] = codes4(nxa[j]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cdb[j] = codes4(nxb[j]);
+          int tg = tile, g = (kt >> 2) + 1;
+          if (4 * g >= p.k_tiles) {
+            g = 0;
+            tg += gridDim.x;
+          }
+          if (tg < ntiles) fetch(tg, g);
+        }
+        // every lane waits (inlined), so the next group's loads stay in
+        // flight across the wait
+        if (!mbar_wait_inl(full_bar(stage), phase, abort_flag, p.status)) {
+          bar_red_or(kHandoffBar, kHandoffThreads, true);
+          break;
+        }
+        tc_fence_after();
+        const int sh = 8 * (kt & 3);
+        uint32_t wa[4], wb[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wa[j] = ((cda[j] >> sh) & 0xFFu) * 0x01010101u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wb[j] = ((cdb[j] >> sh) & 0xFFu) * 0x01010101u;
+        const uint32_t sfa_t = tmem + lane_base + SF_COL0 + SF_SLOT * (uint32_t)stage;
+        tc_st_4cols(sfa_t, wa);
+        tc_st_8cols(sfa_t + 16, wb);
+        tc_wait_st();
+        tc_fence_before();
+        if (bar_red_or(kHandoffBar, kHandoffThreads, false)) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++kt == p.k_tiles) {
+          kt = 0;
+          tile += gridDim.x;
+        }
+      }
+      if (bad) raise_status(p.status, kStatusScaleWindow);
+      ok = false;  // the block-scaled loop below is for the FP4 kinds
+    }
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         int good = 1;
@@ -358,7 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quad = warp & 3;
     const int half = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
-    const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    const float alpha = (FMT == kFP8) ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     float se_o = 1.0f, sd_o = 1.0f;  // tensor scale of the fused output copy
     if (QOUT) {
       tensor_scale_rt(p.fmt_out, __ldg(p.amax_out), p.T_out, se_o, sd_o);
@@ -413,22 +627,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             float mult;
             bool zp;
             code = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
-            for (int g = 0; g < QB / 16; ++g) {
-              float v[16];
+            // 8 values at a time; under SR one Philox block covers 16
+            // elements of the output row (words x, y for the first 8)
+            uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+            for (int h = 0; h < QB / 8; ++h) {
+              float v[8];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = y[o + 16 * g + j];
+              for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
               scale8(v, mult, zp);
-              scale8(v + 8, mult, zp);
-              const int64_t n = n0 + o + 16 * g;
               if (p.sr_out) {
-                // one Philox block per 16 elements of the output row
-                const uint2 qq = encode16_sr(v, p.seed_out, p.offset_out, 0u,
-                                             ((uint64_t)m * (uint64_t)p.N + (uint64_t)n) >> 4);
-                qacc[4 * q + 2 * blk + 2 * g] = qq.x;
-                qacc[4 * q + 2 * blk + 2 * g + 1] = qq.y;
+                if ((h & 1) == 0)
+                  rw = sr_words16(p.seed_out, p.offset_out, 0u,
+                                  ((uint64_t)m * (uint64_t)p.N + (uint64_t)(n0 + o + 8 * h)) >> 4);
+                qacc[4 * q + 2 * blk + h] =
+                    (h & 1) ? e2m1x8_sr(v, rw.z, rw.w) : e2m1x8_sr(v, rw.x, rw.y);
               } else {
-                qacc[4 * q + 2 * blk + 2 * g] = e2m1x8_hw(v);
-                qacc[4 * q + 2 * blk + 2 * g + 1] = e2m1x8_hw(v + 8);
+                qacc[4 * q + 2 * blk + h] = e2m1x8_hw(v);
               }
             }
           }
@@ -556,8 +770,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ------------------------------------------------------------- host side
 template <int FMT, bool QOUT>
-fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int grid,
-                      cudaStream_t s) {
+fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &msa,
+                      const CUtensorMap &msb, const Params &p, int grid, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -565,11 +779,52 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
-  k_gemm<FMT, QOUT><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  k_gemm<FMT, QOUT><<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, msa, msb, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 }  // namespace
+
+fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s) {
+  const size_t elt = j.d_bf16 ? 2 : 4;
+  if (j.K == 0) {
+    return cudaMemsetAsync(j.D, 0, (size_t)j.M * j.N * elt, s) == cudaSuccess ? FP4_OK
+                                                                             : FP4_ERR_CUDA;
+  }
+  uint32_t *status = status_word();
+  if (!status) return FP4_ERR_CUDA;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, j.qa, j.M, j.K, BM) || !make_map(&mb, j.qb, j.N, j.K, BN))
+    return FP4_ERR_CUDA;
+  Params p{};
+  p.s8a = j.sa;
+  p.s8b = j.sb;
+  p.kb8 = j.K / 128;
+  p.D = j.D;
+  p.M = j.M;
+  p.N = j.N;
+  p.K = j.K;
+  p.m_tiles = (int)ceil_div(j.M, BM);
+  p.n_tiles = (int)ceil_div(j.N, BN);
+  p.k_steps = (int)(j.K / 32);   // one K32 MMA step per 32 bytes
+  p.k_tiles = (int)(j.K / 128);  // 128 bytes of K per stage
+  p.n_fast = j.M >= j.N ? 1 : 0;
+  p.d_bf16 = j.d_bf16;
+  p.status = status;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  // scales by tensor TMA when a row of them is a whole number of 16-byte
+  // units and both arrays start 16-byte aligned; else the scale warps load
+  // them (four columns per 16-byte load where aligned)
+  CUtensorMap msa = ma, msb = mb;
+  p.fp8_tma_scales = (p.kb8 % 4 == 0) && ((uintptr_t)j.sa % 16 == 0) && ((uintptr_t)j.sb % 16 == 0) &&
+                     make_map_f32(&msa, j.sa, j.M, p.kb8, 4, BM) &&
+                     make_map_f32(&msb, j.sb, j.N, p.kb8, 4, BN);
+  return launch_fmt<kFP8, false>(ma, mb, msa, msb, p, grid, s);
+}
 
 fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   const size_t elt = j.d_bf16 ? 2 : 4;
@@ -641,11 +896,11 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   }
   fp4_status st;
   if (j.q_out)
-    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, true>(ma, mb, p, grid, s)
-                           : launch_fmt<kNVFP4, true>(ma, mb, p, grid, s);
+    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, true>(ma, mb, ma, mb, p, grid, s)
+                           : launch_fmt<kNVFP4, true>(ma, mb, ma, mb, p, grid, s);
   else
-    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, false>(ma, mb, p, grid, s)
-                           : launch_fmt<kNVFP4, false>(ma, mb, p, grid, s);
+    st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, false>(ma, mb, ma, mb, p, grid, s)
+                           : launch_fmt<kNVFP4, false>(ma, mb, ma, mb, p, grid, s);
   if (st != FP4_OK || !j.q_out) return st;
   if (j.fmt_out == kUE5M3 && j.sf_mma_out && j.shift_out)
     return launch_remap_ue5m3(j.sf_out, j.q_out, j.M, j.N, j.shift_out, s);

@@ -175,6 +175,24 @@ fp4_status fp4_mxfp4_to_fp8_transpose(const uint8_t *q, const uint8_t *sf,
                                       int64_t rows, int64_t cols, uint8_t *q8t,
                                       float *s8t, void *stream);
 
+/* FP8 GEMM on re-encoded copies ([HOP] Method: the direct FP4 -> FP8
+ * conversion feeds an FP8 tensor-core GEMM): D[M][N] = A B^T with
+ * A[m][k] = e4m3(q8a[m][k]) * s8a[m][k/128] and B likewise, exactly the
+ * operands fp4_mxfp4_to_fp8 / fp4_mxfp4_to_fp8_transpose emit.  Runs on
+ * tcgen05.mma.kind::mxf8f6f4 with E8M0 block scales: every s8 must be a
+ * power of two in [2^-127, 2^127] (the re-encoding gives 2^(max E - 6),
+ * outside that range only when all four MXFP4 blocks of a 128-block have
+ * codes below 6); any other value raises FP4_ERR_SCALE_WINDOW in the
+ * status word and its block's scale is read as 1.  The tensor core adds K
+ * in steps of one 32-element MMA into a binary32 accumulator.  D is
+ * binary32 (d_is_bf16 == 0) or BF16 (nearest-even), row pitch N elements.
+ * Shapes: M, N, K >= 0, K % 128 == 0, N % 8 == 0; K == 0 writes zeros.
+ * Alignment: q8a, q8b and D 16 bytes, s8a and s8b 4 bytes.  The caller
+ * owns every buffer; argument errors are returned before any launch. */
+fp4_status fp4_fp8_gemm(const uint8_t *q8a, const float *s8a, const uint8_t *q8b,
+                        const float *s8b, int64_t M, int64_t N, int64_t K, void *D,
+                        int32_t d_is_bf16, void *stream);
+
 /* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
  * payload, RNE or SR, zero-scale rule, 2D weight tiles):
  *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);

@@ -134,6 +134,20 @@ def test_mxfp4_to_fp8_transpose_argument_errors_before_any_launch(L):
     assert f(None, None, 0, 64, None, None, None) == 0      # empty
 
 
+def test_fp8_gemm_argument_errors_before_any_launch(L):
+    f = L.fp4_fp8_gemm
+    ok = (4096, 8192, 12288, 16384)  # q8a, s8a, q8b, s8b (never dereferenced)
+    assert f(*ok, 128, 256, 96, 20480, 0, None) == fq.FP4_ERR_SHAPE      # K % 128
+    assert f(*ok, 128, 252, 128, 20480, 0, None) == fq.FP4_ERR_SHAPE     # N % 8
+    assert f(*ok, -1, 256, 128, 20480, 0, None) == 1
+    assert f(*ok, 128, 256, 128, None, 0, None) == 1                     # no output
+    assert f(4096, None, 12288, 16384, 128, 256, 128, 20480, 0, None) == 1
+    assert f(4104, 8192, 12288, 16384, 128, 256, 128, 20480, 0, None) == 2  # q8a alignment
+    assert f(4096, 8194, 12288, 16384, 128, 256, 128, 20480, 0, None) == 2  # s8a alignment
+    assert f(*ok, 128, 256, 128, 20488, 0, None) == 2                    # D alignment
+    assert f(None, None, None, None, 0, 256, 128, None, 0, None) == 0    # empty: nothing to do
+
+
 def test_amax_argument_errors_before_any_launch(L):
     f = L.fp4_amax
     assert f(4096, 4, 16, 0, 0, None, None, None) == 1          # no output
