@@ -197,8 +197,10 @@ def amax_pair(x, hadamard_n=0, signs=0):
 # -------------------------------------------------------------- quantizers
 
 def quantize_rows(x, fmt, s_enc, s_dec, sr=False, seed=0, offset=0, copy_id=0,
-                  threads=None):
-    """One copy, blocks along rows.  Returns (q [R, C/2] u8, sf [R, C/B] u8)."""
+                  threads=None, row_base=0):
+    """One copy, blocks along rows.  Returns (q [R, C/2] u8, sf [R, C/B] u8).
+    row_base: the copy-row index of x's first row (stochastic-rounding
+    counters use the copy's own row index)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     R, C = x.shape
     B = block_size(fmt)
@@ -213,7 +215,7 @@ def quantize_rows(x, fmt, s_enc, s_dec, sr=False, seed=0, offset=0, copy_id=0,
         if r1 <= r0:
             return
         lib().orc_quantize_rows(_p(x[r0:r1], ctypes.c_float), r1 - r0, C, fmt, s_enc, s_dec,
-                                1 if sr else 0, seed, offset, copy_id, r0,
+                                1 if sr else 0, seed, offset, copy_id, row_base + r0,
                                 _p(q[r0:r1], ctypes.c_uint8), _p(sf[r0:r1], ctypes.c_uint8))
 
     if nt == 1 or R <= chunk:
@@ -273,6 +275,70 @@ def quantize_transpose(x, amax_row, amax_col, fmt, T=448.0, block2d=False, sr_ro
     q_c, sf_c = quantize_rows(xt, fmt, s_enc_c, s_dec_c, sr=sr_col, seed=seed, offset=offset,
                               copy_id=1, threads=threads)
     return dict(q=q_r, sf=sf_r, s_dec=s_dec_r), dict(q=q_c, sf=sf_c, s_dec=s_dec_c)
+
+
+# --------------------------------------------- CTA-local NVFP4 (stripes)
+# "Format-Aware Fusion for Fast FP4 Pretraining", Abstract: a CTA-local NVFP4
+# scale contract.  Reading: the NVFP4 tensor scale taken per 128-row stripe of
+# each K-major copy (over the stripe's full K); every other step is NVFP4's.
+
+STRIPE = 128
+
+
+def stripe_amax(x):
+    """max |x| of each 128-row stripe of x (the last may be shorter)."""
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([amax(x[i:i + STRIPE]) for i in range(0, x.shape[0], STRIPE)],
+                    dtype=np.float32)
+
+
+def quantize_stripes(x, amaxes, T=448.0, sr=False, seed=0, offset=0, copy_id=0):
+    """Row-wise NVFP4 copy of x with stripe i quantised under its own tensor
+    scale from amaxes[i]: each stripe exactly as an NVFP4 copy of that stripe
+    alone, SR counters at the copy's global rows.  Returns dict(q, sf, s_dec
+    [stripes])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    q = np.zeros((R, C // 2), np.uint8)
+    sf = np.zeros((R, C // 16), np.uint8)
+    s_dec = np.zeros(len(amaxes), np.float32)
+    for i, r0 in enumerate(range(0, R, STRIPE)):
+        s_enc_i, s_dec[i] = tensor_scale(NVFP4, T, amaxes[i])
+        q[r0:r0 + STRIPE], sf[r0:r0 + STRIPE] = quantize_rows(
+            x[r0:r0 + STRIPE], NVFP4, s_enc_i, s_dec[i], sr=sr, seed=seed, offset=offset,
+            copy_id=copy_id, row_base=r0)
+    return dict(q=q, sf=sf, s_dec=s_dec)
+
+
+def quantize_transpose_stripes(x, T=448.0, T_col=None, sr_row=False, sr_col=False, seed=0,
+                               offset=0):
+    """Both copies under the stripe contract, with current stripe maxima: the
+    row-wise copy's stripes are 128-row stripes of x, the transposed copy's
+    are 128-column stripes of x (rows of x^T)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    xt = np.ascontiguousarray(x.T)
+    row = quantize_stripes(x, stripe_amax(x), T, sr=sr_row, seed=seed, offset=offset, copy_id=0)
+    col = quantize_stripes(xt, stripe_amax(xt), T if T_col is None else T_col, sr=sr_col,
+                           seed=seed, offset=offset, copy_id=1)
+    return row, col
+
+
+def gemm_model_stripes(qa, sfa, qb, sfb, K, s_dec_a, s_dec_b, mi, ni, canon=False):
+    """The probe-matched model for stripe-scaled NVFP4 operands: output
+    (m, n) is gemm_model with the tensor scales of stripes m // 128 of A and
+    n // 128 of B.  Returns (y_model, y_exact, s_abs) like gemm_model."""
+    mi = np.asarray(mi, np.int64)
+    ni = np.asarray(ni, np.int64)
+    y = np.zeros(len(mi), np.float32)
+    ye = np.zeros(len(mi), np.float64)
+    sa = np.zeros(len(mi), np.float64)
+    keys = (mi // STRIPE) * (1 << 32) + (ni // STRIPE)
+    for key in np.unique(keys):
+        sel = np.flatnonzero(keys == key)
+        i, j = int(key >> 32), int(key & 0xFFFFFFFF)
+        y[sel], ye[sel], sa[sel] = gemm_model(qa, sfa, qb, sfb, NVFP4, K, float(s_dec_a[i]),
+                                              float(s_dec_b[j]), mi[sel], ni[sel], canon=canon)
+    return y, ye, sa
 
 
 # ------------------------------------------------------- tensor-core scales

@@ -866,3 +866,99 @@ def test_transposed_copy_target_t_col():
     np.testing.assert_array_equal(c1["sf"], c2["sf"])
     np.testing.assert_array_equal(c1["q"], c2["q"])
     assert c1["s_dec"] == c2["s_dec"] and r1["s_dec"] == r0["s_dec"]
+
+
+# ------------------------------------------------ CTA-local NVFP4 (stripes)
+# Reading of "Format-Aware Fusion for Fast FP4 Pretraining", Abstract: the
+# NVFP4 tensor scale taken per 128-row stripe of each K-major copy.
+
+def _stripe_input(R=384, C=96, seed=0):
+    return np.random.default_rng(seed).standard_normal((R, C)).astype(np.float32)
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_stripes_reduce_to_the_global_copy_when_maxima_agree(sr):
+    """Every stripe holding the same maximum |x|: each stripe's tensor scale
+    is the global one, so the stripe copy is the global NVFP4 copy bit for
+    bit, stochastic rounding included (a stripe that restarted the SR row
+    counter would differ)."""
+    x = _stripe_input(R=400)
+    for r0 in range(0, 400, 128):
+        x[r0 + 5, 7] = 9.5
+    a = orc.stripe_amax(x)
+    assert np.all(a == np.float32(9.5)) and len(a) == 4
+    got = orc.quantize_stripes(x, a, sr=sr, seed=11, offset=3)
+    want = orc.quantize(x, orc.amax(x), orc.NVFP4, sr=sr, seed=11, offset=3)
+    assert np.array_equal(got["q"], want["q"]) and np.array_equal(got["sf"], want["sf"])
+    assert np.all(got["s_dec"] == np.float32(want["s_dec"]))
+
+
+def test_stripe_scales_absorb_a_power_of_two_per_stripe():
+    """Multiplying stripe i by 2^k_i leaves every code of the stripe copy
+    unchanged and multiplies s_dec_i by exactly 2^k_i (each stripe's tensor
+    scale follows its own maximum).  A global tensor scale, or stripes of
+    another height, would change codes."""
+    x = _stripe_input(R=512)
+    k = [-5, 3, 0, 7]
+    y = x.copy()
+    for i, ki in enumerate(k):
+        y[128 * i:128 * (i + 1)] *= np.float32(2.0 ** ki)
+    cx = orc.quantize_stripes(x, orc.stripe_amax(x))
+    cy = orc.quantize_stripes(y, orc.stripe_amax(y))
+    assert np.array_equal(cx["q"], cy["q"]) and np.array_equal(cx["sf"], cy["sf"])
+    assert np.array_equal(cy["s_dec"], cx["s_dec"] * np.float32(2.0) ** np.array(k, np.float32))
+    glob = orc.quantize(y, orc.amax(y), orc.NVFP4)
+    assert not np.array_equal(glob["sf"], cy["sf"])
+
+
+def test_transposed_copy_stripes_are_column_stripes_of_x():
+    """The transposed copy's stripes are 128-column stripes of x: scaling a
+    column stripe of x by a power of two leaves the transposed copy's codes
+    unchanged (and changes the row-wise copy's)."""
+    x = _stripe_input(R=256, C=384)
+    y = x.copy()
+    y[:, 128:256] *= np.float32(2.0 ** -9)
+    rx, cx = orc.quantize_transpose_stripes(x)
+    ry, cy = orc.quantize_transpose_stripes(y)
+    assert np.array_equal(cx["q"], cy["q"]) and np.array_equal(cx["sf"], cy["sf"])
+    assert cy["s_dec"][1] == cx["s_dec"][1] * np.float32(2.0 ** -9)
+    assert cy["s_dec"][0] == cx["s_dec"][0] and cy["s_dec"][2] == cx["s_dec"][2]
+    assert not np.array_equal(rx["sf"], ry["sf"])
+
+
+def test_stripe_gemm_model_applies_each_stripe_pair_scale():
+    """Model outputs of stripe-scaled operands are the unscaled model outputs
+    times 2^(k_m + k_n) exactly, and the exact reference is the float64 dot
+    product of the decoded operands times s_dec_A[m/128] s_dec_B[n/128]."""
+    K = 128
+    a = _stripe_input(R=256, C=K, seed=1)
+    b = _stripe_input(R=256, C=K, seed=2)
+    ka, kb = [2, -3], [0, 5]
+    a2, b2 = a.copy(), b.copy()
+    for i in range(2):
+        a2[128 * i:128 * (i + 1)] *= np.float32(2.0 ** ka[i])
+        b2[128 * i:128 * (i + 1)] *= np.float32(2.0 ** kb[i])
+    ca, cb = orc.quantize_stripes(a, orc.stripe_amax(a)), orc.quantize_stripes(b, orc.stripe_amax(b))
+    ca2, cb2 = (orc.quantize_stripes(a2, orc.stripe_amax(a2)),
+                orc.quantize_stripes(b2, orc.stripe_amax(b2)))
+    rng = np.random.default_rng(3)
+    mi, ni = rng.integers(0, 256, 200), rng.integers(0, 256, 200)
+    y, ye, _ = orc.gemm_model_stripes(ca["q"], ca["sf"], cb["q"], cb["sf"], K, ca["s_dec"],
+                                      cb["s_dec"], mi, ni)
+    y2, _, _ = orc.gemm_model_stripes(ca2["q"], ca2["sf"], cb2["q"], cb2["sf"], K, ca2["s_dec"],
+                                      cb2["s_dec"], mi, ni)
+    f = np.array([2.0 ** (ka[m // 128] + kb[n // 128]) for m, n in zip(mi, ni)])
+    assert np.array_equal(y2.astype(np.float64), y.astype(np.float64) * f)
+
+    def decode(c, r):
+        vals = np.array([orc.e2m1_value(v) for v in range(16)])
+        q = c["q"][r]
+        codes = np.stack([q & 15, q >> 4], axis=1).reshape(-1)
+        sc = np.repeat([orc.scale_value(orc.NVFP4, s) for s in c["sf"][r]], 16)
+        return vals[codes] * sc
+
+    for t in range(0, 200, 25):
+        m, n = mi[t], ni[t]
+        dot = float(np.dot(decode(ca, m), decode(cb, n)))
+        want = dot * float(ca["s_dec"][m // 128]) * float(cb["s_dec"][n // 128])
+        assert ye[t] == pytest.approx(want, rel=1e-12, abs=1e-300)
