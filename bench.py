@@ -38,7 +38,9 @@ import torch  # noqa: E402
 
 M_TOK, K_FF, N_MODEL = 8192, 14336, 4096
 WORKLOAD = "8B MLP down_proj fwd+bwd (refresh step), UE5M3-b16"
-FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32", 3: "UE5M3-b32"}
+FMT_NAMES = {0: "UE5M3-b16", 1: "NVFP4-b16", 2: "MXFP4-b32", 3: "UE5M3-b32",
+             4: "NVFP4-CTA-local (tensor scale per 128-row stripe)"}
+CTA = 4  # CTA-local NVFP4: current stripe maxima, 1D weight copies
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor ratio on GB300
 UNIT = "% of one GB300 roofline (step ideal time / step time, summed over GPUs)"
 L2_FLUSH_BYTES = 2 * 129 * 1000 * 1000  # twice the L2
@@ -179,12 +181,21 @@ class Layer:
         self.fmt = fmt
         mma = fq.FP4_SF_MMA
         self.px = fq.params(format=fmt, T=448.0, sf_layout=mma)
-        self.pw = fq.params(format=fmt, T=448.0, block2d=True, sf_layout=mma)
+        # (the stripe contract has no 2D tiles: W gets two 1D copies)
+        self.pw = fq.params(format=fmt, T=448.0, block2d=(fmt != CTA), sf_layout=mma)
         self.pdy = fq.params(format=fmt, T=448.0, round_row=fq.FP4_ROUND_SR,
                              round_col=fq.FP4_ROUND_SR, sr_seed=42, sf_layout=mma)
         f32 = dict(dtype=torch.float32, device=device)
-        # one amax per operand (no rotation: the transposed copy uses it too)
-        self.amax = {k: (a, a) for k, a in ((k, torch.zeros(1, **f32)) for k in ("X", "W", "dY"))}
+        if fmt == CTA:
+            # stripe maxima: per 128-row stripe (row-wise copy) and per
+            # 128-column stripe (transposed copy) of each operand
+            self.amax = {k: (torch.zeros(fq.n_stripes(t.shape[0]), **f32),
+                             torch.zeros(fq.n_stripes(t.shape[1]), **f32))
+                         for k, t in (("X", self.X), ("W", self.W), ("dY", self.dY))}
+        else:
+            # one amax per operand (no rotation: the transposed copy uses it too)
+            self.amax = {k: (a, a) for k, a in ((k, torch.zeros(1, **f32))
+                                                for k in ("X", "W", "dY"))}
         self.refresh_amax()
         self.xr, self.xc = fq.quantize_transpose(self.X, *self.amax["X"], self.px)
         self.wr, self.wc = fq.quantize_transpose(self.W, *self.amax["W"], self.pw)
@@ -195,6 +206,10 @@ class Layer:
 
     def refresh_amax(self):
         fq = self.fq
+        if self.fmt == CTA:
+            for k, t in (("X", self.X), ("W", self.W), ("dY", self.dY)):
+                fq._check(fq.fp4_amax_stripes(t, *self.amax[k]), "amax stripes")
+            return
         fq._check(fq.fp4_amax_many([self.X, self.W, self.dY],
                                    [self.amax[k][0] for k in ("X", "W", "dY")]), "amax")
 
@@ -400,9 +415,10 @@ def run_gpu(args, world, rank, local):
 
 
 def layer_launches(fmt):
-    """Kernel launches of one step: amax (zeroing + one batched launch),
-    producers x3, GEMMs x3, one remap per UE5M3 producer."""
-    return 2 + 3 + 3 + (3 if fmt in (0, 3) else 0)
+    """Kernel launches of one step: amax (zeroing + one batched launch; the
+    stripe contract: one stripe-maxima launch per operand), producers x3,
+    GEMMs x3, one remap per UE5M3 producer."""
+    return (3 if fmt == CTA else 2) + 3 + 3 + (3 if fmt in (0, 3) else 0)
 
 
 def median_ms(fn, flush, reps=20):
@@ -453,7 +469,7 @@ def run_per_format(args, world, host, dev, flush, pk):
     """The same step under the comparison formats (NVFP4-b16, MXFP4-b32) and
     the UE5M3-b32 control, measured exactly as the headline format."""
     out = {}
-    for fmt in (0, 1, 2, 3):
+    for fmt in (0, 1, 2, 3, CTA):
         if fmt == args.format:
             continue
         layer = Layer(fmt, seed=0, device=dev, host=host)
@@ -461,6 +477,7 @@ def run_per_format(args, world, host, dev, flush, pk):
         summ = summarize_layer(fmt, m, pk, world)
         out[FMT_NAMES[fmt]] = {"value": round(summ["value"], 3), "unit": UNIT,
                                "ms_per_step": round(m["step_ms"], 4),
+                               "launches_per_step": layer_launches(fmt),
                                "quantize": summ["quantize"], "amax": summ["amax"],
                                "gemm": summ["gemm"]}
         del layer, m

@@ -20,6 +20,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libfp4gb300.so")
 
 FP4_FMT_UE5M3_B16, FP4_FMT_NVFP4_B16, FP4_FMT_MXFP4_B32, FP4_FMT_UE5M3_B32 = 0, 1, 2, 3
+FP4_FMT_NVFP4_CTA = 4  # NVFP4 with one tensor scale per 128-row stripe of each copy
+STRIPE = 128
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
 FP4_SF_PLAIN, FP4_SF_MMA = 0, 1
 FP4_OK = 0
@@ -59,7 +61,8 @@ class FP4Error(RuntimeError):
 
 
 _lib = None
-EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
+EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
+           "fp4_mxfp4_to_fp8_transpose",
            "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
            "fp4_fp8_gemm", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
            "fp4_status_string")
@@ -78,6 +81,7 @@ def lib():
         op = ctypes.POINTER(fp4_operand)
         L.fp4_amax.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp]
         L.fp4_amax_many.argtypes = [ctypes.POINTER(fp4_amax_job), i32, vp]
+        L.fp4_amax_stripes.argtypes = [vp, i64, i64, vp, vp, vp]
         L.fp4_mxfp4_to_fp8.argtypes = [vp, vp, i64, i64, vp, vp, vp]
         L.fp4_mxfp4_to_fp8_transpose.argtypes = [vp, vp, i64, i64, vp, vp, vp]
         L.fp4_quantize.argtypes = [vp, i64, i64, vp, qp, vp, vp, vp, vp, vp]
@@ -93,7 +97,8 @@ def lib():
         L.fp4_status_sync.argtypes = [vp]
         L.fp4_status_string.argtypes = [i32]
         L.fp4_status_string.restype = ctypes.c_char_p
-        for f in ("fp4_amax", "fp4_amax_many", "fp4_mxfp4_to_fp8", "fp4_mxfp4_to_fp8_transpose",
+        for f in ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
+                  "fp4_mxfp4_to_fp8_transpose",
                   "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_status_sync"):
             getattr(L, f).restype = i32
@@ -143,6 +148,12 @@ def fp4_amax_many(xs, outs, stream=None):
         rows, cols = x.shape
         jobs[k] = fp4_amax_job(x.data_ptr() if x.numel() else None, rows, cols, o.data_ptr())
     return lib().fp4_amax_many(jobs, n, _stream(stream))
+
+
+def fp4_amax_stripes(x, amax_rows, amax_cols=None, stream=None):
+    rows, cols = x.shape
+    return lib().fp4_amax_stripes(_ptr(x), rows, cols, _ptr(amax_rows), _ptr(amax_cols),
+                                  _stream(stream))
 
 
 def fp4_mxfp4_to_fp8(q, sf, rows, cols, q8, s8, stream=None):
@@ -228,11 +239,17 @@ class Quantized:
                            self.format, self.rows, self.k)
 
 
+def n_stripes(rows):
+    return (rows + STRIPE - 1) // STRIPE
+
+
 def _alloc_copy(rows, cols, p, device, with_shift):
     q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
     nsf = fp4_sf_bytes(p.format, rows, cols, p.sf_layout)
     sf = torch.empty(max(nsf, 16), dtype=torch.uint8, device=device)
-    s_dec = torch.empty(1, dtype=torch.float32, device=device)
+    # CTA-local NVFP4: one decode scale per 128-row stripe of the copy
+    n_sd = max(n_stripes(rows), 1) if p.format == FP4_FMT_NVFP4_CTA else 1
+    s_dec = torch.empty(n_sd, dtype=torch.float32, device=device)
     shift = None
     if with_shift:
         shift = torch.empty(max(rows, 1), dtype=torch.int8, device=device)
@@ -249,6 +266,18 @@ def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
     a = torch.empty(1, dtype=torch.float32, device=x.device)
     b = torch.empty(1, dtype=torch.float32, device=x.device)
     _check(fp4_amax(x, hadamard_n, hadamard_signs, a, b, stream), "fp4_amax")
+    return a, b
+
+
+def amax_stripes(x, stream=None):
+    """Stripe maxima for the CTA-local NVFP4 contract: (per 128-row stripe,
+    per 128-column stripe) device float32 tensors."""
+    if not x.is_contiguous():
+        raise ValueError("amax_stripes: x must be contiguous")
+    rows, cols = x.shape
+    a = torch.empty(max(n_stripes(rows), 1), dtype=torch.float32, device=x.device)
+    b = torch.empty(max(n_stripes(cols), 1), dtype=torch.float32, device=x.device)
+    _check(fp4_amax_stripes(x, a, b, stream), "fp4_amax_stripes")
     return a, b
 
 

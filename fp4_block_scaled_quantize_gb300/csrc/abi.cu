@@ -36,8 +36,10 @@ namespace {
 
 bool valid_format(int32_t f) {
   return f == FP4_FMT_UE5M3_B16 || f == FP4_FMT_NVFP4_B16 || f == FP4_FMT_MXFP4_B32 ||
-         f == FP4_FMT_UE5M3_B32;
+         f == FP4_FMT_UE5M3_B32 || f == FP4_FMT_NVFP4_CTA;
 }
+// The kernels' format: CTA-local NVFP4 is NVFP4 with per-stripe tensor scales.
+int kernel_format(int32_t f) { return f == FP4_FMT_NVFP4_CTA ? FP4_FMT_NVFP4_B16 : f; }
 bool valid_round(int32_t r) { return r == FP4_ROUND_RNE || r == FP4_ROUND_SR; }
 bool valid_layout(int32_t l) { return l == FP4_SF_PLAIN || l == FP4_SF_MMA; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -56,6 +58,7 @@ fp4_status check_params(const fp4_quant_params *p) {
   if (p->block2d && (p->round_row != FP4_ROUND_RNE || p->round_col != FP4_ROUND_RNE || p->hadamard_n))
     return FP4_ERR_UNSUPPORTED;
   if (p->block2d && p->T_col != 0.0f && p->T_col != p->T) return FP4_ERR_UNSUPPORTED;
+  if (p->format == FP4_FMT_NVFP4_CTA && (p->block2d || p->hadamard_n)) return FP4_ERR_UNSUPPORTED;
   return FP4_OK;
 }
 
@@ -84,6 +87,17 @@ fp4_status fp4_amax(const void *x_bf16, int64_t rows, int64_t cols, int32_t hada
     return FP4_ERR_ALIGNMENT;
   return launch_amax(x_bf16, rows, cols, hadamard_n, hadamard_signs, amax_row_dev, amax_col_dev,
                      as_stream(stream));
+}
+
+fp4_status fp4_amax_stripes(const void *x_bf16, int64_t rows, int64_t cols,
+                            float *amax_rows_dev, float *amax_cols_dev, void *stream) {
+  if (rows < 0 || cols < 0 || !amax_rows_dev) return FP4_ERR_INVALID_ARG;
+  if (rows * cols > 0 && !x_bf16) return FP4_ERR_INVALID_ARG;
+  if (cols % 8 != 0) return FP4_ERR_SHAPE;
+  if ((x_bf16 && !aligned16(x_bf16)) || !aligned4(amax_rows_dev) ||
+      (amax_cols_dev && !aligned4(amax_cols_dev)))
+    return FP4_ERR_ALIGNMENT;
+  return launch_amax_stripes(x_bf16, rows, cols, amax_rows_dev, amax_cols_dev, as_stream(stream));
 }
 
 fp4_status fp4_amax_many(const fp4_amax_job *jobs, int32_t n, void *stream) {
@@ -171,7 +185,8 @@ fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const fl
   j.amax_row = amax_dev;
   j.T = p->T;
   j.T_col = p->T;
-  j.fmt = p->format;
+  j.fmt = kernel_format(p->format);
+  j.stripes = p->format == FP4_FMT_NVFP4_CTA;
   j.block2d = p->block2d;
   j.had_n = 0;
   j.sr_row = p->round_row == FP4_ROUND_SR;
@@ -194,7 +209,7 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   fp4_status st = check_params(p);
   if (st != FP4_OK) return st;
   if (rows < 0 || cols < 0 || !amax_row_dev || !s_dec_row || !s_dec_col) return FP4_ERR_INVALID_ARG;
-  if (p->hadamard_n && !amax_col_dev) return FP4_ERR_INVALID_ARG;
+  if ((p->hadamard_n || p->format == FP4_FMT_NVFP4_CTA) && !amax_col_dev) return FP4_ERR_INVALID_ARG;
   const int B = block_of(p->format);
   const bool empty = rows == 0 || cols == 0;
   if (!empty && (!x_bf16 || !q_row || !sf_row || !q_col || !sf_col)) return FP4_ERR_INVALID_ARG;
@@ -216,7 +231,8 @@ fp4_status fp4_quantize_transpose(const void *x_bf16, int64_t rows, int64_t cols
   j.amax_col = p->block2d ? amax_row_dev : (amax_col_dev ? amax_col_dev : amax_row_dev);
   j.T = p->T;
   j.T_col = p->T_col != 0.0f ? p->T_col : p->T;
-  j.fmt = p->format;
+  j.fmt = kernel_format(p->format);
+  j.stripes = p->format == FP4_FMT_NVFP4_CTA;
   j.block2d = p->block2d;
   j.had_n = p->hadamard_n;
   j.signs = p->hadamard_signs;
@@ -258,7 +274,8 @@ fp4_status gemm_operands(const fp4_operand *A, const fp4_operand *B, int64_t M, 
   j.sdb = B->s_dec;
   j.sha = is_ue5m3_fmt(A->format) ? A->row_shift : nullptr;
   j.shb = is_ue5m3_fmt(B->format) ? B->row_shift : nullptr;
-  j.fmt = A->format;
+  j.fmt = kernel_format(A->format);
+  j.stripes = A->format == FP4_FMT_NVFP4_CTA;
   j.M = M;
   j.N = N;
   j.K = K;
@@ -293,7 +310,8 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64
   j.M = M;
   j.N = N;
   j.K = K;
-  j.fmt = A->format;
+  j.fmt = kernel_format(A->format);
+  j.stripes = A->format == FP4_FMT_NVFP4_CTA;
   j.D = D;
   j.d_bf16 = d_is_bf16 != 0;
   j.canon = canonicalize_1024 != 0;
@@ -310,6 +328,7 @@ fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t
   if (st != FP4_OK) return st;
   if (p->block2d || p->hadamard_n || p->round_col != FP4_ROUND_RNE) return FP4_ERR_UNSUPPORTED;
   if (p->format == FP4_FMT_UE5M3_B32) return FP4_ERR_UNSUPPORTED;  // fused path: block 16 / MX
+  if (p->format == FP4_FMT_NVFP4_CTA) return FP4_ERR_UNSUPPORTED;   // an output stripe spans all N
   if (row_shift && !(is_ue5m3_fmt(p->format) && p->sf_layout == FP4_SF_MMA))
     return FP4_ERR_UNSUPPORTED;
   if (K == 0 || N % block_of(p->format) != 0) return FP4_ERR_SHAPE;

@@ -15,6 +15,13 @@
 // plain tensors can share one launch (CTAs split among them in proportion
 // to their sizes).
 //
+// Stripe variant (CTA-local NVFP4, "Format-Aware Fusion for Fast FP4
+// Pretraining", Abstract; reading: one tensor scale per 128-row stripe of
+// each copy): the maxima of every 128-row stripe and every 128-column stripe
+// of x from one read.  A CTA walks 128 x 128 tiles (eight 16-byte loads in
+// flight per thread); each warp folds its tile maximum into the tile's row
+// stripe and column stripe with one atomicMax each.
+//
 // Hadamard variant ("Technical summary: LLM pretraining with MXFP4",
 // Findings: deterministic H16/H32 on the weight-gradient operand): the amax
 // of the transposed copy after rotating every n consecutive rows of each
@@ -167,6 +174,40 @@ __global__ void __launch_bounds__(kThreads) k_amax_hadamard(const uint32_t *__re
   block_max_to(m_rot, out_col, nullptr, status);
 }
 
+constexpr int kStripe = 128;
+
+__global__ void __launch_bounds__(kThreads) k_amax_stripes(const uint16_t *__restrict__ x,
+                                                           int64_t rows, int64_t cols,
+                                                           float *out_rows, float *out_cols,
+                                                           uint32_t *status) {
+  const int64_t tr = (rows + kStripe - 1) / kStripe, tc = (cols + kStripe - 1) / kStripe;
+  const int chunk = threadIdx.x & 15;  // 16-byte chunk of a tile row
+  const int row0 = threadIdx.x >> 4;   // rows row0, row0 + 16, ... of the tile
+  for (int64_t t = blockIdx.x; t < tr * tc; t += gridDim.x) {
+    const int64_t R0 = (t / tc) * kStripe, C0 = (t % tc) * kStripe;
+    const int64_t c = C0 + 8 * chunk;
+    uint32_t m = 0;
+    if (c < cols) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t r = R0 + row0 + 16 * i;
+        v[i] = r < rows ? __ldg(reinterpret_cast<const uint4 *>(x + r * cols + c))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        m = max(m, max(max(mag2(v[i].x), mag2(v[i].y)), max(mag2(v[i].z), mag2(v[i].w))));
+    }
+    m = warp_max(m << 16);
+    if ((threadIdx.x & 31) == 0) {
+      if (m >= 0x7F800000u) raise_status(status, kStatusNonfinite);
+      atomicMax(reinterpret_cast<unsigned int *>(out_rows + R0 / kStripe), m);
+      if (out_cols) atomicMax(reinterpret_cast<unsigned int *>(out_cols + C0 / kStripe), m);
+    }
+  }
+}
+
 int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -217,6 +258,23 @@ fp4_status launch_amax(const void *x, int64_t rows, int64_t cols, int had_n, uin
                              amax_row, amax_col, status);
   return launch_after_zero(z, k_amax_hadamard<32>, grid_for(items), s, xw, rows, cols, signs,
                            amax_row, amax_col, status);
+}
+
+fp4_status launch_amax_stripes(const void *x, int64_t rows, int64_t cols, float *amax_rows,
+                               float *amax_cols, cudaStream_t s) {
+  uint32_t *status = status_word();
+  if (!status) return FP4_ERR_CUDA;
+  const int64_t nr = ceil_div(rows, kStripe), nc = ceil_div(cols, kStripe);
+  if (nr && cudaMemsetAsync(amax_rows, 0, (size_t)nr * sizeof(float), s) != cudaSuccess)
+    return FP4_ERR_CUDA;
+  if (amax_cols && nc && cudaMemsetAsync(amax_cols, 0, (size_t)nc * sizeof(float), s) != cudaSuccess)
+    return FP4_ERR_CUDA;
+  if (nr == 0 || nc == 0) return FP4_OK;
+  const int64_t tiles = nr * nc;
+  const int64_t cap = (int64_t)sm_count() * 4;
+  k_amax_stripes<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(
+      static_cast<const uint16_t *>(x), rows, cols, amax_rows, amax_cols, status);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 fp4_status launch_amax_many(const void *const *x, const int64_t *n_elems, float *const *amax, int n,

@@ -56,7 +56,8 @@ inline bool aligned16(const void *p) {
 
 inline int block_of(int32_t fmt) {
   if (fmt == FP4_FMT_MXFP4_B32 || fmt == FP4_FMT_UE5M3_B32) return 32;
-  return (fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_NVFP4_B16) ? 16 : -1;
+  return (fmt == FP4_FMT_UE5M3_B16 || fmt == FP4_FMT_NVFP4_B16 || fmt == FP4_FMT_NVFP4_CTA) ? 16
+                                                                                            : -1;
 }
 // UE5M3 scales (block 16 or 32): row shifts onto the tensor core's E4M3 path.
 inline bool is_ue5m3_fmt(int32_t fmt) {
@@ -75,6 +76,9 @@ fp4_status launch_mxfp4_to_fp8(const uint8_t *q, const uint8_t *sf, int64_t rows
 fp4_status launch_mxfp4_to_fp8_t(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
                                  uint8_t *q8t, float *s8t, cudaStream_t s);
 
+// Stripe maxima (128 rows / 128 columns) of one BF16 tensor.
+fp4_status launch_amax_stripes(const void *x, int64_t rows, int64_t cols, float *amax_rows,
+                               float *amax_cols, cudaStream_t s);
 // Plain amax of n <= FP4_AMAX_MAX_JOBS BF16 tensors (n_elems[k] % 8 == 0)
 // in one launch.
 fp4_status launch_amax_many(const void *const *x, const int64_t *n_elems, float *const *amax, int n,
@@ -91,6 +95,7 @@ struct QuantJob {
   uint64_t seed;
   uint32_t offset;
   int sf_mma;
+  int stripes;  // NVFP4 with one tensor scale per 128-row stripe of each copy
   uint8_t *q_row, *sf_row;
   float *s_dec_row;
   int8_t *shift_row;
@@ -117,6 +122,7 @@ struct GemmJob {
   const float *sda, *sdb;
   const int8_t *sha, *shb;
   int fmt;
+  int stripes;  // sda / sdb hold one decode scale per 128-row stripe
   int64_t M, N, K;
   void *D;
   int d_bf16, canon;

@@ -93,6 +93,7 @@ struct Params {
   const uint8_t *sfa, *sfb;
   const float *s8a, *s8b;  // FP8: binary32 scales [rows][K / 128]
   int64_t kb8;             // FP8: scale columns per row
+  int stripes;             // sda / sdb: one decode scale per 128-row stripe
   int fp8_tma_scales;      // FP8: scales by tensor TMA (K % 512 == 0, 16-byte aligned)
   const float *sda, *sdb;
   const int8_t *sha, *shb;
@@ -572,7 +573,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quad = warp & 3;
     const int half = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
-    const float alpha = (FMT == kFP8) ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    // alpha: one per GEMM, or per (A stripe, B stripe) of 128 rows each
+    float alpha = (FMT == kFP8 || p.stripes) ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     float se_o = 1.0f, sd_o = 1.0f;  // tensor scale of the fused output copy
     if (QOUT) {
       tensor_scale_rt(p.fmt_out, __ldg(p.amax_out), p.T_out, se_o, sd_o);
@@ -604,6 +606,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
       const int64_t m = (int64_t)mt * BM + row_in_tile;
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
+      if (p.stripes) {  // this warp's rows: A stripe mt; its 128 columns: B stripe 2 nt + half
+        const int64_t sb = min((int64_t)nt * 2 + half, (p.N + 127) / 128 - 1);
+        alpha = __fmul_rn(__ldg(p.sda + mt), __ldg(p.sdb + sb));
+      }
       // Output: each lane's row segment of 32 values is exchanged within its
       // group of four lanes so that every store instruction writes eight
       // 64-byte row pieces instead of 32 scattered 16-byte pieces.
@@ -845,6 +851,7 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   p.sfb = j.sfb;
   p.sda = j.sda;
   p.sdb = j.sdb;
+  p.stripes = j.stripes;
   p.sha = j.sha;
   p.shb = j.shb;
   p.D = j.D;

@@ -97,6 +97,7 @@ struct Params {
   int n_fast;
   int64_t cp4;              // scale tiles per 128-row group (both operands)
   int64_t ngrp_a, ngrp_b;   // 128-row groups of A and of B
+  int stripes;              // sda / sdb: one decode scale per 128-row stripe
   int d_bf16, canon;
   int stall_producer;
   uint32_t *status;
@@ -469,7 +470,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int quad = warp & 3;
     const int half = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
-    const float alpha = __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
+    // alpha: one per GEMM, or per (A stripe, B stripe) of 128 rows each
+    float alpha = p.stripes ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     const uint32_t acc_empty_leader = map_to_rank(acc_empty, 0u);
     auto load_shifts = [&](int64_t n0, uint32_t(&sh)[8]) {
 #pragma unroll
@@ -497,6 +499,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
       const int64_t m_row0 = (int64_t)mt * PAIR_M + (int64_t)rank * HALF;
       const int64_t m = m_row0 + row_in_tile;
+      if (p.stripes) {  // this CTA's rows: A stripe m_row0 / 128; its columns: B stripe 2 nt + half
+        const int64_t sa_i = min(m_row0 / 128, (p.M + 127) / 128 - 1);
+        const int64_t sb_i = min((int64_t)nt * 2 + half, (p.N + 127) / 128 - 1);
+        alpha = __fmul_rn(__ldg(p.sda + sa_i), __ldg(p.sdb + sb_i));
+      }
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
       const int k4 = lane & 3;
       const int64_t grp_m = m_row0 + quad * 32 + (lane & ~3);
@@ -615,6 +622,7 @@ fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s) {
   p.sfb = j.sfb;
   p.sda = j.sda;
   p.sdb = j.sdb;
+  p.stripes = j.stripes;
   p.sha = j.sha;
   p.shb = j.shb;
   p.D = j.D;

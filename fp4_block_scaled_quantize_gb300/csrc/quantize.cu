@@ -59,6 +59,7 @@ struct Params {
   uint8_t *q_col, *sf_col;
   float *s_dec_col;
   int do_row, do_col, sr_row, sr_col, sf_mma;
+  int stripes;  // one tensor scale per 128-row stripe of each copy (NVFP4)
   uint32_t *status;
   uint64_t seed;
   uint32_t offset, signs;
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     se_c = se_r;
     sd_c = sd_r;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blockIdx.x == 0 && threadIdx.x == 0 && !p.stripes) {
     if (p.do_row) *p.s_dec_row = sd_r;
     if (p.do_col) *p.s_dec_col = sd_c;
   }
@@ -243,6 +244,23 @@ __global__ void __launch_bounds__(kThreads, 4)
   uint32_t phase[2] = {0u, 0u};
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
   const int64_t R0 = (tile / p.tiles_c) * kTile, C0 = (tile % p.tiles_c) * kTile;
+  if (FMT == kNVFP4 && p.stripes) {
+    // CTA-local NVFP4: the tile's row-wise blocks belong to row stripe
+    // R0 / 128 and its transposed blocks to column stripe C0 / 128 (tiles
+    // and stripes are both 128 wide).  Every use of the previous tile's
+    // tables ended before its mid-tile barrier; the barrier after the tile
+    // wait below publishes the new ones.
+    tensor_scale<FMT>(__ldg(p.amax_row + R0 / kTile), p.T, se_r, sd_r);
+    if (p.do_col) tensor_scale<FMT>(__ldg(p.amax_col + C0 / kTile), p.T_col, se_c, sd_c);
+    mtab_r[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_r);
+    mtab_c[threadIdx.x] = mult_of_code<FMT>(threadIdx.x, sd_c);
+    if (threadIdx.x < 128) ctab_r[threadIdx.x] = code_tab_entry<FMT>(threadIdx.x, se_r);
+    else ctab_c[threadIdx.x - 128] = code_tab_entry<FMT>(threadIdx.x - 128, se_c);
+    if (threadIdx.x == 0) {
+      if (p.do_row && C0 == 0) p.s_dec_row[R0 / kTile] = sd_r;
+      if (p.do_col && R0 == 0) p.s_dec_col[C0 / kTile] = sd_c;
+    }
+  }
   // The other buffer was last read in the previous iteration, which ended at
   // a barrier: the next tile can stream into it now.
   if (!mbar_wait_q(bar_a[buf], phase[buf])) tfail = 1;
@@ -688,11 +706,13 @@ fp4_status launch_quantize(const QuantJob &j, cudaStream_t s) {
   p.sr_row = j.sr_row;
   p.sr_col = j.sr_col;
   p.sf_mma = j.sf_mma;
+  p.stripes = j.stripes;
   p.seed = j.seed;
   p.status = status_word();
   if (!p.status) return FP4_ERR_CUDA;
   p.offset = j.offset;
   p.signs = j.signs;
+  if (j.stripes && (j.R == 0 || j.C == 0)) return FP4_OK;  // no stripe holds data
   if (j.R == 0 || j.C == 0) {
     float *sdr = j.s_dec_row;
     float *sdc = j.s_dec_col;

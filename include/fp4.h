@@ -66,12 +66,22 @@ typedef enum {
  *              UE5M3 recipe ([UE5M3] Approach).  In the MMA layout its
  *              scales are stored duplicated per 16-element half (the
  *              block-16 tiling, E4M3 images after the remap), so the tensor
- *              core consumes it through the block-16 path. */
+ *              core consumes it through the block-16 path;
+ *   NVFP4_CTA: CTA-local NVFP4 ([FAF] Abstract names the scale contract):
+ *              NVFP4_B16 with one tensor scale per 128-row stripe of each
+ *              copy instead of one per tensor.  Stripe i of a copy (its rows
+ *              128i .. 128i+127, the last stripe possibly shorter) uses
+ *              s_enc_i, s_dec_i from its own amax (fp4_amax_stripes); every
+ *              amax_*_dev and s_dec_* argument of the producers, and an
+ *              operand's s_dec, then points to one float per stripe.  No 2D
+ *              tiles, no Hadamard view, not an output format of
+ *              fp4_gemm_quantize (FP4_ERR_UNSUPPORTED). */
 typedef enum {
   FP4_FMT_UE5M3_B16 = 0,
   FP4_FMT_NVFP4_B16 = 1,
   FP4_FMT_MXFP4_B32 = 2,
-  FP4_FMT_UE5M3_B32 = 3
+  FP4_FMT_UE5M3_B32 = 3,
+  FP4_FMT_NVFP4_CTA = 4
 } fp4_format;
 
 typedef enum { FP4_ROUND_RNE = 0, FP4_ROUND_SR = 1 } fp4_rounding;
@@ -109,7 +119,8 @@ typedef struct {
   const uint8_t *q;         /* [rows][k/2] payload                          */
   const uint8_t *sf;        /* MMA-layout scales: E4M3 (NVFP4, and UE5M3
                                after remap), E8M0 (MXFP4)                   */
-  const float *s_dec;       /* device: per-tensor decode scale (1 for MX)   */
+  const float *s_dec;       /* device: per-tensor decode scale (1 for MX);
+                               NVFP4_CTA: one per 128-row stripe            */
   const int8_t *row_shift;  /* device, UE5M3 only: [rows] power-of-two
                                exponents from the remap; NULL otherwise     */
   int32_t format;           /* fp4_format                                   */
@@ -129,6 +140,17 @@ typedef struct {
 fp4_status fp4_amax(const void *x_bf16, int64_t rows, int64_t cols,
                     int32_t hadamard_n, uint32_t hadamard_signs,
                     float *amax_row_dev, float *amax_col_dev, void *stream);
+
+/* Stripe maxima for the CTA-local NVFP4 contract ([FAF] Abstract; reading:
+ * one tensor scale per 128-row stripe of each copy).  amax_rows_dev[i] =
+ * max |x| over rows 128i .. 128i+127 of x (the row-wise copy's stripes),
+ * amax_cols_dev[j] = max |x| over columns 128j .. 128j+127 (the transposed
+ * copy's stripes), exact, from one read of x; ceil(rows/128) and
+ * ceil(cols/128) floats.  amax_cols_dev may be NULL.  Inf/NaN sets
+ * FP4_ERR_NONFINITE.  rows == 0 or cols == 0 writes zeros to the existing
+ * stripes.  Shapes: cols % 8 == 0.  Alignment: x 16 bytes, outputs 4. */
+fp4_status fp4_amax_stripes(const void *x_bf16, int64_t rows, int64_t cols,
+                            float *amax_rows_dev, float *amax_cols_dev, void *stream);
 
 /* Plain amax (hadamard_n == 0 above) of several BF16 tensors in one launch
  * ([UE5M3] Approach: on a refresh step every operand's amax cache is
