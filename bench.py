@@ -1117,6 +1117,10 @@ def run_profile(args, local):
         "dgrad": lambda: fq.gemm(layer.dyr, layer.wc, out=layer.dX),
         "wgrad": lambda: fq.gemm(layer.dyc, layer.xc, out=layer.dW),
     }
+    if args.profile == "amax_stripes":
+        ar = torch.empty(fq.n_stripes(M_TOK), dtype=torch.float32, device=layer.X.device)
+        ac = torch.empty(fq.n_stripes(K_FF), dtype=torch.float32, device=layer.X.device)
+        ops["amax_stripes"] = lambda: fq._check(fq.fp4_amax_stripes(layer.X, ar, ac), "stripes")
     if args.profile.startswith("fp8_"):
         # the step's operands as FP8 copies (MXFP4-b32 re-encoded), one GEMM
         p = fq.params(format=fq.FP4_FMT_MXFP4_B32, sf_layout=fq.FP4_SF_PLAIN)
@@ -1161,7 +1165,8 @@ def main():
                     help="launch the timed steps kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", default=None,
                     choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad",
-                             "reencode", "reencode_t", "fp8_fprop", "fp8_dgrad", "fp8_wgrad"],
+                             "reencode", "reencode_t", "fp8_fprop", "fp8_dgrad", "fp8_wgrad",
+                             "amax_stripes"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

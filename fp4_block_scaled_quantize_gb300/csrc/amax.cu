@@ -18,9 +18,10 @@
 // Stripe variant (CTA-local NVFP4, "Format-Aware Fusion for Fast FP4
 // Pretraining", Abstract; reading: one tensor scale per 128-row stripe of
 // each copy): the maxima of every 128-row stripe and every 128-column stripe
-// of x from one read.  A CTA walks 128 x 128 tiles (eight 16-byte loads in
-// flight per thread); each warp folds its tile maximum into the tile's row
-// stripe and column stripe with one atomicMax each.
+// of x from one read.  A CTA walks a contiguous run of 128 x 128 tiles in
+// row-major order (eight 16-byte loads in flight per thread); a tile's
+// maximum goes to its column stripe with one atomicMax, and the run's maximum
+// per row stripe with one atomicMax when the run leaves the stripe.
 //
 // Hadamard variant ("Technical summary: LLM pretraining with MXFP4",
 // Findings: deterministic H16/H32 on the weight-gradient operand): the amax
@@ -176,14 +177,21 @@ __global__ void __launch_bounds__(kThreads) k_amax_hadamard(const uint32_t *__re
 
 constexpr int kStripe = 128;
 
-__global__ void __launch_bounds__(kThreads) k_amax_stripes(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kThreads, 8) k_amax_stripes(const uint16_t *__restrict__ x,
                                                            int64_t rows, int64_t cols,
                                                            float *out_rows, float *out_cols,
                                                            uint32_t *status) {
+  __shared__ uint32_t red[2][kThreads / 32];
   const int64_t tr = (rows + kStripe - 1) / kStripe, tc = (cols + kStripe - 1) / kStripe;
+  const int64_t ntiles = tr * tc;
+  // a contiguous run of tiles in row-major order per CTA: the row stripe's
+  // maximum is carried across the run and published when the run leaves it
+  const int64_t per = (ntiles + gridDim.x - 1) / gridDim.x;
+  const int64_t t0 = blockIdx.x * per, t1 = min(ntiles, t0 + per);
   const int chunk = threadIdx.x & 15;  // 16-byte chunk of a tile row
   const int row0 = threadIdx.x >> 4;   // rows row0, row0 + 16, ... of the tile
-  for (int64_t t = blockIdx.x; t < tr * tc; t += gridDim.x) {
+  uint32_t run = 0;                    // thread 0: max of the run's current row stripe
+  for (int64_t t = t0; t < t1; ++t) {
     const int64_t R0 = (t / tc) * kStripe, C0 = (t % tc) * kStripe;
     const int64_t c = C0 + 8 * chunk;
     uint32_t m = 0;
@@ -200,10 +208,20 @@ __global__ void __launch_bounds__(kThreads) k_amax_stripes(const uint16_t *__res
         m = max(m, max(max(mag2(v[i].x), mag2(v[i].y)), max(mag2(v[i].z), mag2(v[i].w))));
     }
     m = warp_max(m << 16);
-    if ((threadIdx.x & 31) == 0) {
-      if (m >= 0x7F800000u) raise_status(status, kStatusNonfinite);
-      atomicMax(reinterpret_cast<unsigned int *>(out_rows + R0 / kStripe), m);
-      if (out_cols) atomicMax(reinterpret_cast<unsigned int *>(out_cols + C0 / kStripe), m);
+    uint32_t *slot = red[t & 1];  // alternating slots: one barrier per tile
+    if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t w = slot[0];
+#pragma unroll
+      for (int k = 1; k < kThreads / 32; ++k) w = max(w, slot[k]);
+      if (w >= 0x7F800000u) raise_status(status, kStatusNonfinite);
+      if (out_cols) atomicMax(reinterpret_cast<unsigned int *>(out_cols + C0 / kStripe), w);
+      run = max(run, w);
+      if (t + 1 == t1 || (t + 1) / tc != t / tc) {
+        atomicMax(reinterpret_cast<unsigned int *>(out_rows + R0 / kStripe), run);
+        run = 0;
+      }
     }
   }
 }
@@ -270,8 +288,10 @@ fp4_status launch_amax_stripes(const void *x, int64_t rows, int64_t cols, float 
   if (amax_cols && nc && cudaMemsetAsync(amax_cols, 0, (size_t)nc * sizeof(float), s) != cudaSuccess)
     return FP4_ERR_CUDA;
   if (nr == 0 || nc == 0) return FP4_OK;
+  // eight resident CTAs per SM: each warp has one tile's eight 16-byte loads
+  // in flight at a time, so residency is what hides the memory latency
   const int64_t tiles = nr * nc;
-  const int64_t cap = (int64_t)sm_count() * 4;
+  const int64_t cap = (int64_t)sm_count() * 8;
   k_amax_stripes<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, 0, s>>>(
       static_cast<const uint16_t *>(x), rows, cols, amax_rows, amax_cols, status);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
