@@ -146,7 +146,12 @@ struct Fp8GemmJob {
   int d_bf16;
 };
 fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s);
-// Plain GEMM on SM pairs (tcgen05 cta_group::2); K > 0, no fused output.
+// GEMM on SM pairs (tcgen05 cta_group::2); K > 0, M > 128, with or without
+// the fused output producer.
 fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s);
+// Fused-output parameters of a job (and the zeroing of tensor-core scale
+// padding); defined in gemm.cu.
+struct QoutParams;
+fp4_status qout_params(const GemmJob &j, QoutParams &o, cudaStream_t s);
 
 }  // namespace fp4

@@ -60,6 +60,7 @@
 
 #include "common.cuh"
 #include "formats.cuh"
+#include "qout.cuh"
 #include "tcgen05.cuh"
 
 namespace fp4 {
@@ -106,15 +107,7 @@ struct Params {
   int d_bf16, canon;
   int stall_producer;  // test switch: the producer never arrives (waits run out)
   uint32_t *status;
-  // fused row-wise quantisation of the output (q_out != nullptr)
-  uint8_t *q_out, *sf_out;
-  float *sd_out;
-  const float *amax_out;
-  float T_out;
-  int fmt_out, sr_out, sf_mma_out, qb_out;
-  int64_t cb_out, cp4_out;  // output scale columns; 512-byte tiles per 128 rows
-  uint64_t seed_out;
-  uint32_t offset_out;
+  QoutParams qo;  // fused row-wise quantisation of the output (QOUT)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -147,23 +140,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         : "memory");
   }
 }
-// Format chosen at run time (the fused epilogue quantiser).
-__device__ __forceinline__ void tensor_scale_rt(int fmt, float amax, float T, float &se,
-                                                float &sd) {
-  if (fmt == kMXFP4)
-    tensor_scale<kMXFP4>(amax, T, se, sd);
-  else if (fmt == kUE5M3)
-    tensor_scale<kUE5M3>(amax, T, se, sd);
-  else
-    tensor_scale<kNVFP4>(amax, T, se, sd);
-}
-__device__ __forceinline__ uint32_t block_scale_rt(int fmt, float b, float se, float sd,
-                                                   float &mult, bool &zp) {
-  if (fmt == kMXFP4) return block_scale<kMXFP4>(b, se, sd, mult, zp);
-  if (fmt == kUE5M3) return block_scale<kUE5M3>(b, se, sd, mult, zp);
-  return block_scale<kNVFP4>(b, se, sd, mult, zp);
-}
-
 // Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, K-major A and B,
 // M = 128, N = 256; scale type E4M3 (block 16) or E8M0 (block 32).
 // kind::mxf8f6f4 (kFP8): E4M3 x E4M3 (type code 0), E8M0 scales.
@@ -577,8 +553,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     float alpha = (FMT == kFP8 || p.stripes) ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     float se_o = 1.0f, sd_o = 1.0f;  // tensor scale of the fused output copy
     if (QOUT) {
-      tensor_scale_rt(p.fmt_out, __ldg(p.amax_out), p.T_out, se_o, sd_o);
-      if (blockIdx.x == 0 && threadIdx.x == 32 * (2 + SF_WARPS)) *p.sd_out = sd_o;
+      tensor_scale_rt(p.qo.fmt, __ldg(p.qo.amax), p.qo.T, se_o, sd_o);
+      if (blockIdx.x == 0 && threadIdx.x == 32 * (2 + SF_WARPS)) *p.qo.sd = sd_o;
     }
     // B row shifts (int8) of 32 output columns from n0, packed 4 per word;
     // N is a multiple of 8 and the array is 16-byte aligned.
@@ -615,83 +591,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // 64-byte row pieces instead of 32 scattered 16-byte pieces.
       const int k4 = lane & 3;
       const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
-      // Fused producer: the row-wise FP4 copy of this lane's 32 output values
-      // (one or two blocks along N) goes to qacc[q] / qcodes; flush_out()
-      // writes the lane's 128 columns once all four are encoded.
-      uint32_t qacc[16];        // payload: chunk q (16 bytes) = words 4q..4q+3
-      uint32_t qcodes[2];       // scale codes of the 128 columns, 4 per word
-      auto quant_out = [&](int q, int64_t n0, const float(&y)[32]) {
-        const int nb = 32 / p.qb_out;
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          if (blk >= nb) break;
-          uint32_t code = 0u;
-          const int QB = p.qb_out, o = blk * QB;
-          if (n0 + o < p.N) {
-            float b = 0.0f;
-            for (int j = 0; j < QB; ++j) b = fmaxf(b, fabsf(y[o + j]));
-            float mult;
-            bool zp;
-            code = block_scale_rt(p.fmt_out, b, se_o, sd_o, mult, zp);
-            // 8 values at a time; under SR one Philox block covers 16
-            // elements of the output row (words x, y for the first 8)
-            uint4 rw = make_uint4(0u, 0u, 0u, 0u);
-            for (int h = 0; h < QB / 8; ++h) {
-              float v[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) v[j] = y[o + 8 * h + j];
-              scale8(v, mult, zp);
-              if (p.sr_out) {
-                if ((h & 1) == 0)
-                  rw = sr_words16(p.seed_out, p.offset_out, 0u,
-                                  ((uint64_t)m * (uint64_t)p.N + (uint64_t)(n0 + o + 8 * h)) >> 4);
-                qacc[4 * q + 2 * blk + h] =
-                    (h & 1) ? e2m1x8_sr(v, rw.z, rw.w) : e2m1x8_sr(v, rw.x, rw.y);
-              } else {
-                qacc[4 * q + 2 * blk + h] = e2m1x8_hw(v);
-              }
-            }
-          }
-          // code of scale column (q * nb + blk) of this lane's 128 columns
-          const int c = q * nb + blk;
-          qcodes[c >> 2] |= code << (8 * (c & 3));
-        }
-      };
-      auto flush_out = [&](int64_t nbase) {
-        // payload: four lanes exchange their 16-byte chunks so each store
-        // instruction writes eight 64-byte row pieces
-        transpose4x16B(qacc, k4);
-        const int64_t n = nbase + 32 * k4;
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int64_t mm = grp_m + rr;
-          if (mm >= p.M || n >= p.N) continue;
-          uint8_t *dst = p.q_out + mm * (p.N / 2) + n / 2;  // 8-byte aligned (N % 16 == 0)
-          if (n + 32 <= p.N && (p.N & 31) == 0) {
-            *reinterpret_cast<uint4 *>(dst) =
-                make_uint4(qacc[4 * rr], qacc[4 * rr + 1], qacc[4 * rr + 2], qacc[4 * rr + 3]);
-          } else {
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(qacc[4 * rr], qacc[4 * rr + 1]);
-            if (n + 32 <= p.N)
-              *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(qacc[4 * rr + 2], qacc[4 * rr + 3]);
-          }
-        }
-        if (m >= p.M) return;
-        const int ncodes = 128 / p.qb_out;
-        const int64_t c0 = nbase / p.qb_out;
-        for (int wd = 0; wd < ncodes / 4; ++wd) {
-          const int64_t col = c0 + 4 * wd;  // first of four scale columns
-          if (col >= p.cb_out) break;
-          if (p.sf_mma_out) {
-            const int64_t off = ((m >> 7) * p.cp4_out + (col >> 2)) * 512 + (m & 31) * 16 +
-                                ((m >> 5) & 3) * 4;
-            *reinterpret_cast<uint32_t *>(p.sf_out + off) = qcodes[wd];
-          } else {
-            for (int c = 0; c < 4 && col + c < p.cb_out; ++c)
-              p.sf_out[m * p.cb_out + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
-          }
-        }
-      };
+      // Fused producer: the row-wise FP4 copy of this lane's 128 output
+      // columns (qout.cuh), written once all four chunks are encoded.
+      QoutLane ql;
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform
@@ -707,7 +609,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           y[j] = __fmul_rn(v, alpha);
         }
         if (QOUT) {
-          quant_out(q, n0, y);
+          ql.quant(p.qo, p.N, m, q, n0, y, se_o, sd_o);
           return;
         }
         if (p.d_bf16) {
@@ -751,18 +653,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(acc_empty);
       acc_phase ^= 1u;
-      if (QOUT) {
-        qcodes[0] = qcodes[1] = 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qacc[i] = 0u;
-      }
+      if (QOUT) ql.reset();
       emit(0, acc[0], sh0);
       emit(1, acc[1], sh1);
       load_shifts(nbase + 64, sh0);
       load_shifts(nbase + 96, sh1);
       emit(2, acc[2], sh0);
       emit(3, acc[3], sh1);
-      if (QOUT && nbase < p.N) flush_out(nbase);
+      if (QOUT && nbase < p.N) ql.flush(p.qo, p.M, p.N, m, grp_m, k4, nbase);
     }
   }
   tc_fence_before();
@@ -790,6 +688,27 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const CUtens
 }
 
 }  // namespace
+
+fp4_status qout_params(const GemmJob &j, QoutParams &o, cudaStream_t s) {
+  o.q = j.q_out;
+  o.sf = j.sf_out;
+  o.sd = j.sd_out;
+  o.amax = j.amax_out;
+  o.T = j.T_out;
+  o.fmt = j.fmt_out;
+  o.sr = j.sr_out;
+  o.sf_mma = j.sf_mma_out;
+  o.seed = j.seed_out;
+  o.offset = j.offset_out;
+  o.qb = j.fmt_out == kMXFP4 ? 32 : 16;
+  o.cb = j.N / o.qb;
+  o.cp4 = ceil_div(o.cb, 4);
+  // tensor-core layout: padding rows and scale columns read as zero
+  if (j.sf_mma_out &&
+      cudaMemsetAsync(j.sf_out, 0, (size_t)(ceil_div(j.M, 128) * 128 * o.cp4 * 4), s) != cudaSuccess)
+    return FP4_ERR_CUDA;
+  return FP4_OK;
+}
 
 fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s) {
   const size_t elt = j.d_bf16 ? 2 : 4;
@@ -840,7 +759,7 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   }
   // More than one 128-row block of A: SM pairs with a 256 x 256 tile
   // (gemm2.cu) halve the operand bytes each SM loads per MMA.
-  if (!j.q_out && j.M > 128) return launch_gemm_pair(j, s);
+  if (j.M > 128) return launch_gemm_pair(j, s);
   uint32_t *status = status_word();
   if (!status) return FP4_ERR_CUDA;
   CUtensorMap ma, mb;
@@ -881,26 +800,7 @@ fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  if (j.q_out) {
-    p.q_out = j.q_out;
-    p.sf_out = j.sf_out;
-    p.sd_out = j.sd_out;
-    p.amax_out = j.amax_out;
-    p.T_out = j.T_out;
-    p.fmt_out = j.fmt_out;
-    p.sr_out = j.sr_out;
-    p.sf_mma_out = j.sf_mma_out;
-    p.seed_out = j.seed_out;
-    p.offset_out = j.offset_out;
-    p.qb_out = j.fmt_out == kMXFP4 ? 32 : 16;
-    p.cb_out = j.N / p.qb_out;
-    p.cp4_out = ceil_div(p.cb_out, 4);
-    // tensor-core layout: padding rows and scale columns read as zero
-    if (j.sf_mma_out &&
-        cudaMemsetAsync(j.sf_out, 0, (size_t)(ceil_div(j.M, 128) * 128 * p.cp4_out * 4), s) !=
-            cudaSuccess)
-      return FP4_ERR_CUDA;
-  }
+  if (j.q_out && qout_params(j, p.qo, s) != FP4_OK) return FP4_ERR_CUDA;
   fp4_status st;
   if (j.q_out)
     st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, true>(ma, mb, ma, mb, p, grid, s)

@@ -41,7 +41,9 @@
 //           commit multicast to both CTAs' empty barriers, and at the end of
 //           a tile to both CTAs' accumulator barriers;
 //   warps 6-13 epilogue (both CTAs): each CTA drains its own 128 x 256
-//           accumulator, releases it to the leader, then scales and stores.
+//           accumulator, releases it to the leader, then scales and stores
+//           (or, with the fused output producer, quantises each row's 128
+//           columns to their FP4 copy: qout.cuh).
 // Every wait is bounded (about one second); on expiry the CTA raises the
 // timeout status bit, marks both CTAs as aborting, drains what it issued and
 // leaves through the final cluster barrier, which keeps each CTA's shared and
@@ -56,6 +58,7 @@
 
 #include "common.cuh"
 #include "formats.cuh"
+#include "qout.cuh"
 #include "tcgen05.cuh"
 
 namespace fp4 {
@@ -101,6 +104,7 @@ struct Params {
   int d_bf16, canon;
   int stall_producer;
   uint32_t *status;
+  QoutParams qo;  // fused row-wise quantisation of the output (QOUT)
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -226,7 +230,7 @@ __device__ __forceinline__ uint32_t idesc_pair(uint32_t a_sf_id, uint32_t b_sf_i
   return d;
 }
 
-template <int FMT>
+template <int FMT, bool QOUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                 const Params p) {
@@ -473,6 +477,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // alpha: one per GEMM, or per (A stripe, B stripe) of 128 rows each
     float alpha = p.stripes ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
     const uint32_t acc_empty_leader = map_to_rank(acc_empty, 0u);
+    float se_o = 1.0f, sd_o = 1.0f;  // tensor scale of the fused output copy
+    if (QOUT) {
+      tensor_scale_rt(p.qo.fmt, __ldg(p.qo.amax), p.qo.T, se_o, sd_o);
+      if (blockIdx.x == 0 && threadIdx.x == 32 * (2 + SF_WARPS)) *p.qo.sd = sd_o;
+    }
     auto load_shifts = [&](int64_t n0, uint32_t(&sh)[8]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -507,6 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
       const int k4 = lane & 3;
       const int64_t grp_m = m_row0 + quad * 32 + (lane & ~3);
+      QoutLane ql;  // fused producer: this lane's 128 output columns of row m
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = nbase + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform
@@ -520,6 +530,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           if (p.canon) v = __fmul_rn(rintf(__fmul_rn(v, 1024.0f)), 0x1p-10f);
           y[j] = __fmul_rn(v, alpha);
+        }
+        if (QOUT) {
+          ql.quant(p.qo, p.N, m, q, n0, y, se_o, sd_o);
+          return;
         }
         if (p.d_bf16) {
           uint32_t w[16];
@@ -562,12 +576,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
       acc_phase ^= 1u;
+      if (QOUT) ql.reset();
       emit(0, acc[0], sh0);
       emit(1, acc[1], sh1);
       load_shifts(nbase + 64, sh0);
       load_shifts(nbase + 96, sh1);
       emit(2, acc[2], sh0);
       emit(3, acc[3], sh1);
+      if (QOUT && nbase < p.N) ql.flush(p.qo, p.M, p.N, m, grp_m, k4, nbase);
     }
   }
   tc_fence_before();
@@ -580,14 +596,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int FMT>
+template <int FMT, bool QOUT>
 fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params &p, int64_t tiles,
                       cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters[64] = {0};
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
@@ -599,18 +615,18 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT, QOUT>, &cfg) != cudaSuccess || n <= 0)
       return FP4_ERR_CUDA;
     max_clusters[dev] = n;
   }
   const int64_t nc = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
-  k_gemm_pair<FMT><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  k_gemm_pair<FMT, QOUT><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 }  // namespace
 
-// Plain GEMM (no fused output producer) on SM pairs; K > 0.
+// GEMM on SM pairs, with or without the fused output producer; K > 0.
 fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s) {
   uint32_t *status = status_word();
   if (!status) return FP4_ERR_CUDA;
@@ -644,8 +660,16 @@ fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s) {
   const char *stall = std::getenv("FP4_TEST_STALL_PRODUCER");
   p.stall_producer = (stall && stall[0] == '1') ? 1 : 0;
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-  return (j.fmt == kMXFP4) ? launch_fmt<kMXFP4>(ma, mb, p, tiles, s)
-                           : launch_fmt<kNVFP4>(ma, mb, p, tiles, s);
+  if (!j.q_out)
+    return (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, false>(ma, mb, p, tiles, s)
+                             : launch_fmt<kNVFP4, false>(ma, mb, p, tiles, s);
+  if (qout_params(j, p.qo, s) != FP4_OK) return FP4_ERR_CUDA;
+  const fp4_status st = (j.fmt == kMXFP4) ? launch_fmt<kMXFP4, true>(ma, mb, p, tiles, s)
+                                          : launch_fmt<kNVFP4, true>(ma, mb, p, tiles, s);
+  if (st != FP4_OK) return st;
+  if (j.fmt_out == kUE5M3 && j.sf_mma_out && j.shift_out)
+    return launch_remap_ue5m3(j.sf_out, j.q_out, j.M, j.N, j.shift_out, s);
+  return FP4_OK;
 }
 
 }  // namespace fp4
