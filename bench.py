@@ -984,7 +984,7 @@ def gemm_source_digest():
     another version of the kernel is stale."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemm.cu", "gemm2.cu", "tcgen05.cuh"):
+    for name in ("gemm.cu", "gemm2.cu", "tcgen05.cuh", "qout.cuh"):
         with open(os.path.join(ROOT, "fp4_block_scaled_quantize_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
