@@ -736,6 +736,8 @@ fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s) {
   p.n_fast = j.M >= j.N ? 1 : 0;
   p.d_bf16 = j.d_bf16;
   p.status = status;
+  const char *stall = std::getenv("FP4_TEST_STALL_PRODUCER");  // failure-detection test switch
+  p.stall_producer = (stall && stall[0] == '1') ? 1 : 0;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

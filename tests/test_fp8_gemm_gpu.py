@@ -130,3 +130,24 @@ def test_fp8_gemm_k0_writes_zeros():
     fq.fp8_gemm(q, s, qb, sb, out=y)
     assert fq.fp4_status_sync() == fq.FP4_OK
     assert torch.count_nonzero(y).item() == 0
+
+
+@pytest.mark.parametrize("K", [512, 384])
+def test_fp8_gemm_bounded_wait_reports_timeout_and_context_survives(monkeypatch, K):
+    """With the producer stalled by the test switch, every wait of the FP8
+    kernel (scales by TMA for K = 512, by the scale warps for K = 384) runs
+    out after about a second, fp4_status_sync reports FP4_ERR_TIMEOUT, and
+    the next GEMM on the same context is correct."""
+    need_gpu()
+    M, N = 128, 256
+    q8a, s8a = operand(M, K, seed=3)
+    q8b, s8b = operand(N, K, seed=4)
+    args = [torch.from_numpy(t).cuda() for t in (q8a, s8a, q8b, s8b)]
+    monkeypatch.setenv("FP4_TEST_STALL_PRODUCER", "1")
+    fq.fp8_gemm(*args)
+    assert fq.fp4_status_sync() == fq.FP4_ERR_TIMEOUT
+    monkeypatch.delenv("FP4_TEST_STALL_PRODUCER")
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    y = run(q8a, s8a, q8b, s8b, torch.float32)
+    mi, ni = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    check(y, q8a, s8a, q8b, s8b, mi.ravel(), ni.ravel(), torch.float32, "after timeout")
