@@ -108,13 +108,14 @@ def test_down_proj_8b_full_size(fmt):
         check(yg, oa, ob, fmt, K, mi, ni, name=f"{name} fmt{fmt}")
 
 
+@pytest.mark.parametrize("M,N,K", [(4096, 2048, 8192), (2048, 4096, 2048), (8192, 2048, 4096)])
 @pytest.mark.parametrize("fmt,had,signs", [(MX, 32, 0x5A5AF00F), (UE, 16, 0), (UE, 0, 0)])
-def test_sweep_wgrad_hadamard(fmt, had, signs):
+def test_sweep_wgrad_hadamard(fmt, had, signs, M, N, K):
     """Sweep operands (N(0,1), 1% x50, seed 7) with the rotation fused into
     the transposed copies of both wgrad operands; the rotation cancels in the
-    product, so the GEMM is checked against the model of the rotated copies."""
+    product, so the GEMM is checked against the model of the rotated copies.
+    Three sweep shapes (wgrad contracts over the inputs' K rows)."""
     need_gpu()
-    M, N, K = 4096, 2048, 8192  # wgrad: contraction over K rows of the inputs
     a = inputs.sweep_operand(K, M, seed=7)   # dY-like [K][M]
     b = inputs.sweep_operand(K, N, seed=8)   # X-like  [K][N]
     outs = []
