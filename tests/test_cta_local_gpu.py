@@ -174,3 +174,21 @@ def test_stripe_contract_rejects_2d_and_hadamard_and_fused_output():
     with pytest.raises(fq.FP4Error):
         fq.gemm_quantize(q, q, amax_y, fq.params(format=CTA, sf_layout=fq.FP4_SF_MMA))
     assert fq.fp4_status_sync() == fq.FP4_OK
+
+
+def test_stripe_empty_inputs():
+    """No rows or no columns: the stripe maxima that exist are zero, and the
+    producers write nothing (and succeed)."""
+    need_gpu()
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    a, b = fq.amax_stripes(x)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    assert torch.count_nonzero(b).item() == 0          # one column stripe, zeroed
+    x2 = torch.zeros((256, 0), dtype=torch.bfloat16, device="cuda")
+    a2, _ = fq.amax_stripes(x2)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    assert torch.count_nonzero(a2).item() == 0         # two row stripes, zeroed
+    p = fq.params(format=CTA, sf_layout=fq.FP4_SF_MMA)
+    fq.quantize(x, a, p)
+    fq.quantize_transpose(x2, a2, torch.zeros(1, device="cuda"), p)
+    assert fq.fp4_status_sync() == fq.FP4_OK
