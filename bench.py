@@ -370,6 +370,7 @@ def run_gpu(args, world, rank, local):
     per_format = run_per_format(args, world, host, dev, flush, pk)
     fp8_vs_fp4 = run_fp8_vs_fp4(host, dev, flush, pk,
                                 dict(per_format, **{FMT_NAMES[args.format]: summ}))
+    exact = run_exact_path(host, dev, flush, pk, dict(per_format, **{FMT_NAMES[args.format]: summ}))
     del host
     configs = run_configs(dev, flush, pk)
 
@@ -404,6 +405,7 @@ def run_gpu(args, world, rank, local):
         "gemm_out_dtypes": out_dtypes,
         "per_format": per_format,
         "fp8_vs_fp4": fp8_vs_fp4,
+        "ue5m3_exact_path": exact,
         "configs": configs,
         "epilogue_fused_producer": fused,
         "mxfp4_to_fp8": reencode,
@@ -531,6 +533,50 @@ def run_fp8_vs_fp4(host, dev, flush, pk, per_format):
     fq._check(fq.fp4_status_sync(), "fp8 gemm")
     out["note"] = "FP4 figures are the step's GEMMs (frac of FP4 peak " + \
                   f"{round(fp4_peak, 1)} TFLOP/s in per_format)"
+    return out
+
+
+def run_exact_path(host, dev, flush, pk, per_format):
+    """The exact path for UE5M3 copies outside the E4M3 scale window on the
+    step's fprop: plain-layout UE5M3-b16 copies of X and W, fp4_dequantize of
+    each (0.5 + 1/16 B read, 2 B written per element) and fp4_gemm_bf16 on
+    the BF16 tensor cores (peak: the measured BF16 burst), against the FP4
+    fprop of the step."""
+    import fp4_block_scaled_quantize_gb300 as fq
+    X, W = (host[k].to(dev) for k in ("X", "W"))
+    p = fq.params(format=fq.FP4_FMT_UE5M3_B16, sf_layout=fq.FP4_SF_PLAIN)
+    cx = fq.quantize(X, fq.amax_many([X])[0], p)
+    cw = fq.quantize(W, fq.amax_many([W])[0], p)
+    del X, W
+    torch.cuda.empty_cache()
+    yx = torch.empty((M_TOK, K_FF), dtype=torch.bfloat16, device=dev)
+    yw = torch.empty((N_MODEL, K_FF), dtype=torch.bfloat16, device=dev)
+    D = torch.empty((M_TOK, N_MODEL), dtype=torch.bfloat16, device=dev)
+    deq_x = lambda: fq._check(fq.fp4_dequantize(cx.q, cx.sf, cx.format, M_TOK, K_FF, yx), "deq")
+    deq_w = lambda: fq._check(fq.fp4_dequantize(cw.q, cw.sf, cw.format, N_MODEL, K_FF, yw), "deq")
+    mm = lambda: fq.gemm_bf16(yx, yw, cx.s_dec, cw.s_dec, out=D)
+    deq_x()
+    deq_w()
+    mm()
+    fq._check(fq.fp4_status_sync(), "exact path")
+    out = {"operands": "plain-layout UE5M3-b16 copies of the step's X and W",
+           "bf16_peak_tflops": round(pk["bf16_tflops"], 1),
+           "bf16_peak_source": f"{pk['source']} bf16 burst"}
+    nb = M_TOK * K_FF * (0.5 + 1 / 16 + 2)
+    ms = graph_ms(deq_x, flush)
+    gbs = nb / (ms * 1e-3) / 1e9
+    out["dequantize_X"] = {"shape": [M_TOK, K_FF], "bytes_per_launch": int(nb), "ms": round(ms, 4),
+                           "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+    ms_w = graph_ms(deq_w, flush)
+    ms_g = median_ms(mm, flush)
+    flop = 2.0 * M_TOK * N_MODEL * K_FF
+    tf = flop / (ms_g * 1e-3) / 1e12
+    out["gemm_bf16_fprop"] = {"shape": [M_TOK, N_MODEL, K_FF], "ms": round(ms_g, 4),
+                              "tflops": round(tf, 1), "frac": round(tf / pk["bf16_tflops"], 4)}
+    out["exact_fprop_ms"] = round(ms + ms_w + ms_g, 4)
+    pf = per_format.get("UE5M3-b16")
+    if pf is not None:
+        out["fp4_fprop_ms"] = pf["gemm"]["per_gemm"]["fprop"]["ms"]
     return out
 
 
@@ -1146,6 +1192,14 @@ def run_profile(args, local):
         s8t = torch.empty((K_FF, M_TOK // 128), dtype=torch.float32, device=layer.X.device)
         ops["reencode_t"] = lambda: fq._check(
             fq.fp4_mxfp4_to_fp8_transpose(mx.q, sf, M_TOK, K_FF, q8t, s8t), "reencode_t")
+    if args.profile in ("dequantize", "gemm_bf16"):
+        p = fq.params(format=fq.FP4_FMT_UE5M3_B16, sf_layout=fq.FP4_SF_PLAIN)
+        cx = fq.quantize(layer.X, layer.amax["X"][0], p)
+        cw = fq.quantize(layer.W, layer.amax["W"][0], p)
+        yx, yw = fq.dequantize(cx), fq.dequantize(cw)
+        ops["dequantize"] = lambda: fq._check(
+            fq.fp4_dequantize(cx.q, cx.sf, cx.format, M_TOK, K_FF, yx), "dequantize")
+        ops["gemm_bf16"] = lambda: fq.gemm_bf16(yx, yw, cx.s_dec, cw.s_dec, out=layer.Y)
     torch.cuda.synchronize()
     for _ in range(3):
         ops[args.profile]()
@@ -1166,7 +1220,7 @@ def main():
     ap.add_argument("--profile", default=None,
                     choices=["amax", "quant_X", "quant_W", "quant_dY", "fprop", "dgrad", "wgrad",
                              "reencode", "reencode_t", "fp8_fprop", "fp8_dgrad", "fp8_wgrad",
-                             "amax_stripes"],
+                             "amax_stripes", "dequantize", "gemm_bf16"],
                     help="run only this kernel (3 launches after set-up) for an ncu capture")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

@@ -64,7 +64,7 @@ _lib = None
 EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
            "fp4_mxfp4_to_fp8_transpose",
            "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
-           "fp4_fp8_gemm", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
+           "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
            "fp4_status_string")
 
 
@@ -90,6 +90,8 @@ def lib():
         L.fp4_gemm.argtypes = [op, op, i64, i64, i64, vp, i32, i32, vp]
         L.fp4_gemm_quantize.argtypes = [op, op, i64, i64, i64, vp, qp, vp, vp, vp, vp, i32, vp]
         L.fp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, vp]
+        L.fp4_dequantize.argtypes = [vp, vp, i32, i64, i64, vp, vp]
+        L.fp4_gemm_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, i32, vp]
         L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
         L.fp4_sf_bytes.restype = i64
         L.fp4_block_size.argtypes = [i32]
@@ -100,7 +102,8 @@ def lib():
         for f in ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
                   "fp4_mxfp4_to_fp8_transpose",
                   "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
-                  "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_status_sync"):
+                  "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16",
+                  "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -196,6 +199,16 @@ def fp4_gemm_quantize(A, B, M, N, K, amax, p, q, sf, s_dec, row_shift=None, cano
 def fp4_fp8_gemm(q8a, s8a, q8b, s8b, M, N, K, D, d_is_bf16, stream=None):
     return lib().fp4_fp8_gemm(_ptr(q8a), _ptr(s8a), _ptr(q8b), _ptr(s8b), M, N, K, _ptr(D),
                               int(bool(d_is_bf16)), _stream(stream))
+
+
+def fp4_dequantize(q, sf, format, rows, cols, y, stream=None):
+    return lib().fp4_dequantize(_ptr(q), _ptr(sf), format, rows, cols, _ptr(y), _stream(stream))
+
+
+def fp4_gemm_bf16(a, s_dec_a, b, s_dec_b, M, N, K, D, d_is_bf16, canonicalize_1024=0,
+                  stream=None):
+    return lib().fp4_gemm_bf16(_ptr(a), _ptr(s_dec_a), _ptr(b), _ptr(s_dec_b), M, N, K, _ptr(D),
+                               int(bool(d_is_bf16)), int(canonicalize_1024), _stream(stream))
 
 
 def fp4_sf_bytes(format, rows, cols, layout):
@@ -404,6 +417,59 @@ def fp8_gemm(q8a, s8a, q8b, s8b, out_dtype=torch.float32, out=None, stream=None)
     _check(fp4_fp8_gemm(q8a, s8a, q8b, s8b, M, N, K, D, D.dtype == torch.bfloat16, stream),
            "fp4_fp8_gemm")
     return D
+
+
+def dequantize(c, stream=None):
+    """BF16 values e2m1(q) * dec(block scale) of a row-wise copy in the plain
+    scale layout (the tensor scale c.s_dec left out); exact."""
+    if c.sf_layout != FP4_SF_PLAIN:
+        raise ValueError("dequantize: the copy needs the plain scale layout")
+    y = torch.empty((c.rows, c.k), dtype=torch.bfloat16, device=c.q.device)
+    _check(fp4_dequantize(c.q, c.sf, c.format, c.rows, c.k, y, stream), "fp4_dequantize")
+    return y
+
+
+def _out(M, N, device, out_dtype, out, where):
+    if out is not None:
+        if out.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError(f"{where}: out must be float32 or bfloat16")
+        if tuple(out.shape) != (M, N) or not out.is_contiguous() or out.device != device:
+            raise ValueError(f"{where}: out must be a contiguous [{M}, {N}] tensor on {device}")
+        return out
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"{where}: out_dtype must be float32 or bfloat16")
+    return torch.empty((M, N), dtype=out_dtype, device=device)
+
+
+def gemm_bf16(a, b, s_dec_a, s_dec_b, out_dtype=torch.float32, out=None,
+              canonicalize_1024=False, stream=None):
+    """D = RN32(s_dec_a s_dec_b) A B^T on the BF16 tensor cores for BF16
+    A [M, K], B [N, K] and 1-element float32 decode scales on the device."""
+    for t, name in ((a, "a"), (b, "b")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"gemm_bf16: {name} must be a contiguous 2-D bfloat16 tensor")
+    for t, name in ((s_dec_a, "s_dec_a"), (s_dec_b, "s_dec_b")):
+        if t.dtype != torch.float32 or t.numel() < 1:
+            raise ValueError(f"gemm_bf16: {name} must be a float32 tensor")
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("gemm_bf16: operand shapes disagree")
+    D = _out(M, N, a.device, out_dtype, out, "gemm_bf16")
+    _check(fp4_gemm_bf16(a, s_dec_a, b, s_dec_b, M, N, K, D, D.dtype == torch.bfloat16,
+                         canonicalize_1024, stream), "fp4_gemm_bf16")
+    return D
+
+
+def gemm_exact(a, b, out_dtype=torch.float32, out=None, canonicalize_1024=False, stream=None):
+    """D = alpha A B^T for two plain-layout copies of one format, through the
+    exact dequantisation and the BF16 tensor cores: the product of the FP4
+    values for any UE5M3 scale span (the route for copies whose rows raised
+    FP4_ERR_SCALE_WINDOW on the tensor-core scale path)."""
+    if a.format != b.format or a.k != b.k:
+        raise ValueError("gemm_exact: operands must share format and K")
+    return gemm_bf16(dequantize(a, stream), dequantize(b, stream), a.s_dec, b.s_dec,
+                     out_dtype, out, canonicalize_1024, stream)
 
 
 def gemm_quantize(a, b, amax_dev, p, remap=True, canonicalize_1024=False, stream=None):

@@ -27,6 +27,7 @@ UNITS = {
     "quantize.cu": ["-fmad=false"],
     "remap.cu": ["-fmad=false"],
     "convert.cu": ["-fmad=false"],
+    "dequant.cu": ["-fmad=false"],
     "gemm.cu": [],
     "gemm2.cu": [],
 }

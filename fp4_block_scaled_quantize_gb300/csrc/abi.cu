@@ -164,6 +164,45 @@ fp4_status fp4_fp8_gemm(const uint8_t *q8a, const float *s8a, const uint8_t *q8b
   return launch_gemm_fp8(j, as_stream(stream));
 }
 
+fp4_status fp4_dequantize(const uint8_t *q, const uint8_t *sf, int32_t format, int64_t rows,
+                          int64_t cols, void *y_bf16, void *stream) {
+  if (!valid_format(format) || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;
+  if (format != FP4_FMT_UE5M3_B16 && format != FP4_FMT_UE5M3_B32 && format != FP4_FMT_NVFP4_B16)
+    return FP4_ERR_UNSUPPORTED;
+  if (cols % block_of(format) != 0) return FP4_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return FP4_OK;
+  if (!q || !sf || !y_bf16) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(y_bf16)) return FP4_ERR_ALIGNMENT;
+  return launch_dequant_bf16(q, sf, rows, cols, format, y_bf16, as_stream(stream));
+}
+
+fp4_status fp4_gemm_bf16(const void *a_bf16, const float *s_dec_a, const void *b_bf16,
+                         const float *s_dec_b, int64_t M, int64_t N, int64_t K, void *D,
+                         int32_t d_is_bf16, int32_t canonicalize_1024, void *stream) {
+  if (M < 0 || N < 0 || K < 0) return FP4_ERR_INVALID_ARG;
+  if (K % 16 != 0 || N % 8 != 0) return FP4_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP4_OK;
+  if (!D) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(D)) return FP4_ERR_ALIGNMENT;
+  if (K > 0) {
+    if (!a_bf16 || !b_bf16 || !s_dec_a || !s_dec_b) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(a_bf16) || !aligned16(b_bf16) || !aligned4(s_dec_a) || !aligned4(s_dec_b))
+      return FP4_ERR_ALIGNMENT;
+  }
+  Bf16GemmJob j{};
+  j.a = a_bf16;
+  j.b = b_bf16;
+  j.sda = s_dec_a;
+  j.sdb = s_dec_b;
+  j.M = M;
+  j.N = N;
+  j.K = K;
+  j.D = D;
+  j.d_bf16 = d_is_bf16 != 0;
+  j.canon = canonicalize_1024 != 0;
+  return launch_gemm_bf16(j, as_stream(stream));
+}
+
 fp4_status fp4_quantize(const void *x_bf16, int64_t rows, int64_t cols, const float *amax_dev,
                         const fp4_quant_params *p, uint8_t *q, uint8_t *sf, float *s_dec_dev,
                         int8_t *row_shift, void *stream) {

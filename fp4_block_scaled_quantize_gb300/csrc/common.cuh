@@ -146,6 +146,18 @@ struct Fp8GemmJob {
   int d_bf16;
 };
 fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s);
+// BF16 GEMM (kind::f16) on dequantised copies: D = RN32(sda sdb) A B^T.
+struct Bf16GemmJob {
+  const void *a, *b;  // BF16 [M][K], [N][K]
+  const float *sda, *sdb;
+  int64_t M, N, K;
+  void *D;
+  int d_bf16, canon;
+};
+fp4_status launch_gemm_bf16(const Bf16GemmJob &j, cudaStream_t s);
+// FP4 copy (plain scale layout) -> BF16 values e2m1(q) * dec(sf); exact.
+fp4_status launch_dequant_bf16(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
+                               int fmt, void *out, cudaStream_t s);
 // GEMM on SM pairs (tcgen05 cta_group::2); K > 0, M > 128, with or without
 // the fused output producer.
 fp4_status launch_gemm_pair(const GemmJob &j, cudaStream_t s);

@@ -50,6 +50,15 @@
 // stage's tensor-memory slot (four stages' scales of a row are one 16-byte
 // load, issued a group of stages ahead); a scale that is not a power of two
 // in [2^-127, 2^127] raises the scale-window status bit.
+//
+// Instantiated for kBF16 it multiplies BF16 operands (64 elements per stage,
+// four tcgen05.mma.kind::f16 K16 steps, no block scales; the scale warps
+// only hand landed stages over): the exact fallback for UE5M3 copies whose
+// rows span more binades than the E4M3 scale path holds, run on their
+// dequantised values ("UE5M3 FP4 Block Scaling for Stable Language Model
+// Pretraining", Limitations: UE5M3 is not native).  A product of two
+// dequantised values has at most 12 significant bits, so the only rounding
+// is the binary32 accumulation, as on the FP4 path.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -67,7 +76,8 @@ namespace fp4 {
 
 namespace {
 
-constexpr int kFP8 = 8;  // FP8 operand kind of this kernel (not a producer format)
+constexpr int kFP8 = 8;   // FP8 operand kind of this kernel (not a producer format)
+constexpr int kBF16 = 9;  // BF16 operand kind (dequantised copies)
 constexpr int BM = 128, BN = 256;
 constexpr int BK_BYTES = 128;  // 256 FP4 elements per stage
 constexpr int STAGES = 4;
@@ -117,7 +127,13 @@ constexpr uint32_t kHandoffBar = 1;  // barrier 0 is __syncthreads
 template <int FMT>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  if (FMT == kFP8) {
+  if (FMT == kBF16) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else if (FMT == kFP8) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
@@ -143,8 +159,13 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
 // Instruction descriptor, kind::mxf4nvf4: E2M1 x E2M1, K-major A and B,
 // M = 128, N = 256; scale type E4M3 (block 16) or E8M0 (block 32).
 // kind::mxf8f6f4 (kFP8): E4M3 x E4M3 (type code 0), E8M0 scales.
+// kind::f16 (kBF16): binary32 D (bits 4-5 = 1), BF16 A and B (type code 1
+// in bits 7-9 and 10-12), both K-major, no scale fields.
 template <int FMT>
 __device__ __forceinline__ uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
+  if (FMT == kBF16)
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
   uint32_t d = 0;
   d |= (b_sf_id & 3u) << 4;
   if (FMT != kFP8) {
@@ -222,12 +243,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t *st = smem + stage * STAGE_BYTES;
         const uint32_t fb = full_bar(stage);
-        if (FMT == kFP8) {
-          // FP8: operand tiles; with TMA scales, every fourth stage also
-          // brings the binary32 scales of its group of four stages (4
-          // columns x 128 A rows, 4 x 256 B rows) into the group buffer
-          // (the unused scale area of stage slot (group & 1))
-          const bool sg = p.fp8_tma_scales && (kt & 3) == 0;
+        if (FMT == kFP8 || FMT == kBF16) {
+          // FP8 / BF16: operand tiles; FP8 with TMA scales: every fourth
+          // stage also brings the binary32 scales of its group of four
+          // stages (4 columns x 128 A rows, 4 x 256 B rows) into the group
+          // buffer (the unused scale area of stage slot (group & 1))
+          const bool sg = FMT == kFP8 && p.fp8_tma_scales && (kt & 3) == 0;
           mbar_expect_tx(fb, A_BYTES + B_BYTES + (sg ? (uint32_t)(SFA_BYTES + SFB_BYTES) : 0u));
           tma_load_2d(smem_u32(st), &tma_a, fb, kt * BK_BYTES, mt * BM);
           tma_load_2d(smem_u32(st + A_BYTES), &tma_b, fb, kt * BK_BYTES, nt * BN);
@@ -507,6 +528,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
+        if (FMT == kBF16) {  // no scales: hand the landed stage over
+          if (bar_red_or(kHandoffBar, kHandoffThreads, false)) {
+            ok = false;
+            break;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         const uint8_t *st = smem + stage * STAGE_BYTES;
         const uint8_t *sfa_s = st + A_BYTES + B_BYTES;
         const uint8_t *sfb_s = sfa_s + SFA_BYTES;
@@ -751,6 +783,43 @@ fp4_status launch_gemm_fp8(const Fp8GemmJob &j, cudaStream_t s) {
                      make_map_f32(&msa, j.sa, j.M, p.kb8, 4, BM) &&
                      make_map_f32(&msb, j.sb, j.N, p.kb8, 4, BN);
   return launch_fmt<kFP8, false>(ma, mb, msa, msb, p, grid, s);
+}
+
+fp4_status launch_gemm_bf16(const Bf16GemmJob &j, cudaStream_t s) {
+  const size_t elt = j.d_bf16 ? 2 : 4;
+  if (j.K == 0) {
+    return cudaMemsetAsync(j.D, 0, (size_t)j.M * j.N * elt, s) == cudaSuccess ? FP4_OK
+                                                                             : FP4_ERR_CUDA;
+  }
+  uint32_t *status = status_word();
+  if (!status) return FP4_ERR_CUDA;
+  // BF16 rows of 2K bytes; a 128-byte stage box holds 64 elements
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, j.a, j.M, 2 * j.K, BM) || !make_map(&mb, j.b, j.N, 2 * j.K, BN))
+    return FP4_ERR_CUDA;
+  Params p{};
+  p.sda = j.sda;
+  p.sdb = j.sdb;
+  p.D = j.D;
+  p.M = j.M;
+  p.N = j.N;
+  p.K = j.K;
+  p.m_tiles = (int)ceil_div(j.M, BM);
+  p.n_tiles = (int)ceil_div(j.N, BN);
+  p.k_steps = (int)(j.K / 16);           // one K16 MMA step per 32 bytes
+  p.k_tiles = (int)ceil_div(j.K, 64);    // 128 bytes of K per stage
+  p.n_fast = j.M >= j.N ? 1 : 0;
+  p.d_bf16 = j.d_bf16;
+  p.canon = j.canon;
+  p.status = status;
+  const char *stall = std::getenv("FP4_TEST_STALL_PRODUCER");  // failure-detection test switch
+  p.stall_producer = (stall && stall[0] == '1') ? 1 : 0;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  return launch_fmt<kBF16, false>(ma, mb, ma, mb, p, grid, s);
 }
 
 fp4_status launch_gemm(const GemmJob &j, cudaStream_t s) {

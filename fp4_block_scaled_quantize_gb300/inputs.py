@@ -118,3 +118,14 @@ def mxfp4_copy(rows, cols, seed=11, spread=20):
         idx = torch.randperm(flat.numel(), generator=g)[:3]
         flat[idx] = torch.tensor([0, 254, 255], dtype=torch.int32)
     return q.to(torch.uint8), sf.to(torch.uint8)
+
+
+def fp4_copy(rows, cols, block, max_code, seed=13):
+    """Random bytes in the shape of a row-wise FP4 copy with plain-layout
+    scales: payload [rows][cols/2] (uniform bytes: every E2M1 code and sign)
+    and scale codes [rows][cols/block] uniform in 0 .. max_code.  Returns
+    uint8 tensors."""
+    g = _gen(seed)
+    q = torch.randint(0, 256, (rows, cols // 2), generator=g, dtype=torch.int32)
+    sf = torch.randint(0, max_code + 1, (rows, cols // block), generator=g, dtype=torch.int32)
+    return q.to(torch.uint8), sf.to(torch.uint8)

@@ -215,6 +215,35 @@ fp4_status fp4_fp8_gemm(const uint8_t *q8a, const float *s8a, const uint8_t *q8b
                         const float *s8b, int64_t M, int64_t N, int64_t K, void *D,
                         int32_t d_is_bf16, void *stream);
 
+/* Dequantisation of a row-wise FP4 copy to BF16 ([UE5M3] Limitations: the
+ * tensor core has no UE5M3 scale type, so a UE5M3 row whose block scales
+ * span more binades than the E4M3 remap holds -- FP4_ERR_SCALE_WINDOW --
+ * is multiplied through this path and fp4_gemm_bf16 instead):
+ *   y[r][c] = e2m1(q[r][c]) * dec(sf[r][c/B]),
+ * the tensor scale s_dec left out (fp4_gemm_bf16 applies it).  Exact: each
+ * value has at most 6 significant bits and lies in BF16's normal range.
+ * Input: q [rows][cols/2] (element 2j in the low nibble of byte j), sf in
+ * the PLAIN layout [rows][cols/B] (UE5M3 or E4M3 codes, as fp4_quantize
+ * writes them with FP4_SF_PLAIN).  Formats: UE5M3_B16, UE5M3_B32,
+ * NVFP4_B16 (others FP4_ERR_UNSUPPORTED).  Output: y_bf16 [rows][cols].
+ * Shapes: cols % B == 0; rows == 0 or cols == 0 writes nothing.  Alignment:
+ * q and y_bf16 16 bytes.  The caller owns every buffer. */
+fp4_status fp4_dequantize(const uint8_t *q, const uint8_t *sf, int32_t format,
+                          int64_t rows, int64_t cols, void *y_bf16, void *stream);
+
+/* BF16 GEMM D[M][N] = alpha * A[M][K] * B[N][K]^T, alpha = RN32(*s_dec_a *
+ * *s_dec_b), on tcgen05.mma.kind::f16 with a binary32 accumulator in tensor
+ * memory (K16 steps).  With A and B from fp4_dequantize and s_dec the
+ * copies' decode scales this is the FP4 GEMM of those copies for any UE5M3
+ * scale span: every product of two dequantised values is exact, the only
+ * rounding is the binary32 accumulation.  canonicalize_1024 and the output
+ * as in fp4_gemm.  Shapes: M, N, K >= 0, K % 16 == 0, N % 8 == 0; K == 0
+ * writes zeros.  Alignment: a_bf16, b_bf16, D 16 bytes; s_dec_a, s_dec_b
+ * (device floats) 4 bytes.  Argument errors are returned before any launch. */
+fp4_status fp4_gemm_bf16(const void *a_bf16, const float *s_dec_a, const void *b_bf16,
+                         const float *s_dec_b, int64_t M, int64_t N, int64_t K, void *D,
+                         int32_t d_is_bf16, int32_t canonicalize_1024, void *stream);
+
 /* Row-wise copy of x[rows][cols] ([UE5M3] Approach: block scales, E2M1
  * payload, RNE or SR, zero-scale rule, 2D weight tiles):
  *   s_enc = RN32(RN32(6T) / amax), s_dec = RN32(1 / s_enc)  (MX: 1, 1);

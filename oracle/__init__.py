@@ -418,6 +418,27 @@ def fp8_gemm_exact(q8a, s8a, q8b, s8b, mi, ni):
     return y, s
 
 
+# ------------------------------------------------------ dequantisation
+
+def dequantize(q, sf, fmt):
+    """Values of a row-wise copy without its tensor scale ("UE5M3 FP4 Block
+    Scaling for Stable Language Model Pretraining", Approach: an element is
+    its E2M1 value times its block's decoded scale): y[r][c] =
+    e2m1(nibble c of row r) * scale(sf[r][c / B]), nibble 2j the low half of
+    byte j, sf in the plain layout [R][C/B].  Binary64, exact."""
+    q = np.ascontiguousarray(q, np.uint8)
+    sf = np.ascontiguousarray(sf, np.uint8)
+    R, C = q.shape[0], 2 * q.shape[1]
+    B = block_size(fmt)
+    assert sf.shape == (R, C // B)
+    e2m1 = np.array([e2m1_value(c) for c in range(16)], np.float64)
+    dec = np.array([scale_value(fmt, c) for c in range(256)], np.float64)
+    codes = np.empty((R, C), np.uint8)
+    codes[:, 0::2] = q & 0x0F
+    codes[:, 1::2] = q >> 4
+    return e2m1[codes] * np.repeat(dec[sf], B, axis=1)
+
+
 # ------------------------------------------------------------------ GEMM
 
 def gemm_model(qa, sfa, qb, sfb, fmt, K, s_dec_a, s_dec_b, mi, ni, canon=False,

@@ -148,6 +148,36 @@ def test_fp8_gemm_argument_errors_before_any_launch(L):
     assert f(None, None, None, None, 0, 256, 128, None, 0, None) == 0    # empty: nothing to do
 
 
+def test_dequantize_argument_errors_before_any_launch(L):
+    f = L.fp4_dequantize
+    ue, nv, mx = fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_NVFP4_B16, fq.FP4_FMT_MXFP4_B32
+    assert f(4096, 8192, mx, 4, 32, 16384, None) == fq.FP4_ERR_UNSUPPORTED
+    assert f(4096, 8192, fq.FP4_FMT_NVFP4_CTA, 4, 32, 16384, None) == fq.FP4_ERR_UNSUPPORTED
+    assert f(4096, 8192, 9, 4, 32, 16384, None) == 1
+    assert f(4096, 8192, ue, -1, 32, 16384, None) == 1
+    assert f(4096, 8192, fq.FP4_FMT_UE5M3_B32, 4, 48, 16384, None) == fq.FP4_ERR_SHAPE
+    assert f(4096, 8192, nv, 4, 40, 16384, None) == fq.FP4_ERR_SHAPE
+    assert f(None, 8192, ue, 4, 32, 16384, None) == 1
+    assert f(4096, 8192, ue, 4, 32, None, None) == 1
+    assert f(4100, 8192, ue, 4, 32, 16384, None) == 2                    # q alignment
+    assert f(4096, 8192, ue, 4, 32, 16386, None) == 2                    # y alignment
+    assert f(None, None, ue, 0, 32, None, None) == 0                     # empty
+
+
+def test_gemm_bf16_argument_errors_before_any_launch(L):
+    f = L.fp4_gemm_bf16
+    ok = (4096, 8192, 12288, 16384)  # a, s_dec_a, b, s_dec_b (never dereferenced)
+    assert f(*ok, 128, 256, 24, 20480, 0, 0, None) == fq.FP4_ERR_SHAPE   # K % 16
+    assert f(*ok, 128, 252, 32, 20480, 0, 0, None) == fq.FP4_ERR_SHAPE   # N % 8
+    assert f(*ok, -1, 256, 32, 20480, 0, 0, None) == 1
+    assert f(*ok, 128, 256, 32, None, 0, 0, None) == 1                   # no output
+    assert f(4096, None, 12288, 16384, 128, 256, 32, 20480, 0, 0, None) == 1
+    assert f(4104, 8192, 12288, 16384, 128, 256, 32, 20480, 0, 0, None) == 2  # a alignment
+    assert f(4096, 8194, 12288, 16384, 128, 256, 32, 20480, 0, 0, None) == 2  # s_dec_a
+    assert f(*ok, 128, 256, 32, 20488, 0, 0, None) == 2                  # D alignment
+    assert f(None, None, None, None, 0, 256, 32, None, 0, 0, None) == 0  # empty
+
+
 def test_amax_argument_errors_before_any_launch(L):
     f = L.fp4_amax
     assert f(4096, 4, 16, 0, 0, None, None, None) == 1          # no output

@@ -962,3 +962,53 @@ def test_stripe_gemm_model_applies_each_stripe_pair_scale():
         dot = float(np.dot(decode(ca, m), decode(cb, n)))
         want = dot * float(ca["s_dec"][m // 128]) * float(cb["s_dec"][n // 128])
         assert ye[t] == pytest.approx(want, rel=1e-12, abs=1e-300)
+
+
+# ------------------------------------------------------ dequantisation
+
+def test_dequantize_closed_forms():
+    """Element values fixed by the format definitions ("UE5M3 FP4 Block
+    Scaling for Stable Language Model Pretraining", Approach: UE5M3's
+    largest scale is 61,440; E4M3's is 448; E2M1 codes 7 = +6, 9 = -0.5):
+    the low nibble of byte j is element 2j."""
+    q = np.zeros((2, 8), np.uint8)
+    q[:, 0] = 0x97  # element 0: code 7 (+6), element 1: code 9 (-0.5)
+    sf = np.array([[0xF7], [0x01]], np.uint8)  # 61,440 and 2^-17 (subnormal)
+    y = orc.dequantize(q, sf, orc.UE5M3)
+    assert y.shape == (2, 16)
+    assert (y[0, 0], y[0, 1]) == (368640.0, -30720.0)
+    assert (y[1, 0], y[1, 1]) == (6 * 2.0 ** -17, -(2.0 ** -18))
+    assert not y[:, 2:].any()
+    sf = np.array([[0x7E], [0x01]], np.uint8)  # E4M3: 448 and 2^-9 (subnormal)
+    y = orc.dequantize(q, sf, orc.NVFP4)
+    assert (y[0, 0], y[0, 1]) == (2688.0, -224.0)
+    assert (y[1, 0], y[1, 1]) == (6 * 2.0 ** -9, -(2.0 ** -10))
+    # block 32: elements 31 and 32 (nibbles of byte 15 and 16) in blocks 0, 1
+    q = np.zeros((1, 32), np.uint8)
+    q[0, 15] = 0x20  # element 31: code 2 (1.0)
+    q[0, 16] = 0x02  # element 32: code 2
+    sf = np.array([[0x78, 0x80]], np.uint8)  # UE5M3 1.0 and 2.0
+    y = orc.dequantize(q, sf, orc.UE5M3_B32)
+    assert y[0, 31] == 1.0 and y[0, 32] == 2.0
+    assert np.count_nonzero(y) == 2
+
+
+@pytest.mark.parametrize("fmt", [orc.UE5M3, orc.NVFP4, orc.UE5M3_B32])
+def test_dequantize_round_trip_within_half_gap(fmt):
+    """x against its copy's values times s_dec: E2M1's gaps are at most 2
+    (between 4 and 6) on the scaled axis, so nearest rounding moves an
+    element by at most 1 scale unit dec(sf) s_dec; saturation of a block
+    maximum rounded above 6 by the scale's own rounding (3 mantissa bits)
+    moves it by at most 6 / 16 of a unit."""
+    from fp4_block_scaled_quantize_gb300 import inputs
+    x = inputs.sweep_operand(48, 256, seed=5).float().numpy()
+    amax = float(np.abs(x).max())
+    c = orc.quantize(x, amax, fmt)
+    y = orc.dequantize(c["q"], c["sf"], fmt)
+    B = orc.block_size(fmt)
+    unit = np.repeat(np.vectorize(lambda k: orc.scale_value(fmt, int(k)))(c["sf"]), B, 1)
+    unit = unit * float(c["s_dec"])
+    err = np.abs(x.astype(np.float64) - y * float(c["s_dec"]))
+    assert (err <= 1.01 * unit).all()
+    # and the copy is not trivially coarse: most elements land within half a unit
+    assert np.mean(err <= 0.5 * unit) > 0.9
