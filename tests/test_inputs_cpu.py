@@ -74,3 +74,15 @@ def test_mxfp4_copy_structure():
     # payload bytes cover every E2M1 code in both nibbles
     qb = q.numpy()
     assert len(np.unique(qb & 15)) == 16 and len(np.unique(qb >> 4)) == 16
+
+
+def test_fp4_copy_structure():
+    q, sf = inputs.fp4_copy(64, 512, 16, 0xF7, seed=3)
+    assert q.shape == (64, 256) and sf.shape == (64, 32)
+    assert q.dtype == torch.uint8 and sf.dtype == torch.uint8
+    s = sf.numpy()
+    assert s.max() == 0xF7 and s.min() == 0  # the whole code range, nothing above
+    qb = q.numpy()
+    assert len(np.unique(qb & 15)) == 16 and len(np.unique(qb >> 4)) == 16
+    q2, sf2 = inputs.fp4_copy(64, 512, 16, 0xF7, seed=3)
+    assert torch.equal(q, q2) and torch.equal(sf, sf2)
