@@ -22,13 +22,24 @@ library's per-device status word, which stays set until it is read.
 ``FP4Linear.next_step()`` reads it once per step (outside the hot loop) and
 raises ``FP4Error`` if anything was recorded; pass ``check_status=False`` to
 leave that to the caller.
+
+UE5M3 rows whose block scales span more binades than the tensor core's E4M3
+scale path holds (the hardware has no UE5M3 scale type: "UE5M3 FP4 Block
+Scaling ...", Limitations) raise the scale-window condition.  With
+``exact_fallback=True`` the layer reads the status word after producing its
+operands: on a miss, the forward or backward step produces plain-layout
+copies (the same codes) and multiplies their exact BF16 dequantisations on
+the BF16 tensor cores (``gemm_exact``).  Each forward and backward then costs
+one host synchronisation; the BF16 input and weight are kept for the
+backward pass.
 """
 import itertools
 
 import torch
 
-from . import (FP4_FMT_UE5M3_B16, FP4_OK, FP4_ROUND_SR, FP4_SF_MMA, FP4Error, _check, fp4_amax,
-               fp4_status_sync, gemm, params, quantize_transpose)
+from . import (FP4_ERR_SCALE_WINDOW, FP4_FMT_UE5M3_B16, FP4_FMT_UE5M3_B32, FP4_OK,
+               FP4_ROUND_SR, FP4_SF_MMA, FP4_SF_PLAIN, FP4Error, _check, fp4_amax, fp4_status_sync,
+               gemm, gemm_exact, params, quantize_transpose)
 
 # Distinct stochastic-rounding streams per module: the default Philox key of
 # the k-th FP4Linear built in this process is (42 << 32) | k, so two layers
@@ -63,6 +74,25 @@ class AmaxCache:
         return True
 
 
+def _plain(p):
+    """The same producer options with plain-layout scales (UE5M3 codes kept,
+    no remap): the exact path's operands."""
+    q = type(p).from_buffer_copy(p)
+    q.sf_layout = FP4_SF_PLAIN
+    return q
+
+
+def _window_missed(where):
+    """Read (and clear) the status word: True on a UE5M3 scale-window miss;
+    any other recorded condition raises."""
+    st = fp4_status_sync()
+    if st == FP4_ERR_SCALE_WINDOW:
+        return True
+    if st != FP4_OK:
+        raise FP4Error(st, where)
+    return False
+
+
 class _FP4LinearFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, w, mod):
@@ -71,21 +101,43 @@ class _FP4LinearFn(torch.autograd.Function):
         mod.cache_w.update(w, mod.step)
         xr, xc = quantize_transpose(x2, mod.cache_x.row, mod.cache_x.col, mod.p_x)
         wr, wc = quantize_transpose(w, mod.cache_w.row, mod.cache_w.col, mod.p_w)
-        y = gemm(xr, wr, out_dtype=torch.bfloat16)
+        exact = mod.exact_fallback and _window_missed(f"FP4Linear step {mod.step} forward")
+        if exact:
+            xr, xc = quantize_transpose(x2, mod.cache_x.row, mod.cache_x.col, _plain(mod.p_x))
+            wr, wc = quantize_transpose(w, mod.cache_w.row, mod.cache_w.col, _plain(mod.p_w))
+            y = gemm_exact(xr, wr, out_dtype=torch.bfloat16)
+        else:
+            y = gemm(xr, wr, out_dtype=torch.bfloat16)
         ctx.x_shape = x.shape
-        ctx.saved = (xc, wc, mod)
+        ctx.exact = exact
+        keep = mod.exact_fallback and not exact  # the backward may still need plain copies
+        ctx.saved = (xc, wc, mod, x2 if keep else None, w if keep else None)
         return y.reshape(*x.shape[:-1], w.shape[0])
 
     @staticmethod
     def backward(ctx, dy):
-        xc, wc, mod = ctx.saved
+        xc, wc, mod, x2, w = ctx.saved
         dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
         mod.cache_dy.update(dy2, mod.step)
         p = mod.p_dy
         p.sr_offset = mod.step & 0xFFFFFFFF  # fresh random bits every step
         dyr, dyc = quantize_transpose(dy2, mod.cache_dy.row, mod.cache_dy.col, p)
-        dx = gemm(dyr, wc, out_dtype=torch.bfloat16)   # [M, K]
-        dw = gemm(dyc, xc, out_dtype=torch.float32)    # [N, K]
+        exact = ctx.exact
+        if mod.exact_fallback:
+            exact = _window_missed(f"FP4Linear step {mod.step} backward") or exact
+        if exact:
+            # plain copies with the same codes (the SR counters do not depend
+            # on the scale layout); X^T and W^T again if the forward pass ran
+            # on the tensor-core path
+            dyr, dyc = quantize_transpose(dy2, mod.cache_dy.row, mod.cache_dy.col, _plain(p))
+            if not ctx.exact:
+                xc = quantize_transpose(x2, mod.cache_x.row, mod.cache_x.col, _plain(mod.p_x))[1]
+                wc = quantize_transpose(w, mod.cache_w.row, mod.cache_w.col, _plain(mod.p_w))[1]
+            dx = gemm_exact(dyr, wc, out_dtype=torch.bfloat16)
+            dw = gemm_exact(dyc, xc, out_dtype=torch.float32)
+        else:
+            dx = gemm(dyr, wc, out_dtype=torch.bfloat16)   # [M, K]
+            dw = gemm(dyc, xc, out_dtype=torch.float32)    # [N, K]
         return dx.reshape(ctx.x_shape), dw.to(mod.weight.dtype), None
 
 
@@ -97,17 +149,22 @@ class FP4Linear(torch.nn.Module):
     ``format`` is one of the library's FP4 formats (UE5M3 block 16 by
     default); ``T_dy`` is the per-module target for the upstream gradient's
     transposed (Wgrad) copy; ``sr_seed`` (default: distinct per module) keys
-    the stochastic rounding of dY.
+    the stochastic rounding of dY; ``exact_fallback`` (UE5M3 formats only)
+    sends a step whose copies miss the E4M3 scale window through the exact
+    dequantised path instead of reporting the miss.
     Call ``next_step()`` once per optimizer step to advance the
     sample-and-hold clock."""
 
     def __init__(self, in_features, out_features, D=50, T=448.0, T_dy=None,
                  format=FP4_FMT_UE5M3_B16, sr_seed=None, device="cuda", dtype=torch.bfloat16,
-                 check_status=True):
+                 check_status=True, exact_fallback=False):
         super().__init__()
+        if exact_fallback and format not in (FP4_FMT_UE5M3_B16, FP4_FMT_UE5M3_B32):
+            raise ValueError("exact_fallback applies to the UE5M3 formats only")
         if sr_seed is None:
             sr_seed = (42 << 32) | next(_module_index)
         self.check_status = bool(check_status)
+        self.exact_fallback = bool(exact_fallback)
         self.in_features, self.out_features = in_features, out_features
         self.weight = torch.nn.Parameter(
             torch.empty(out_features, in_features, device=device, dtype=dtype))

@@ -129,3 +129,81 @@ def test_linear_holds_amax_between_refreshes():
         lin(X1.cuda())
     assert lin.cache_x.last_refresh == 50
     assert float(lin.cache_x.row.item()) == 2 * a0
+
+
+def test_exact_fallback_policy_reads_the_status_word(monkeypatch):
+    import fp4_block_scaled_quantize_gb300.linear as L
+    with pytest.raises(ValueError):
+        FP4Linear(128, 64, device="cpu", format=NV, exact_fallback=True)
+    monkeypatch.setattr(L, "fp4_status_sync", lambda: fq.FP4_ERR_SCALE_WINDOW)
+    assert L._window_missed("test") is True
+    monkeypatch.setattr(L, "fp4_status_sync", lambda: fq.FP4_OK)
+    assert L._window_missed("test") is False
+    monkeypatch.setattr(L, "fp4_status_sync", lambda: fq.FP4_ERR_NONFINITE)
+    with pytest.raises(fq.FP4Error):
+        L._window_missed("test")
+    p = fq.params(format=UE, T=2048.0, sf_layout=fq.FP4_SF_MMA, sr_seed=7, sr_offset=3,
+                  round_row=fq.FP4_ROUND_SR)
+    q = L._plain(p)
+    assert q.sf_layout == fq.FP4_SF_PLAIN and p.sf_layout == fq.FP4_SF_MMA
+    assert (q.format, q.T, q.sr_seed, q.sr_offset, q.round_row) == (UE, 2048.0, 7, 3,
+                                                                    fq.FP4_ROUND_SR)
+
+
+def _check_exact(y_gpu, oa, ob, fmt, K, name):
+    """One GEMM of the exact path against the oracle's exact product: the
+    binary32 accumulation bound (K/16 + 16) 2^-23 S plus the BF16 rounding of
+    the output."""
+    Mo, No = y_gpu.shape
+    mm, nn = np.meshgrid(np.arange(Mo), np.arange(No), indexing="ij")
+    _, ye, s_abs = orc.gemm_model(oa["q"], oa["sf"], ob["q"], ob["sf"], ORC_FMT[fmt], K,
+                                  oa["s_dec"], ob["s_dec"], mm.ravel(), nn.ravel())
+    g = y_gpu.detach().float().cpu().numpy().ravel().astype(np.float64)
+    tol = (K / 16 + 16) * 2.0 ** -23 * s_abs + np.abs(ye) * 2.0 ** -8
+    err = np.abs(g - ye)
+    assert np.all(err <= tol), f"{name}: max err/tol {np.max(err / np.maximum(tol, 1e-300))}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wide", ["x", "dy"])
+def test_linear_exact_fallback_outside_the_scale_window(wide):
+    """A row of X (or of dY) with blocks ~22 binades apart misses the E4M3
+    window: without the policy the step reports FP4_ERR_SCALE_WINDOW; with it
+    the GEMMs that meet the miss run on the exact path and match the oracle's
+    exact products of the same copies."""
+    need_gpu()
+    M, K, N = 256, 384, 192
+    d = inputs.down_proj_8b(M=M, K=K, N=N)
+    X, W, dY = f32(d["X"]), d["W"], f32(d["dY"])
+    if wide == "x":
+        X[0, 0:16] = 4096.0
+        X[0, 16:32] *= 2.0 ** -12
+    else:
+        dY[0, 0:16] = 0.4
+        dY[0, 16:32] *= 2.0 ** -12
+    X, dY = torch.from_numpy(X).to(torch.bfloat16), torch.from_numpy(dY).to(torch.bfloat16)
+    T_dy = 2048.0
+    plain = FP4Linear(K, N, D=50, T_dy=T_dy, format=UE)
+    lin = FP4Linear(K, N, D=50, T_dy=T_dy, format=UE, exact_fallback=True,
+                    sr_seed=plain.p_dy.sr_seed)
+    for m in (plain, lin):
+        with torch.no_grad():
+            m.weight.copy_(W.cuda())
+    x0 = X.cuda().requires_grad_(True)
+    plain(x0).backward(dY.cuda())
+    with pytest.raises(fq.FP4Error) as e:
+        plain.next_step()
+    assert e.value.code == fq.FP4_ERR_SCALE_WINDOW
+    x = X.cuda().requires_grad_(True)
+    y = lin(x)
+    y.backward(dY.cuda())
+    lin.next_step()  # the miss was handled: nothing left in the status word
+    a32 = lambda t: float(np.max(np.abs(f32(t))))
+    fp, dg, wg = _oracle_layer(X, W, dY, UE, a32(X), a32(W), a32(dY), T_dy, offset=0,
+                               seed=lin.p_dy.sr_seed)
+    if wide == "x":
+        _check_exact(y, *fp, UE, K, "fprop (exact path)")
+    else:
+        _check_bf16(y, *fp, UE, K, "fprop (tensor cores)")
+    _check_exact(x.grad, *dg, UE, N, "dgrad (exact path)")
+    _check_exact(lin.weight.grad, *wg, UE, M, "wgrad (exact path)")
