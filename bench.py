@@ -373,6 +373,7 @@ def run_gpu(args, world, rank, local):
     exact = run_exact_path(host, dev, flush, pk, dict(per_format, **{FMT_NAMES[args.format]: summ}))
     del host
     configs = run_configs(dev, flush, pk)
+    ceiling = run_mma_ceiling(dom_tflops)
 
     clocks = clk.summary()
     out = {
@@ -406,6 +407,7 @@ def run_gpu(args, world, rank, local):
         "per_format": per_format,
         "fp8_vs_fp4": fp8_vs_fp4,
         "ue5m3_exact_path": exact,
+        "tensor_pipe_ceiling": ceiling,
         "configs": configs,
         "epilogue_fused_producer": fused,
         "mxfp4_to_fp8": reencode,
@@ -577,6 +579,20 @@ def run_exact_path(host, dev, flush, pk, per_format):
     pf = per_format.get("UE5M3-b16")
     if pf is not None:
         out["fp4_fprop_ms"] = pf["gemm"]["per_gemm"]["fprop"]["ms"]
+    return out
+
+
+def run_mma_ceiling(dominant_tflops):
+    """What the tensor pipe sustains on this device for the GEMMs' MMA forms
+    (fp4_mma_loop: back-to-back M128 N256 MMAs on resident operands, no
+    copies or hand-offs), beside the dominant GEMM's rate.  Context for the
+    roofline, whose peak stays the measured BF16 burst x the nominal ratio."""
+    import fp4_block_scaled_quantize_gb300 as fq
+    out = {"what": "tcgen05.mma M128 N256 back to back on operands resident in shared memory "
+                   "(fp4_mma_loop), median of 5 launches"}
+    for name, kind in (("fp4", fq.FP4_MMA_FP4), ("fp8", fq.FP4_MMA_FP8), ("bf16", fq.FP4_MMA_BF16)):
+        out[name + "_tflops"] = round(fq.mma_loop_tflops(kind), 1)
+    out["dominant_gemm_frac_of_fp4_loop"] = round(dominant_tflops / out["fp4_tflops"], 4)
     return out
 
 

@@ -24,6 +24,8 @@ FP4_FMT_NVFP4_CTA = 4  # NVFP4 with one tensor scale per 128-row stripe of each 
 STRIPE = 128
 FP4_ROUND_RNE, FP4_ROUND_SR = 0, 1
 FP4_SF_PLAIN, FP4_SF_MMA = 0, 1
+FP4_MMA_FP4, FP4_MMA_FP8, FP4_MMA_BF16 = 0, 1, 2  # tensor-pipe rate diagnostic kinds
+MMA_LOOP_K = {FP4_MMA_FP4: 64, FP4_MMA_FP8: 32, FP4_MMA_BF16: 16}
 FP4_OK = 0
 (FP4_ERR_INVALID_ARG, FP4_ERR_ALIGNMENT, FP4_ERR_UNSUPPORTED, FP4_ERR_CUDA, FP4_ERR_TIMEOUT,
  FP4_ERR_NONFINITE, FP4_ERR_SCALE_WINDOW, FP4_ERR_SHAPE) = range(1, 9)
@@ -64,7 +66,7 @@ _lib = None
 EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
            "fp4_mxfp4_to_fp8_transpose",
            "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
-           "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
+           "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16", "fp4_mma_loop", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
            "fp4_status_string")
 
 
@@ -91,6 +93,7 @@ def lib():
         L.fp4_gemm_quantize.argtypes = [op, op, i64, i64, i64, vp, qp, vp, vp, vp, vp, i32, vp]
         L.fp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, vp]
         L.fp4_dequantize.argtypes = [vp, vp, i32, i64, i64, vp, vp]
+        L.fp4_mma_loop.argtypes = [i32, i64, vp]
         L.fp4_gemm_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, i32, vp]
         L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
         L.fp4_sf_bytes.restype = i64
@@ -103,7 +106,7 @@ def lib():
                   "fp4_mxfp4_to_fp8_transpose",
                   "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16",
-                  "fp4_status_sync"):
+                  "fp4_mma_loop", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -210,6 +213,30 @@ def fp4_gemm_bf16(a, s_dec_a, b, s_dec_b, M, N, K, D, d_is_bf16, canonicalize_10
     return lib().fp4_gemm_bf16(_ptr(a), _ptr(s_dec_a), _ptr(b), _ptr(s_dec_b), M, N, K, _ptr(D),
                                int(bool(d_is_bf16)), int(canonicalize_1024), _stream(stream))
 
+
+def fp4_mma_loop(kind, iters, stream=None):
+    return lib().fp4_mma_loop(int(kind), int(iters), _stream(stream))
+
+
+def mma_loop_tflops(kind, iters=20000, reps=5, stream=None):
+    """Dense rate the tensor pipe sustains for one MMA kind on this device
+    (fp4_mma_loop timed with CUDA events on the launching stream, median of
+    `reps` launches after one warm-up), in TFLOP/s."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    _check(fp4_mma_loop(kind, iters, s), "fp4_mma_loop")
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        _check(fp4_mma_loop(kind, iters, s), "fp4_mma_loop")
+        b.record(s)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    _check(fp4_status_sync(s), "fp4_mma_loop")
+    ms = sorted(times)[len(times) // 2]
+    flop = sms * iters * 4 * 2.0 * 128 * 256 * MMA_LOOP_K[kind]
+    return flop / (ms * 1e-3) / 1e12
 
 def fp4_sf_bytes(format, rows, cols, layout):
     return lib().fp4_sf_bytes(format, rows, cols, layout)

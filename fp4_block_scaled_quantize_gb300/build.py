@@ -30,6 +30,7 @@ UNITS = {
     "dequant.cu": ["-fmad=false"],
     "gemm.cu": [],
     "gemm2.cu": [],
+    "mmarate.cu": [],
 }
 
 

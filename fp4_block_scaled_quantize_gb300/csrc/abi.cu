@@ -164,6 +164,12 @@ fp4_status fp4_fp8_gemm(const uint8_t *q8a, const float *s8a, const uint8_t *q8b
   return launch_gemm_fp8(j, as_stream(stream));
 }
 
+fp4_status fp4_mma_loop(int32_t kind, int64_t iters, void *stream) {
+  if (kind != FP4_MMA_FP4 && kind != FP4_MMA_FP8 && kind != FP4_MMA_BF16) return FP4_ERR_INVALID_ARG;
+  if (iters < 1 || iters > 1000000) return FP4_ERR_INVALID_ARG;
+  return launch_mma_loop(kind, iters, as_stream(stream));
+}
+
 fp4_status fp4_dequantize(const uint8_t *q, const uint8_t *sf, int32_t format, int64_t rows,
                           int64_t cols, void *y_bf16, void *stream) {
   if (!valid_format(format) || rows < 0 || cols < 0) return FP4_ERR_INVALID_ARG;

@@ -326,6 +326,18 @@ fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t
                              float *s_dec_dev, int8_t *row_shift,
                              int32_t canonicalize_1024, void *stream);
 
+/* Tensor-pipe rate diagnostic (roofline context for the GEMMs, not a step of
+ * the method): one CTA per SM issues `iters` groups of four tcgen05.mma
+ * M128 N256 (cta_group::1) back to back on zero operands resident in shared
+ * memory, scales resident in tensor memory, with no copies or hand-offs --
+ * the instruction forms of the GEMMs: FP4_MMA_FP4 kind::mxf4nvf4 with E4M3
+ * scales per 16 elements (K64), FP4_MMA_FP8 kind::mxf8f6f4 with E8M0 scales
+ * per 32 (K32), FP4_MMA_BF16 kind::f16 (K16).  The caller times the launch;
+ * flops per launch = SMs x iters x 4 x 2 x 128 x 256 x K.  1 <= iters <=
+ * 1,000,000 (about a quarter second).  Nothing is read back. */
+typedef enum { FP4_MMA_FP4 = 0, FP4_MMA_FP8 = 1, FP4_MMA_BF16 = 2 } fp4_mma_kind;
+fp4_status fp4_mma_loop(int32_t kind, int64_t iters, void *stream);
+
 /* Bytes of one scale-factor output for a copy with `rows` rows and `cols`
  * elements per row; -1 for an invalid format/layout. */
 int64_t fp4_sf_bytes(int32_t format, int64_t rows, int64_t cols,

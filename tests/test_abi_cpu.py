@@ -247,3 +247,11 @@ def test_gemm_wrapper_rejects_bad_operands_before_any_launch(L):
             fq.gemm(a, b, out=bad)
     with pytest.raises(ValueError, match="out_dtype"):
         fq.gemm(a, b, out_dtype=torch.float16)
+
+
+def test_mma_loop_argument_errors_before_any_launch(L):
+    f = L.fp4_mma_loop
+    assert f(3, 100, None) == 1
+    assert f(-1, 100, None) == 1
+    assert f(fq.FP4_MMA_FP4, 0, None) == 1
+    assert f(fq.FP4_MMA_FP4, 1000001, None) == 1
