@@ -301,8 +301,37 @@ def _want_shift(p, remap):
             and p.sf_layout == FP4_SF_MMA)
 
 
+def _need_cuda(where, *ts):
+    """Every tensor a kernel reads or writes is a CUDA tensor on one device
+    (a host tensor's pointer must never reach a kernel)."""
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{where}: tensors must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{where}: tensors must share one device")
+
+
+def _need_bf16(where, x, two_d=True):
+    if x.dtype != torch.bfloat16 or (two_d and x.dim() != 2) or not x.is_contiguous():
+        raise ValueError(f"{where}: x must be a contiguous {'2-D ' if two_d else ''}"
+                         "bfloat16 tensor")
+
+
+def _need_f32(where, *ts):
+    for t in ts:
+        if t is not None and (t.dtype != torch.float32 or t.numel() < 1):
+            raise ValueError(f"{where}: amax / decode-scale tensors must be float32")
+
+
 def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
     """(amax_row, amax_col) device float32 tensors of shape [1]."""
+    _need_bf16("amax", x)
+    _need_cuda("amax", x)
     a = torch.empty(1, dtype=torch.float32, device=x.device)
     b = torch.empty(1, dtype=torch.float32, device=x.device)
     _check(fp4_amax(x, hadamard_n, hadamard_signs, a, b, stream), "fp4_amax")
@@ -312,8 +341,8 @@ def amax(x, hadamard_n=0, hadamard_signs=0, stream=None):
 def amax_stripes(x, stream=None):
     """Stripe maxima for the CTA-local NVFP4 contract: (per 128-row stripe,
     per 128-column stripe) device float32 tensors."""
-    if not x.is_contiguous():
-        raise ValueError("amax_stripes: x must be contiguous")
+    _need_bf16("amax_stripes", x)
+    _need_cuda("amax_stripes", x)
     rows, cols = x.shape
     a = torch.empty(max(n_stripes(rows), 1), dtype=torch.float32, device=x.device)
     b = torch.empty(max(n_stripes(cols), 1), dtype=torch.float32, device=x.device)
@@ -323,8 +352,9 @@ def amax_stripes(x, stream=None):
 
 def amax_many(xs, stream=None):
     """[amax] device float32 tensors of shape [1], one per tensor, one launch."""
-    if any(not x.is_contiguous() for x in xs):
-        raise ValueError("amax_many: tensors must be contiguous")
+    for x in xs:
+        _need_bf16("amax_many", x, two_d=False)
+    _need_cuda("amax_many", *xs)
     outs = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
     _check(fp4_amax_many(xs, outs, stream), "fp4_amax_many")
     return outs
@@ -334,8 +364,10 @@ def mxfp4_to_fp8(q, sf, stream=None):
     """FP8 E4M3-b128 copy (q8 uint8 [R][C], s8 float32 [R][C/128]) of an
     MXFP4-b32 row-wise copy given by its payload q [R][C/2] and plain-layout
     E8M0 scales sf [R][C/32]."""
-    if not (q.is_contiguous() and sf.is_contiguous()):
-        raise ValueError("mxfp4_to_fp8: q and sf must be contiguous")
+    if not (q.is_contiguous() and sf.is_contiguous()) or q.dtype != torch.uint8 or \
+            sf.dtype != torch.uint8 or q.dim() != 2:
+        raise ValueError("mxfp4_to_fp8: q [R][C/2] and sf must be contiguous uint8 tensors")
+    _need_cuda("mxfp4_to_fp8", q, sf)
     rows, cols = q.shape[0], q.shape[1] * 2
     q8 = torch.empty((rows, cols), dtype=torch.uint8, device=q.device)
     s8 = torch.empty((rows, cols // 128), dtype=torch.float32, device=q.device)
@@ -347,8 +379,11 @@ def mxfp4_to_fp8_transpose(q, sf, stream=None):
     """FP8 E4M3-b128 copy of x^T (q8t uint8 [C][R], s8t float32 [C][R/128])
     from x's MXFP4-b32 row-wise copy (payload q [R][C/2], plain E8M0 scales
     sf [R][C/32])."""
-    if not (q.is_contiguous() and sf.is_contiguous()):
-        raise ValueError("mxfp4_to_fp8_transpose: q and sf must be contiguous")
+    if not (q.is_contiguous() and sf.is_contiguous()) or q.dtype != torch.uint8 or \
+            sf.dtype != torch.uint8 or q.dim() != 2:
+        raise ValueError("mxfp4_to_fp8_transpose: q [R][C/2] and sf must be contiguous uint8 "
+                         "tensors")
+    _need_cuda("mxfp4_to_fp8_transpose", q, sf)
     rows, cols = q.shape[0], q.shape[1] * 2
     q8t = torch.empty((cols, rows), dtype=torch.uint8, device=q.device)
     s8t = torch.empty((cols, rows // 128), dtype=torch.float32, device=q.device)
@@ -358,6 +393,9 @@ def mxfp4_to_fp8_transpose(q, sf, stream=None):
 
 
 def quantize(x, amax_dev, p, remap=True, stream=None):
+    _need_bf16("quantize", x)
+    _need_f32("quantize", amax_dev)
+    _need_cuda("quantize", x, amax_dev)
     rows, cols = x.shape
     out = _alloc_copy(rows, cols, p, x.device, _want_shift(p, remap))
     _check(fp4_quantize(x, amax_dev, p, out.q, out.sf, out.s_dec, out.row_shift, stream),
@@ -366,6 +404,9 @@ def quantize(x, amax_dev, p, remap=True, stream=None):
 
 
 def quantize_transpose(x, amax_row, amax_col, p, remap=True, stream=None):
+    _need_bf16("quantize_transpose", x)
+    _need_f32("quantize_transpose", amax_row, amax_col)
+    _need_cuda("quantize_transpose", x, amax_row, amax_col)
     rows, cols = x.shape
     ws = _want_shift(p, remap)
     r = _alloc_copy(rows, cols, p, x.device, ws)
@@ -413,6 +454,7 @@ def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, strea
         if out_dtype not in (torch.float32, torch.bfloat16):
             raise ValueError("gemm: out_dtype must be float32 or bfloat16")
         D = torch.empty((M, N), dtype=out_dtype, device=a.q.device)
+    _need_cuda("gemm", a.q, a.sf, a.s_dec, a.row_shift, b.q, b.sf, b.s_dec, b.row_shift, D)
     _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
                     canonicalize_1024, stream), "fp4_gemm")
     return D
@@ -427,6 +469,7 @@ def fp8_gemm(q8a, s8a, q8b, s8b, out_dtype=torch.float32, out=None, stream=None)
     for t, name in ((s8a, "s8a"), (s8b, "s8b")):
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise ValueError(f"fp8_gemm: {name} must be a contiguous float32 tensor")
+    _need_cuda("fp8_gemm", q8a, s8a, q8b, s8b, out)
     M, K = q8a.shape
     N = q8b.shape[0]
     if q8b.shape[1] != K or s8a.numel() != M * (K // 128) or s8b.numel() != N * (K // 128):
@@ -451,6 +494,7 @@ def dequantize(c, stream=None):
     scale layout (the tensor scale c.s_dec left out); exact."""
     if c.sf_layout != FP4_SF_PLAIN:
         raise ValueError("dequantize: the copy needs the plain scale layout")
+    _need_cuda("dequantize", c.q, c.sf)
     y = torch.empty((c.rows, c.k), dtype=torch.bfloat16, device=c.q.device)
     _check(fp4_dequantize(c.q, c.sf, c.format, c.rows, c.k, y, stream), "fp4_dequantize")
     return y
@@ -478,6 +522,7 @@ def gemm_bf16(a, b, s_dec_a, s_dec_b, out_dtype=torch.float32, out=None,
     for t, name in ((s_dec_a, "s_dec_a"), (s_dec_b, "s_dec_b")):
         if t.dtype != torch.float32 or t.numel() < 1:
             raise ValueError(f"gemm_bf16: {name} must be a float32 tensor")
+    _need_cuda("gemm_bf16", a, b, s_dec_a, s_dec_b, out)
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
@@ -503,6 +548,9 @@ def gemm_quantize(a, b, amax_dev, p, remap=True, canonicalize_1024=False, stream
     """Row-wise FP4 copy of y = alpha * A B^T, quantised in the GEMM epilogue
     (the product is never stored).  Returns a Quantized of y [M, N]."""
     _check_operands(a, b, "gemm_quantize")
+    _need_f32("gemm_quantize", amax_dev)
+    _need_cuda("gemm_quantize", a.q, a.sf, a.s_dec, a.row_shift, b.q, b.sf, b.s_dec, b.row_shift,
+               amax_dev)
     M, N, K = a.rows, b.rows, a.k
     out = _alloc_copy(M, N, p, a.q.device, _want_shift(p, remap))
     _check(fp4_gemm_quantize(a.operand(), b.operand(), M, N, K, amax_dev, p, out.q, out.sf,

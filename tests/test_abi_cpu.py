@@ -255,3 +255,38 @@ def test_mma_loop_argument_errors_before_any_launch(L):
     assert f(-1, 100, None) == 1
     assert f(fq.FP4_MMA_FP4, 0, None) == 1
     assert f(fq.FP4_MMA_FP4, 1000001, None) == 1
+
+
+def test_wrappers_reject_host_tensors_and_wrong_dtypes_before_any_launch(L):
+    """A host tensor's pointer never reaches a kernel: every allocating
+    wrapper checks device, dtype and layout first (these tensors live on the
+    CPU, so any launch would be an error)."""
+    x = torch.zeros((64, 64), dtype=torch.bfloat16)
+    one = torch.ones(1)
+    p = fq.params()
+    for call in (lambda: fq.amax(x), lambda: fq.amax_stripes(x), lambda: fq.amax_many([x]),
+                 lambda: fq.quantize(x, one, p), lambda: fq.quantize_transpose(x, one, one, p)):
+        with pytest.raises(ValueError, match="CUDA"):
+            call()
+    for bad in (x.float(), x[:, :32], torch.zeros(64, dtype=torch.bfloat16)):
+        with pytest.raises(ValueError, match="bfloat16"):
+            fq.quantize(bad, one, p)
+    with pytest.raises(ValueError, match="float32"):
+        fq.quantize(x, torch.ones(1, dtype=torch.float64), p)
+    q = torch.zeros((128, 64), dtype=torch.uint8)
+    sf = torch.zeros((128, 4), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.mxfp4_to_fp8(q, sf)
+    with pytest.raises(ValueError, match="uint8"):
+        fq.mxfp4_to_fp8(q.int(), sf)
+    q8 = torch.zeros((128, 128), dtype=torch.uint8)
+    s8 = torch.ones((128, 1))
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.fp8_gemm(q8, s8, q8, s8)
+    a = torch.zeros((128, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.gemm_bf16(a, a, one, one)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.gemm(_cpu_operand(64, 128), _cpu_operand(32, 128))
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.dequantize(_cpu_operand(64, 128, layout=fq.FP4_SF_PLAIN))
