@@ -43,7 +43,11 @@
 //   warps 6-13 epilogue (both CTAs): each CTA drains its own 128 x 256
 //           accumulator, releases it to the leader, then scales and stores
 //           (or, with the fused output producer, quantises each row's 128
-//           columns to their FP4 copy: qout.cuh).
+//           columns to their FP4 copy: qout.cuh).  When no cluster gets a
+//           second tile (LEAN), nothing waits for the release, and the
+//           drain works on two 32-column chunks at a time: holding all
+//           128 columns spills to local memory, which costs a single-tile
+//           product ~2 us.
 // Every wait is bounded (about one second); on expiry the CTA raises the
 // timeout status bit, marks both CTAs as aborting, drains what it issued and
 // leaves through the final cluster barrier, which keeps each CTA's shared and
@@ -230,7 +234,7 @@ __device__ __forceinline__ uint32_t idesc_pair(uint32_t a_sf_id, uint32_t b_sf_i
   return d;
 }
 
-template <int FMT, bool QOUT>
+template <int FMT, bool QOUT, bool LEAN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                 const Params p) {
@@ -568,21 +572,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
       };
-      uint32_t acc[4][32];
+      if (LEAN) {
+        // At most one tile per cluster: nothing waits for the accumulator,
+        // so two 32-column chunks at a time stay within the register budget
+        // (holding all four spills to local memory).
+        uint32_t a0[32], a1[32];
+        tc_ld_32cols_nw(taddr, a0);
+        tc_ld_32cols_nw(taddr + 32, a1);
+        tc_wait_ld();
+        if (QOUT) ql.reset();
+        emit(0, a0, sh0);
+        tc_ld_32cols_nw(taddr + 64, a0);
+        tc_wait_ld();
+        emit(1, a1, sh1);
+        tc_ld_32cols_nw(taddr + 96, a1);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+        acc_phase ^= 1u;
+        load_shifts(nbase + 64, sh0);
+        load_shifts(nbase + 96, sh1);
+        emit(2, a0, sh0);
+        emit(3, a1, sh1);
+      } else {
+        // all 128 columns into registers, release, then convert and store:
+        // the next tile's MMAs start as early as possible
+        uint32_t acc[4][32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-      acc_phase ^= 1u;
-      if (QOUT) ql.reset();
-      emit(0, acc[0], sh0);
-      emit(1, acc[1], sh1);
-      load_shifts(nbase + 64, sh0);
-      load_shifts(nbase + 96, sh1);
-      emit(2, acc[2], sh0);
-      emit(3, acc[3], sh1);
+        for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+        acc_phase ^= 1u;
+        if (QOUT) ql.reset();
+        emit(0, acc[0], sh0);
+        emit(1, acc[1], sh1);
+        load_shifts(nbase + 64, sh0);
+        load_shifts(nbase + 96, sh1);
+        emit(2, acc[2], sh0);
+        emit(3, acc[3], sh1);
+      }
       if (QOUT && nbase < p.N) ql.flush(p.qo, p.M, p.N, m, grp_m, k4, nbase);
     }
   }
@@ -603,8 +634,11 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters[64] = {0};
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
   int dev = 0;
@@ -615,12 +649,17 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT, QOUT>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT, QOUT, false>, &cfg) != cudaSuccess ||
+        n <= 0)
       return FP4_ERR_CUDA;
     max_clusters[dev] = n;
   }
   const int64_t nc = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
-  k_gemm_pair<FMT, QOUT><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  // one tile per cluster at most: the lean epilogue (no early release needed)
+  if (tiles <= max_clusters[dev])
+    k_gemm_pair<FMT, QOUT, true><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  else
+    k_gemm_pair<FMT, QOUT, false><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
