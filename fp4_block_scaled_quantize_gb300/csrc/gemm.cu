@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
       // Fused producer: the row-wise FP4 copy of this lane's 128 output
       // columns (qout.cuh), written once all four chunks are encoded.
-      QoutLane ql;
+      QoutLane<4> ql;
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform

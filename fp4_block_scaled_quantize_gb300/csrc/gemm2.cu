@@ -14,7 +14,7 @@
 // pair reading each other's halves) needs 9.5 KB per SM per step, under
 // 135 cycles.
 //
-// Kernel (clusters of two CTAs, one CTA per SM, 448 threads per CTA):
+// Kernel (clusters of two CTAs, one CTA per SM, 736 threads per CTA):
 //   warp 0  TMA producer (both CTAs): per 256-element K step its own A and B
 //           halves [128 x 128 B] by tensor TMA, the A scale tiles of its own
 //           128 rows and the B scale tiles of all 256 rows by bulk copy, onto
@@ -30,7 +30,7 @@
 //           peer's arrival ~200 ns, so a lockstep hand-off per stage (as a
 //           named barrier with the MMA warp would impose) tripled the time
 //           of a stage;
-//   warp 14 waiter (leader CTA only): polls the stage's ready barrier (and,
+//   warp 22 waiter (leader CTA only): polls the stage's ready barrier (and,
 //           at the start of a tile, the accumulator-empty barrier) and hands
 //           the stage to the MMA warp through a named barrier.  Measured on
 //           this part, a shared-memory barrier poll by the thread that
@@ -40,14 +40,13 @@
 //           tcgen05.mma.cta_group::2 (M256 N256 K64) from one thread, a
 //           commit multicast to both CTAs' empty barriers, and at the end of
 //           a tile to both CTAs' accumulator barriers;
-//   warps 6-13 epilogue (both CTAs): each CTA drains its own 128 x 256
+//   warps 6-21 epilogue (both CTAs): each CTA drains its own 128 x 256
 //           accumulator, releases it to the leader, then scales and stores
 //           (or, with the fused output producer, quantises each row's 128
-//           columns to their FP4 copy: qout.cuh).  When no cluster gets a
-//           second tile (LEAN), nothing waits for the release, and the
-//           drain works on two 32-column chunks at a time: holding all
-//           128 columns spills to local memory, which costs a single-tile
-//           product ~2 us.
+//           columns to their FP4 copy: qout.cuh).  Four warps per lane
+//           quadrant, 64 columns each: with eight, each thread held 128
+//           accumulator values and spilled to local memory, which made
+//           each tile's drain several microseconds long.
 // Every wait is bounded (about one second); on expiry the CTA raises the
 // timeout status bit, marks both CTAs as aborting, drains what it issued and
 // leaves through the final cluster barrier, which keeps each CTA's shared and
@@ -82,7 +81,7 @@ constexpr int SFB_BYTES = 2 * 4 * 512;     // both 128-row groups of the pair's 
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 38 KB
 constexpr int NBARS = 3 * STAGES + 3;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 8 * NBARS + 16;  // + flag, tmem
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;  // four per lane quadrant, 64 columns each
 constexpr int SF_WARPS = 4;
 constexpr int WAITER_WARP = 2 + SF_WARPS + EPI_WARPS;  // the last warp
 constexpr int THREADS = 32 * (WAITER_WARP + 1);
@@ -234,7 +233,7 @@ __device__ __forceinline__ uint32_t idesc_pair(uint32_t a_sf_id, uint32_t b_sf_i
   return d;
 }
 
-template <int FMT, bool QOUT, bool LEAN>
+template <int FMT, bool QOUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                 const Params p) {
@@ -472,11 +471,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 2 + SF_WARPS) {
     // --------------------------------------------------------------- epilogue
-    // Each warp reads its lane quadrant (warp % 4) and one half of the 256
-    // accumulator columns into registers, releases the accumulator to the
-    // leader's MMA warp, and only then scales, converts and stores.
+    // Each warp reads its lane quadrant (warp % 4) and one quarter of the
+    // 256 accumulator columns into registers (64 per thread: holding more
+    // spills to local memory), releases the accumulator to the leader's MMA
+    // warp, and only then scales, converts and stores.
     const int quad = warp & 3;
-    const int half = (warp - 2 - SF_WARPS) >> 2;
+    const int quarter = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
     // alpha: one per GEMM, or per (A stripe, B stripe) of 128 rows each
     float alpha = p.stripes ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
@@ -500,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = cid; tile < ntiles; tile += ncl) {
       const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
       const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
-      const int64_t nbase = (int64_t)nt * PAIR_N + 128 * half;
+      const int64_t nbase = (int64_t)nt * PAIR_N + 64 * quarter;
       uint32_t sh0[8], sh1[8];
       load_shifts(nbase, sh0);
       load_shifts(nbase + 32, sh1);
@@ -509,18 +509,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 64 * quarter;
       const int64_t m_row0 = (int64_t)mt * PAIR_M + (int64_t)rank * HALF;
       const int64_t m = m_row0 + row_in_tile;
-      if (p.stripes) {  // this CTA's rows: A stripe m_row0 / 128; its columns: B stripe 2 nt + half
+      if (p.stripes) {  // this CTA's rows: A stripe m_row0 / 128; its columns: B stripe 2 nt + quarter / 2
         const int64_t sa_i = min(m_row0 / 128, (p.M + 127) / 128 - 1);
-        const int64_t sb_i = min((int64_t)nt * 2 + half, (p.N + 127) / 128 - 1);
+        const int64_t sb_i = min((int64_t)nt * 2 + (quarter >> 1), (p.N + 127) / 128 - 1);
         alpha = __fmul_rn(__ldg(p.sda + sa_i), __ldg(p.sdb + sb_i));
       }
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
       const int k4 = lane & 3;
       const int64_t grp_m = m_row0 + quad * 32 + (lane & ~3);
-      QoutLane ql;  // fused producer: this lane's 128 output columns of row m
+      QoutLane<2> ql;  // fused producer: this lane's 64 output columns of row m
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
         const int64_t n0 = nbase + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform
@@ -572,48 +572,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
       };
-      if (LEAN) {
-        // At most one tile per cluster: nothing waits for the accumulator,
-        // so two 32-column chunks at a time stay within the register budget
-        // (holding all four spills to local memory).
-        uint32_t a0[32], a1[32];
-        tc_ld_32cols_nw(taddr, a0);
-        tc_ld_32cols_nw(taddr + 32, a1);
-        tc_wait_ld();
-        if (QOUT) ql.reset();
-        emit(0, a0, sh0);
-        tc_ld_32cols_nw(taddr + 64, a0);
-        tc_wait_ld();
-        emit(1, a1, sh1);
-        tc_ld_32cols_nw(taddr + 96, a1);
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-        acc_phase ^= 1u;
-        load_shifts(nbase + 64, sh0);
-        load_shifts(nbase + 96, sh1);
-        emit(2, a0, sh0);
-        emit(3, a1, sh1);
-      } else {
-        // all 128 columns into registers, release, then convert and store:
-        // the next tile's MMAs start as early as possible
-        uint32_t acc[4][32];
+      uint32_t acc[2][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-        acc_phase ^= 1u;
-        if (QOUT) ql.reset();
-        emit(0, acc[0], sh0);
-        emit(1, acc[1], sh1);
-        load_shifts(nbase + 64, sh0);
-        load_shifts(nbase + 96, sh1);
-        emit(2, acc[2], sh0);
-        emit(3, acc[3], sh1);
-      }
+      for (int q = 0; q < 2; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      acc_phase ^= 1u;
+      if (QOUT) ql.reset();
+      emit(0, acc[0], sh0);
+      emit(1, acc[1], sh1);
       if (QOUT && nbase < p.N) ql.flush(p.qo, p.M, p.N, m, grp_m, k4, nbase);
     }
   }
@@ -634,11 +603,8 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters[64] = {0};
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(k_gemm_pair<FMT, QOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return FP4_ERR_CUDA;
   int dev = 0;
@@ -649,17 +615,12 @@ fp4_status launch_fmt(const CUtensorMap &ma, const CUtensorMap &mb, const Params
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT, QOUT, false>, &cfg) != cudaSuccess ||
-        n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<FMT, QOUT>, &cfg) != cudaSuccess || n <= 0)
       return FP4_ERR_CUDA;
     max_clusters[dev] = n;
   }
   const int64_t nc = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
-  // one tile per cluster at most: the lean epilogue (no early release needed)
-  if (tiles <= max_clusters[dev])
-    k_gemm_pair<FMT, QOUT, true><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
-  else
-    k_gemm_pair<FMT, QOUT, false><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+  k_gemm_pair<FMT, QOUT><<<(unsigned)(2 * nc), THREADS, SMEM_BYTES, s>>>(ma, mb, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 

@@ -2,12 +2,13 @@
 // gemm2.cu): the binary32 GEMM output y quantised to its row-wise FP4 copy
 // instead of being stored ("Format-Aware Fusion for Fast FP4 Pretraining",
 // Abstract: the producer co-designed with its consumer, where the data is).
-// Each epilogue lane owns one output row and, per tile, 128 consecutive
-// columns in four chunks of 32; blocks of 16 (or 32 for MXFP4) along N are
-// encoded exactly as fp4_quantize encodes a binary32 input (tensor scale from
-// the held amax and T, block scale, RNE or Philox SR with counter group
-// (m N + n) >> 4 and copy 0, zero-scale rule), then written as one 16-byte
-// payload piece per row and one 32-bit word of four scale codes at a time.
+// Each epilogue lane owns one output row and, per tile, NQ chunks of 32
+// consecutive columns (four on one SM, two on SM pairs); blocks of 16 (or 32
+// for MXFP4) along N are encoded exactly as fp4_quantize encodes a binary32
+// input (tensor scale from the held amax and T, block scale, RNE or Philox
+// SR with counter group (m N + n) >> 4 and copy 0, zero-scale rule), then
+// written as 16-byte payload pieces and 32-bit words of four scale codes
+// (16-bit halves where a lane owns two codes of a word).
 #pragma once
 
 #include "formats.cuh"
@@ -43,16 +44,18 @@ __device__ __forceinline__ uint32_t block_scale_rt(int fmt, float b, float se, f
   return block_scale<kNVFP4>(b, se, sd, mult, zp);
 }
 
-// One lane's 128 output columns of one row: payload chunk q (16 bytes) in
-// words 4q .. 4q + 3 of qacc, scale codes four per word in qcodes.
+// One lane's 32 NQ output columns of one row: payload chunk q (16 bytes)
+// in words 4q .. 4q + 3 of qacc, scale codes four per word in qcodes.
+template <int NQ>
 struct QoutLane {
-  uint32_t qacc[16];
-  uint32_t qcodes[2];
+  uint32_t qacc[4 * NQ];
+  uint32_t qcodes[NQ / 2];
 
   __device__ __forceinline__ void reset() {
-    qcodes[0] = qcodes[1] = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) qacc[i] = 0u;
+    for (int i = 0; i < NQ / 2; ++i) qcodes[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4 * NQ; ++i) qacc[i] = 0u;
   }
 
   // Chunk q: columns n0 .. n0 + 31 of row m.
@@ -88,44 +91,68 @@ struct QoutLane {
           }
         }
       }
-      // code of scale column (q * nb + blk) of this lane's 128 columns
+      // code of scale column (q * nb + blk) of this lane's columns
       const int c = q * nb + blk;
       qcodes[c >> 2] |= code << (8 * (c & 3));
     }
   }
 
-  // Write the lane's 128 columns from nbase: four lanes (k4 = lane & 3 of a
-  // group whose first row is grp_m) exchange 16-byte chunks so each store
-  // instruction writes eight 64-byte row pieces; then this row's codes.
+  // One 16-byte payload piece (32 columns from n) of row mm; dst is 8-byte
+  // aligned (N % 16 == 0), 16-byte aligned when N % 32 == 0.
+  __device__ __forceinline__ static void store_piece(const QoutParams &o, int64_t N, int64_t mm,
+                                                     int64_t n, uint32_t w0, uint32_t w1,
+                                                     uint32_t w2, uint32_t w3) {
+    uint8_t *dst = o.q + mm * (N / 2) + n / 2;
+    if (n + 32 <= N && (N & 31) == 0) {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+    } else {
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(w0, w1);
+      if (n + 32 <= N) *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(w2, w3);
+    }
+  }
+
+  // Write the lane's columns from nbase, then this row's codes.  Four
+  // chunks: the four lanes of a group (k4 = lane & 3, first row grp_m)
+  // exchange 16-byte chunks so each store instruction writes eight 64-byte
+  // row pieces.  Two chunks: each lane writes its own row's 32 bytes.
   __device__ __forceinline__ void flush(const QoutParams &o, int64_t M, int64_t N, int64_t m,
                                         int64_t grp_m, int k4, int64_t nbase) {
-    tc::transpose4x16B(qacc, k4);
-    const int64_t n = nbase + 32 * k4;
+    if constexpr (NQ == 4) {
+      tc::transpose4x16B(qacc, k4);
+      const int64_t n = nbase + 32 * k4;
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int64_t mm = grp_m + rr;
-      if (mm >= M || n >= N) continue;
-      uint8_t *dst = o.q + mm * (N / 2) + n / 2;  // 8-byte aligned (N % 16 == 0)
-      if (n + 32 <= N && (N & 31) == 0) {
-        *reinterpret_cast<uint4 *>(dst) =
-            make_uint4(qacc[4 * rr], qacc[4 * rr + 1], qacc[4 * rr + 2], qacc[4 * rr + 3]);
-      } else {
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(qacc[4 * rr], qacc[4 * rr + 1]);
-        if (n + 32 <= N)
-          *reinterpret_cast<uint2 *>(dst + 8) = make_uint2(qacc[4 * rr + 2], qacc[4 * rr + 3]);
+      for (int rr = 0; rr < 4; ++rr) {
+        const int64_t mm = grp_m + rr;
+        if (mm >= M || n >= N) continue;
+        store_piece(o, N, mm, n, qacc[4 * rr], qacc[4 * rr + 1], qacc[4 * rr + 2],
+                    qacc[4 * rr + 3]);
+      }
+    } else if (m < M) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const int64_t n = nbase + 32 * q;
+        if (n < N)
+          store_piece(o, N, m, n, qacc[4 * q], qacc[4 * q + 1], qacc[4 * q + 2], qacc[4 * q + 3]);
       }
     }
     if (m >= M) return;
-    const int ncodes = 128 / o.qb;
+    // scale columns c0 .. c0 + ncodes - 1; ncodes is 2 only for MXFP4 on two
+    // chunks: half of a four-code word, starting at an even column
+    const int ncodes = 32 * NQ / o.qb;
     const int64_t c0 = nbase / o.qb;
-    for (int wd = 0; wd < ncodes / 4; ++wd) {
-      const int64_t col = c0 + 4 * wd;  // first of four scale columns
+    for (int wd = 0; 4 * wd < ncodes; ++wd) {
+      const int64_t col = c0 + 4 * wd;  // first scale column of this word
       if (col >= o.cb) break;
+      const int nc = ncodes - 4 * wd < 4 ? ncodes - 4 * wd : 4;
       if (o.sf_mma) {
         const int64_t off = ((m >> 7) * o.cp4 + (col >> 2)) * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4;
-        *reinterpret_cast<uint32_t *>(o.sf + off) = qcodes[wd];
+        if (nc == 4)
+          *reinterpret_cast<uint32_t *>(o.sf + off) = qcodes[wd];
+        else  // two codes at column col (col % 4 is 0 or 2): one 16-bit store
+          *reinterpret_cast<uint16_t *>(o.sf + off + (col & 3)) = (uint16_t)qcodes[wd];
       } else {
-        for (int c = 0; c < 4 && col + c < o.cb; ++c) o.sf[m * o.cb + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
+        for (int c = 0; c < nc && col + c < o.cb; ++c)
+          o.sf[m * o.cb + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
       }
     }
   }
