@@ -10,7 +10,7 @@
 // K in steps of one 64-element MMA into a binary32 accumulator in tensor
 // memory, the grouping the page's probe-matched model describes.
 //
-// Kernel (one persistent CTA per SM, 448 threads):
+// Kernel (one persistent CTA per SM, 704 threads):
 //   warp 0  TMA producer: per 256-element K step, A [128 x 128 B] and
 //           B [256 x 128 B] payload tiles (128-byte swizzle) by tensor TMA,
 //           plus the matching 512-byte scale tiles by bulk copy;
@@ -28,8 +28,8 @@
 //           the tensor pipe about as long as the MMAs that consume them, and
 //           the MMA warp's shared-memory barrier polls stall on a port the
 //           operand reads keep busy;
-//   warps 6-13 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
-//           (two warps per lane quadrant, 128 columns each), release, then
+//   warps 6-21 epilogue: tcgen05.ld of the 128 x 256 binary32 accumulator
+//           (four warps per lane quadrant, 64 columns each), release, then
 //           shift / canonicalise / alpha and BF16 or binary32 stores.
 // Tiles are walked n-fastest when B is the smaller operand (m-fastest
 // otherwise), so the CTAs of one wave share the streamed panel and the
@@ -87,7 +87,7 @@ constexpr int SFA_BYTES = 4 * 512;              // up to 4 scale tiles (block 16
 constexpr int SFB_BYTES = 2 * 4 * 512;          // two 128-row groups
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // 54 KB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quadrant
+constexpr int EPI_WARPS = 16;  // four per tensor-memory lane quadrant, 64 columns each
 constexpr int SF_WARPS = 4;    // one per tensor-memory lane quadrant
 constexpr int THREADS = 64 + 32 * SF_WARPS + 32 * EPI_WARPS;
 constexpr uint32_t kHandoffThreads = 32 * (1 + SF_WARPS);  // MMA warp + scale warps
@@ -574,12 +574,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 2 + SF_WARPS) {
     // --------------------------------------------------------------- epilogue
-    // Each warp reads its lane quadrant (warp % 4) and one half of the 256
-    // accumulator columns into registers, releases the accumulator to the
-    // MMA warp, and only then scales, converts and stores -- the stores of
-    // tile t overlap the MMAs of tile t + 1.
+    // Each warp reads its lane quadrant (warp % 4) and one quarter of the 256
+    // accumulator columns into registers (64 per thread: holding more
+    // spills to local memory), releases the accumulator to the MMA warp,
+    // and only then scales, converts and stores -- the stores of tile t
+    // overlap the MMAs of tile t + 1.
     const int quad = warp & 3;
-    const int half = (warp - 2 - SF_WARPS) >> 2;
+    const int quarter = (warp - 2 - SF_WARPS) >> 2;
     const int row_in_tile = quad * 32 + lane;
     // alpha: one per GEMM, or per (A stripe, B stripe) of 128 rows each
     float alpha = (FMT == kFP8 || p.stripes) ? 1.0f : __fmul_rn(__ldg(p.sda), __ldg(p.sdb));
@@ -604,18 +605,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
       const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
-      // column shifts of the first 64 columns, fetched before the wait
-      const int64_t nbase = (int64_t)nt * BN + 128 * half;
+      // column shifts of this warp's 64 columns, fetched before the wait
+      const int64_t nbase = (int64_t)nt * BN + 64 * quarter;
       uint32_t sh0[8], sh1[8];
       load_shifts(nbase, sh0);
       load_shifts(nbase + 32, sh1);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 128 * half;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ACC_COL + 64 * quarter;
       const int64_t m = (int64_t)mt * BM + row_in_tile;
       const int sa = (p.sha && m < p.M) ? (int)__ldg(p.sha + m) : 0;
-      if (p.stripes) {  // this warp's rows: A stripe mt; its 128 columns: B stripe 2 nt + half
-        const int64_t sb = min((int64_t)nt * 2 + half, (p.N + 127) / 128 - 1);
+      if (p.stripes) {  // this warp's rows: A stripe mt; its 64 columns: B stripe 2 nt + quarter / 2
+        const int64_t sb = min((int64_t)nt * 2 + (quarter >> 1), (p.N + 127) / 128 - 1);
         alpha = __fmul_rn(__ldg(p.sda + mt), __ldg(p.sdb + sb));
       }
       // Output: each lane's row segment of 32 values is exchanged within its
@@ -623,11 +624,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // 64-byte row pieces instead of 32 scattered 16-byte pieces.
       const int k4 = lane & 3;
       const int64_t grp_m = (int64_t)mt * BM + quad * 32 + (lane & ~3);
-      // Fused producer: the row-wise FP4 copy of this lane's 128 output
-      // columns (qout.cuh), written once all four chunks are encoded.
-      QoutLane<4> ql;
+      // Fused producer: the row-wise FP4 copy of this lane's 64 output
+      // columns (qout.cuh), written once both chunks are encoded.
+      QoutLane<2> ql;
       auto emit = [&](int q, const uint32_t(&r)[32], const uint32_t(&sh)[8]) {
-        const int64_t n0 = (int64_t)nt * BN + 128 * half + 32 * q;
+        const int64_t n0 = nbase + 32 * q;
         if (n0 >= p.N) return;  // warp-uniform
         float y[32];
 #pragma unroll
@@ -677,10 +678,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       };
-      uint32_t acc[4][32];
-      // all 128 columns of this warp's half into registers, then release
+      uint32_t acc[2][32];
+      // all 64 columns of this warp's quarter into registers, then release
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
+      for (int q = 0; q < 2; ++q) tc_ld_32cols_nw(taddr + 32 * q, acc[q]);
       tc_wait_ld();
       tc_fence_before();
       mbar_arrive(acc_empty);
@@ -688,10 +689,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (QOUT) ql.reset();
       emit(0, acc[0], sh0);
       emit(1, acc[1], sh1);
-      load_shifts(nbase + 64, sh0);
-      load_shifts(nbase + 96, sh1);
-      emit(2, acc[2], sh0);
-      emit(3, acc[3], sh1);
       if (QOUT && nbase < p.N) ql.flush(p.qo, p.M, p.N, m, grp_m, k4, nbase);
     }
   }
