@@ -173,14 +173,16 @@ __device__ __forceinline__ void write_scales(const uint8_t (*sfs)[8], uint8_t *s
 
 // SR: the kernel carries the stochastic-rounding code (dY); the RNE-only
 // instantiations leave it out, which keeps them small in the instruction cache.
-// Resident CTAs per SM: four for the nearest-even instantiations (64
+// Resident CTAs per SM: four for the plain nearest-even instantiations (64
 // registers); three under SR, whose Philox state needs the registers (80:
-// measured 8% faster on dY than four CTAs with spills).
-template <bool SR>
-constexpr int ctas_per_sm() { return SR ? 3 : 4; }
+// measured 8% faster on dY than four CTAs with spills), and three with the
+// Hadamard rotation, whose 64 rotated values per lane spilled at 64
+// registers (8192 x 8192: MXFP4 + H32 82 -> 66 us, UE5M3 + H16 102 -> 79 us).
+template <bool SR, int HAD>
+constexpr int ctas_per_sm() { return (SR || HAD != 0) ? 3 : 4; }
 
 template <int FMT, int HAD, bool TWO_D, bool SR>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<SR>())
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<SR, HAD>()))
     k_quantize(const __grid_constant__ CUtensorMap tmap, Params p) {
   constexpr int B = Fmt<FMT>::B;
   constexpr int NSC = kTile / B;                    // scale columns per tile
@@ -655,7 +657,7 @@ bool tile_map(CUtensorMap *m, const void *x, int64_t R, int64_t C) {
 
 template <int FMT, int HAD, bool TWO_D, bool SR>
 fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
-  // ctas_per_sm<SR>() resident CTAs per SM, each walking tiles
+  // ctas_per_sm<SR, HAD>() resident CTAs per SM, each walking tiles
   static int sms[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4_ERR_CUDA;
@@ -674,7 +676,7 @@ fp4_status launch_t(const Params &p, int64_t tiles, cudaStream_t s) {
   if (attr != cudaSuccess) return FP4_ERR_CUDA;
   CUtensorMap map;
   if (!tile_map(&map, p.x, p.R, p.C)) return FP4_ERR_CUDA;
-  const int64_t cap = ctas_per_sm<SR>() * (int64_t)sms[dev];
+  const int64_t cap = ctas_per_sm<SR, HAD>() * (int64_t)sms[dev];
   kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kDynSmem, s>>>(map, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
