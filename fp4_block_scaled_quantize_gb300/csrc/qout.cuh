@@ -58,17 +58,28 @@ struct QoutLane {
     for (int i = 0; i < 4 * NQ; ++i) qacc[i] = 0u;
   }
 
-  // Chunk q: columns n0 .. n0 + 31 of row m.
+  // Chunk q: columns n0 .. n0 + 31 of row m.  The block size is a
+  // compile-time constant of each branch, so every index into y, qacc and
+  // qcodes is static and the lane's state stays in registers.
   __device__ __forceinline__ void quant(const QoutParams &o, int64_t N, int64_t m, int q,
                                         int64_t n0, const float (&y)[32], float se, float sd) {
-    const int nb = 32 / o.qb;
+    if (o.qb == 16)
+      quant_b<16>(o, N, m, q, n0, y, se, sd);
+    else
+      quant_b<32>(o, N, m, q, n0, y, se, sd);
+  }
+
+  template <int QB>
+  __device__ __forceinline__ void quant_b(const QoutParams &o, int64_t N, int64_t m, int q,
+                                          int64_t n0, const float (&y)[32], float se, float sd) {
+    constexpr int NB = 32 / QB;
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      if (blk >= nb) break;
+    for (int blk = 0; blk < NB; ++blk) {
       uint32_t code = 0u;
-      const int QB = o.qb, off = blk * QB;
+      const int off = blk * QB;
       if (n0 + off < N) {
         float b = 0.0f;
+#pragma unroll
         for (int j = 0; j < QB; ++j) b = fmaxf(b, fabsf(y[off + j]));
         float mult;
         bool zp;
@@ -76,6 +87,7 @@ struct QoutLane {
         // 8 values at a time; under SR one Philox block covers 16 elements
         // of the output row (words x, y for its first 8)
         uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
         for (int h = 0; h < QB / 8; ++h) {
           float v[8];
 #pragma unroll
@@ -91,8 +103,8 @@ struct QoutLane {
           }
         }
       }
-      // code of scale column (q * nb + blk) of this lane's columns
-      const int c = q * nb + blk;
+      // code of scale column (q * NB + blk) of this lane's columns
+      const int c = q * NB + blk;
       qcodes[c >> 2] |= code << (8 * (c & 3));
     }
   }
@@ -136,14 +148,24 @@ struct QoutLane {
       }
     }
     if (m >= M) return;
-    // scale columns c0 .. c0 + ncodes - 1; ncodes is 2 only for MXFP4 on two
-    // chunks: half of a four-code word, starting at an even column
-    const int ncodes = 32 * NQ / o.qb;
-    const int64_t c0 = nbase / o.qb;
-    for (int wd = 0; 4 * wd < ncodes; ++wd) {
+    if (o.qb == 16)
+      flush_codes<16>(o, m, nbase);
+    else
+      flush_codes<32>(o, m, nbase);
+  }
+
+  // This row's scale codes of the lane's columns: columns c0 .. c0 + NC - 1;
+  // NC is 2 only for MXFP4 on two chunks (half of a four-code word,
+  // starting at an even column).
+  template <int QB>
+  __device__ __forceinline__ void flush_codes(const QoutParams &o, int64_t m, int64_t nbase) {
+    constexpr int NC = 32 * NQ / QB;
+    const int64_t c0 = nbase / QB;
+#pragma unroll
+    for (int wd = 0; 4 * wd < NC; ++wd) {
       const int64_t col = c0 + 4 * wd;  // first scale column of this word
       if (col >= o.cb) break;
-      const int nc = ncodes - 4 * wd < 4 ? ncodes - 4 * wd : 4;
+      constexpr int nc = NC < 4 ? NC : 4;
       if (o.sf_mma) {
         const int64_t off = ((m >> 7) * o.cp4 + (col >> 2)) * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4;
         if (nc == 4)
@@ -151,8 +173,9 @@ struct QoutLane {
         else  // two codes at column col (col % 4 is 0 or 2): one 16-bit store
           *reinterpret_cast<uint16_t *>(o.sf + off + (col & 3)) = (uint16_t)qcodes[wd];
       } else {
-        for (int c = 0; c < nc && col + c < o.cb; ++c)
-          o.sf[m * o.cb + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
+#pragma unroll
+        for (int c = 0; c < nc; ++c)
+          if (col + c < o.cb) o.sf[m * o.cb + col + c] = (uint8_t)(qcodes[wd] >> (8 * c));
       }
     }
   }
