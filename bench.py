@@ -318,10 +318,18 @@ def summarize_layer(fmt, m, pk, world):
         per_producer[k] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
                            "frac": round(gbs / pk["hbm_gbs"], 4)}
     per_gemm = {}
+    B = 32 if fmt in (2, 3) else 16
     for k in ("fprop", "dgrad", "wgrad"):
         tf = flops[k] / (avg[k] * 1e-3) / 1e12
+        # applicable roofline: the larger of the math time and the time to
+        # move the operands and the output (FP32 outputs are not free)
+        Mg, Ng, Kg, ob = gemms[k]
+        gbytes = (Mg + Ng) * Kg * (0.5 + 1.0 / B) + Mg * Ng * ob
+        t_roof = max(flops[k] / (fp4_peak * 1e12), gbytes / hbm)
         per_gemm[k] = {"ms": round(avg[k], 4), "tflops": round(tf, 1),
-                       "frac": round(tf / fp4_peak, 4)}
+                       "frac": round(tf / fp4_peak, 4),
+                       "roofline_us": round(t_roof * 1e6, 1),
+                       "frac_of_applicable_roofline": round(t_roof / (avg[k] * 1e-3), 4)}
     return {
         "ideal_s": ideal,
         "value": 100.0 * ideal / (m["step_ms"] * 1e-3) * world,
