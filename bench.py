@@ -996,7 +996,7 @@ def run_e2e(layer, args, world, ideal, graph=None):
                  for k, t in (("Y", L.Y), ("dX", L.dX), ("dW", L.dW))} for L in sets]
     h2d = sum(t.numel() * t.element_size() for t in layer.host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
-    steps = max(2, min(args.steps, 20))
+    steps = max(2, min(args.steps, 60))  # amortises the pipeline's fill and drain
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
