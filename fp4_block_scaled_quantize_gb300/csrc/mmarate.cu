@@ -111,10 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_mma_loop(int64_t iters, uint32_
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // block-16 FP4 scales: one 4-column atom per K64 step; FP8: the
-          // same atom, byte kk
+          // same atom, scale byte kk (bits 4-5 and 29-30 of the descriptor)
           const uint32_t a = KIND == FP4_MMA_FP4 ? (uint32_t)kk : 0u;
-          mma<KIND>(tmem, da + 2 * kk, db + 2 * kk, KIND == FP4_MMA_FP8 ? id | ((uint32_t)kk << 4) | ((uint32_t)kk << 29) : id,
-                    tmem + kSfCol + 4 * a, tmem + kSfCol + 16 + 8 * a, (uint32_t)(it | kk) != 0);
+          const uint32_t d =
+              KIND == FP4_MMA_FP8 ? id | ((uint32_t)kk << 4) | ((uint32_t)kk << 29) : id;
+          mma<KIND>(tmem, da + 2 * kk, db + 2 * kk, d, tmem + kSfCol + 4 * a,
+                    tmem + kSfCol + 16 + 8 * a, (uint32_t)(it | kk) != 0);
         }
       }
       tc_commit(smem_u32(&done));
