@@ -182,3 +182,38 @@ def test_out_of_window_rows_through_the_exact_path():
     _, ye, s_abs = orc.gemm_model(ca["q"], ca["sf"], cb["q"], cb["sf"], orc.UE5M3, K,
                                   ca["s_dec"], cb["s_dec"], mm.ravel(), nn.ravel())
     check_exact(y.cpu().numpy().astype(np.float64).ravel(), ye, s_abs, K, False)
+
+
+def test_exact_path_full_size_fprop():
+    """The 8B down_proj fprop (8192 x 4096 x 14336) through the exact path,
+    the way bench.py times it: plain-layout UE5M3-b16 copies of X and W from
+    the producer, both dequantised, the BF16 GEMM with BF16 output.  The
+    copies and sampled rows of the dequantisation against the oracle bit for
+    bit; 2048 sampled outputs (every 128 x 256 tile corner in budget) against
+    the oracle's exact product."""
+    need_gpu()
+    from test_gemm_gpu import sample_indices
+    d = inputs.down_proj_8b()
+    X, W = d["X"], d["W"]
+    M, K, N = X.shape[0], X.shape[1], W.shape[0]
+    xg, wg = X.cuda(), W.cuda()
+    plain = fq.params(format=fq.FP4_FMT_UE5M3_B16, sf_layout=fq.FP4_SF_PLAIN)
+    a, b = fq.quantize(xg, fq.amax(xg)[0], plain), fq.quantize(wg, fq.amax(wg)[0], plain)
+    ya, yb = fq.dequantize(a), fq.dequantize(b)
+    y = fq.gemm_bf16(ya, yb, a.s_dec, b.s_dec, out_dtype=torch.bfloat16)
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    x32, w32 = f32(X), f32(W)
+    ca = orc.quantize(x32, float(np.abs(x32).max()), orc.UE5M3)
+    cb = orc.quantize(w32, float(np.abs(w32).max()), orc.UE5M3)
+    mismatch_report(np_u8(a.q), ca["q"], "q_x")
+    mismatch_report(np_u8(a.sf).reshape(ca["sf"].shape), ca["sf"], "sf_x")
+    mismatch_report(np_u8(b.q), cb["q"], "q_w")
+    rows = np.array([0, 1, 127, 128, 4095, 8191])
+    want = orc.dequantize(ca["q"][rows], ca["sf"][rows], orc.UE5M3)
+    mismatch_report(ya[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64),
+                    want, "dequantised rows")
+    mi, ni = sample_indices(M, N, 2048, seed=3)
+    _, ye, s_abs = orc.gemm_model(ca["q"], ca["sf"], cb["q"], cb["sf"], orc.UE5M3, K,
+                                  ca["s_dec"], cb["s_dec"], mi, ni)
+    g = y.float().cpu().numpy()[mi, ni].astype(np.float64)
+    check_exact(g, ye, s_abs, K, True)
