@@ -369,6 +369,7 @@ def run_gpu(args, world, rank, local):
     fused = run_fused_producer(layer, flush)
     reencode = run_reencode(layer, flush, pk["hbm_gbs"])
     linear = run_linear(layer, flush)
+    feed = run_gemm_feed(layer, flush)
     e2e = run_e2e(layer, args, world, ideal, graph)
     out_dtypes = run_out_dtypes(layer, flush, flops, fp4_peak)
     host = layer.host
@@ -382,6 +383,7 @@ def run_gpu(args, world, rank, local):
     del host
     configs = run_configs(dev, flush, pk)
     ceiling = run_mma_ceiling(dom_tflops)
+    ceiling["gemm_feed"] = feed
 
     clocks = clk.summary()
     out = {
@@ -601,6 +603,45 @@ def run_mma_ceiling(dominant_tflops):
     for name, kind in (("fp4", fq.FP4_MMA_FP4), ("fp8", fq.FP4_MMA_FP8), ("bf16", fq.FP4_MMA_BF16)):
         out[name + "_tflops"] = round(fq.mma_loop_tflops(kind), 1)
     out["dominant_gemm_frac_of_fp4_loop"] = round(dominant_tflops / out["fp4_tflops"], 4)
+    return out
+
+
+def run_gemm_feed(layer, flush, reps=5):
+    """Each GEMM of the step against its own copies into shared memory
+    (gemm_copies: the same tiles, boxes, scale tiles and ring, no MMA and no
+    output), both L2-flushed, median of `reps`: the share of the GEMM's time
+    that filling its shared memory takes, and the fill rate per SM it implies
+    (each CTA takes in 128 rows of A and of B and its scale tiles per K256
+    stage)."""
+    fq = layer.fq
+    sms = torch.cuda.get_device_properties(layer.X.device).multi_processor_count
+    stage = 2 * 16384 + 3 * (2 if layer.fmt == 2 else 4) * 512
+
+    def med(fn):
+        ts = []
+        for _ in range(reps + 1):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts = sorted(ts[1:])
+        return ts[len(ts) // 2]
+
+    out = {"what": "GEMM vs its own copies alone (fp4_gemm_copies), L2 flushed, median of %d" % reps,
+           "stage_bytes_per_cta": stage}
+    for k, a, b, D in (("fprop", layer.xr, layer.wr, layer.Y), ("dgrad", layer.dyr, layer.wc, layer.dX),
+                       ("wgrad", layer.dyc, layer.xc, layer.dW)):
+        t_g = med(lambda: fq.gemm(a, b, out=D))
+        t_c = med(lambda: fq.gemm_copies(a, b))
+        tiles = -(-a.rows // 256) * -(-b.rows // 256)
+        nbytes = tiles * -(-a.k // 256) * 2 * stage
+        out[k] = {"gemm_us": round(t_g * 1e3, 1), "copies_us": round(t_c * 1e3, 1),
+                  "copies_share": round(t_c / t_g, 3),
+                  "fill_gbs_per_sm": round(nbytes / sms / (t_c * 1e-3) / 1e9, 1)}
+    layer.fq._check(fq.fp4_status_sync(), "gemm_copies")
     return out
 
 

@@ -66,7 +66,7 @@ _lib = None
 EXPORTS = ("fp4_amax", "fp4_amax_many", "fp4_amax_stripes", "fp4_mxfp4_to_fp8",
            "fp4_mxfp4_to_fp8_transpose",
            "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm", "fp4_gemm_quantize",
-           "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16", "fp4_mma_loop", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
+           "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16", "fp4_mma_loop", "fp4_gemm_copies", "fp4_sf_bytes", "fp4_block_size", "fp4_status_sync",
            "fp4_status_string")
 
 
@@ -94,6 +94,7 @@ def lib():
         L.fp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, vp]
         L.fp4_dequantize.argtypes = [vp, vp, i32, i64, i64, vp, vp]
         L.fp4_mma_loop.argtypes = [i32, i64, vp]
+        L.fp4_gemm_copies.argtypes = [op, op, i64, i64, i64, vp]
         L.fp4_gemm_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i32, i32, vp]
         L.fp4_sf_bytes.argtypes = [i32, i64, i64, i32]
         L.fp4_sf_bytes.restype = i64
@@ -106,7 +107,7 @@ def lib():
                   "fp4_mxfp4_to_fp8_transpose",
                   "fp4_quantize", "fp4_quantize_transpose", "fp4_gemm",
                   "fp4_gemm_quantize", "fp4_fp8_gemm", "fp4_dequantize", "fp4_gemm_bf16",
-                  "fp4_mma_loop", "fp4_status_sync"):
+                  "fp4_mma_loop", "fp4_gemm_copies", "fp4_status_sync"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -216,6 +217,10 @@ def fp4_gemm_bf16(a, s_dec_a, b, s_dec_b, M, N, K, D, d_is_bf16, canonicalize_10
 
 def fp4_mma_loop(kind, iters, stream=None):
     return lib().fp4_mma_loop(int(kind), int(iters), _stream(stream))
+
+
+def fp4_gemm_copies(A, B, M, N, K, stream=None):
+    return lib().fp4_gemm_copies(ctypes.byref(A), ctypes.byref(B), M, N, K, _stream(stream))
 
 
 def mma_loop_tflops(kind, iters=20000, reps=5, stream=None):
@@ -458,6 +463,16 @@ def gemm(a, b, out_dtype=torch.float32, canonicalize_1024=False, out=None, strea
     _check(fp4_gemm(a.operand(), b.operand(), M, N, K, D, D.dtype == torch.bfloat16,
                     canonicalize_1024, stream), "fp4_gemm")
     return D
+
+
+def gemm_copies(a, b, stream=None):
+    """Diagnostic: the copies gemm(a, b) makes into shared memory (same
+    tiles, boxes, scale tiles and ring; M > 128), with no MMA and no output.
+    Timed against gemm on the same operands it gives the share of the GEMM's
+    time that filling its shared memory takes."""
+    _check_operands(a, b, "gemm_copies")
+    _need_cuda("gemm_copies", a.q, a.sf, a.s_dec, a.row_shift, b.q, b.sf, b.s_dec, b.row_shift)
+    _check(fp4_gemm_copies(a.operand(), b.operand(), a.rows, b.rows, a.k, stream), "fp4_gemm_copies")
 
 
 def fp8_gemm(q8a, s8a, q8b, s8b, out_dtype=torch.float32, out=None, stream=None):

@@ -363,6 +363,22 @@ fp4_status fp4_gemm(const fp4_operand *A, const fp4_operand *B, int64_t M, int64
   return launch_gemm(j, as_stream(stream));
 }
 
+fp4_status fp4_gemm_copies(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
+                           int64_t K, void *stream) {
+  fp4_status st = gemm_shapes(A, B, M, N, K);
+  if (st != FP4_OK) return st;
+  if (M == 0 || N == 0 || K == 0) return FP4_OK;
+  if (M <= 128) return FP4_ERR_UNSUPPORTED;  // the one-SM kernel has its own schedule
+  GemmJob j{};
+  st = gemm_operands(A, B, M, N, K, j);
+  if (st != FP4_OK) return st;
+  j.M = M;
+  j.N = N;
+  j.K = K;
+  j.fmt = kernel_format(A->format);
+  return launch_gemm_copies(j, as_stream(stream));
+}
+
 fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
                              int64_t K, const float *amax_dev, const fp4_quant_params *p,
                              uint8_t *q, uint8_t *sf, float *s_dec_dev, int8_t *row_shift,

@@ -157,6 +157,7 @@ struct Bf16GemmJob {
 fp4_status launch_gemm_bf16(const Bf16GemmJob &j, cudaStream_t s);
 // Tensor-pipe rate diagnostic: back-to-back MMAs on resident operands.
 fp4_status launch_mma_loop(int kind, int64_t iters, cudaStream_t s);
+fp4_status launch_gemm_copies(const GemmJob &j, cudaStream_t s);
 // FP4 copy (plain scale layout) -> BF16 values e2m1(q) * dec(sf); exact.
 fp4_status launch_dequant_bf16(const uint8_t *q, const uint8_t *sf, int64_t rows, int64_t cols,
                                int fmt, void *out, cudaStream_t s);

@@ -7,9 +7,18 @@
 // E8M0 scales per 32 elements, K32) and BF16 (kind::f16, K16).  The operands
 // are zero; the results are not read.  A diagnostic, not a step of the
 // method.
+//
+// k_gemm_copies: the other side of the GEMMs' roofline -- the pair GEMM's
+// copies alone.  Each CTA issues exactly the loads its producer warp in
+// k_gemm_pair issues (the same tile walk over the same clusters, the same
+// tensor boxes and bulk copies of scale tiles into the same five-stage ring
+// of 38,912-byte stages), with no MMA and no epilogue: a slot is refilled as
+// soon as its previous copies have landed.  The GEMM's time against this
+// one's says how much of it is the time its shared memory takes to fill.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "formats.cuh"
 #include "tcgen05.cuh"
 
 namespace fp4 {
@@ -148,7 +157,114 @@ fp4_status launch_kind(int64_t iters, uint32_t *status, int grid, cudaStream_t s
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
+// The pair GEMM's tiling and ring (k_gemm_pair): 256 x 256 tiles per SM
+// pair, 128 rows of A and of B per CTA, K256 stages, five of them.
+constexpr int kCpStages = 5;
+constexpr int kCpHalf = 128;
+constexpr int kCpBkb = 128;                                  // bytes of K per stage
+constexpr int kCpA = kCpHalf * kCpBkb, kCpB = kCpHalf * kCpBkb;
+constexpr int kCpSfa = 4 * 512, kCpSfb = 2 * 4 * 512;
+constexpr int kCpStage = kCpA + kCpB + kCpSfa + kCpSfb;     // 38,912
+constexpr int kCpSmem = kCpStages * kCpStage + 1024 + 8 * kCpStages + 16;
+
+struct CopyParams {
+  const uint8_t *sfa, *sfb;
+  int m_tiles, n_tiles, k_tiles, n_fast, apk;
+  int64_t cp4, ngrp_a, ngrp_b;
+  uint32_t *status;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32, 1)
+    k_gemm_copies(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                  const CopyParams p) {
+  extern __shared__ uint8_t cp_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(cp_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kCpStages * kCpStage);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + kCpStages);
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kCpStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+  *abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  uint32_t rank, cid, ncl;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cid));
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(ncl));
+  const int ntiles = p.m_tiles * p.n_tiles;
+  int64_t issued = 0;
+  bool ok = true;
+  for (int tile = (int)cid; ok && tile < ntiles; tile += (int)ncl) {
+    const int mt = p.n_fast ? tile / p.n_tiles : tile % p.m_tiles;
+    const int nt = p.n_fast ? tile % p.n_tiles : tile / p.m_tiles;
+    const int64_t ga = 2 * (int64_t)mt + rank;
+    const bool a_ok = ga < p.ngrp_a;
+    const bool g1 = (2 * (int64_t)nt + 1) < p.ngrp_b;
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++issued) {
+      const int stage = (int)(issued % kCpStages);
+      const uint32_t fb = smem_u32(&bars[stage]);
+      if (issued >= kCpStages &&
+          !mbar_wait(fb, (uint32_t)((issued / kCpStages - 1) & 1), abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t *st = smem + stage * kCpStage;
+      const uint32_t atoms = (uint32_t)min((int64_t)p.apk, p.cp4 - (int64_t)kt * p.apk);
+      mbar_expect_tx(fb, kCpA + kCpB + atoms * 512u * ((a_ok ? 1u : 0u) + 1u + (g1 ? 1u : 0u)));
+      tma_load_2d(smem_u32(st), &tma_a, fb, kt * kCpBkb, mt * 256 + (int)rank * kCpHalf);
+      tma_load_2d(smem_u32(st + kCpA), &tma_b, fb, kt * kCpBkb, nt * 256 + (int)rank * kCpHalf);
+      if (a_ok)
+        bulk_load(smem_u32(st + kCpA + kCpB), p.sfa + (ga * p.cp4 + (int64_t)kt * p.apk) * 512,
+                  atoms * 512u, fb);
+      const uint8_t *sfb0 = p.sfb + ((2 * (int64_t)nt) * p.cp4 + (int64_t)kt * p.apk) * 512;
+      bulk_load(smem_u32(st + kCpA + kCpB + kCpSfa), sfb0, atoms * 512u, fb);
+      if (g1)
+        bulk_load(smem_u32(st + kCpA + kCpB + kCpSfa + 4 * 512), sfb0 + p.cp4 * 512, atoms * 512u,
+                  fb);
+    }
+  }
+  // nothing may still be landing in shared memory when the CTA leaves
+  const int64_t first = issued > kCpStages ? issued - kCpStages : 0;
+  for (int64_t j = first; j < issued; ++j)
+    mbar_wait_drain(smem_u32(&bars[j % kCpStages]), (uint32_t)((j / kCpStages) & 1));
+}
+
 }  // namespace
+
+// The pair GEMM's copies for D = A B^T (M > 128, K > 0), no MMAs.
+fp4_status launch_gemm_copies(const GemmJob &j, cudaStream_t s) {
+  uint32_t *status = status_word();
+  if (!status) return FP4_ERR_CUDA;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, j.qa, j.M, j.K / 2, kCpHalf) || !make_map(&mb, j.qb, j.N, j.K / 2, kCpHalf))
+    return FP4_ERR_CUDA;
+  CopyParams p{};
+  p.sfa = j.sfa;
+  p.sfb = j.sfb;
+  p.m_tiles = (int)ceil_div(j.M, 256);
+  p.n_tiles = (int)ceil_div(j.N, 256);
+  p.k_tiles = (int)ceil_div(j.K, 256);
+  p.n_fast = j.M >= j.N ? 1 : 0;
+  const int blk = (j.fmt == kMXFP4) ? 32 : 16;
+  p.apk = (j.fmt == kMXFP4) ? 2 : 4;
+  p.cp4 = ceil_div(j.K / blk, 4);
+  p.ngrp_a = ceil_div(j.M, 128);
+  p.ngrp_b = ceil_div(j.N, 128);
+  p.status = status;
+  static cudaError_t attr =
+      cudaFuncSetAttribute(k_gemm_copies, cudaFuncAttributeMaxDynamicSharedMemorySize, kCpSmem);
+  if (attr != cudaSuccess) return FP4_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = kCpSmem;
+  int nmax = 0;
+  if (cudaOccupancyMaxActiveClusters(&nmax, k_gemm_copies, &cfg) != cudaSuccess || nmax <= 0)
+    return FP4_ERR_CUDA;
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int64_t nc = tiles < nmax ? tiles : nmax;
+  k_gemm_copies<<<(unsigned)(2 * nc), 32, kCpSmem, s>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
 
 fp4_status launch_mma_loop(int kind, int64_t iters, cudaStream_t s) {
   uint32_t *status = status_word();

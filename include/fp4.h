@@ -338,6 +338,21 @@ fp4_status fp4_gemm_quantize(const fp4_operand *A, const fp4_operand *B, int64_t
 typedef enum { FP4_MMA_FP4 = 0, FP4_MMA_FP8 = 1, FP4_MMA_BF16 = 2 } fp4_mma_kind;
 fp4_status fp4_mma_loop(int32_t kind, int64_t iters, void *stream);
 
+/* Copy-side diagnostic for fp4_gemm (the other roofline context for the
+ * GEMMs, not a step of the method): for D = A B^T with M > 128 it issues
+ * exactly the copies the SM-pair kernel issues -- per 256 x 256 tile and
+ * K256 stage, 128 rows of A and of B per CTA by tensor TMA and the scale
+ * tiles by bulk copy, into the same five-stage shared-memory ring over the
+ * same clusters -- with no MMA and no epilogue, each slot refilled as soon
+ * as its copies have landed.  The caller times it against fp4_gemm on the
+ * same operands: the ratio is the share of the GEMM's time that its shared
+ * memory takes to fill.  Operands, shapes and errors as fp4_gemm (nothing is
+ * written); M <= 128 returns FP4_ERR_UNSUPPORTED; M, N or K == 0 does
+ * nothing.  A copy that does not land within about a second raises the
+ * timeout status bit. */
+fp4_status fp4_gemm_copies(const fp4_operand *A, const fp4_operand *B, int64_t M, int64_t N,
+                           int64_t K, void *stream);
+
 /* Bytes of one scale-factor output for a copy with `rows` rows and `cols`
  * elements per row; -1 for an invalid format/layout. */
 int64_t fp4_sf_bytes(int32_t format, int64_t rows, int64_t cols,

@@ -257,6 +257,21 @@ def test_mma_loop_argument_errors_before_any_launch(L):
     assert f(fq.FP4_MMA_FP4, 1000001, None) == 1
 
 
+def test_gemm_copies_argument_errors_before_any_launch(L):
+    """fp4_gemm_copies validates like fp4_gemm; the one-SM shapes (M <= 128)
+    are refused and empty shapes do nothing, all before any pointer is used
+    (every operand below has null pointers)."""
+    f = L.fp4_gemm_copies
+    op = lambda fmt, rows, k: ctypes.byref(fq.fp4_operand(None, None, None, None, fmt, rows, k))
+    assert f(None, None, 256, 256, 256, None) == fq.FP4_ERR_INVALID_ARG
+    assert f(op(0, 256, 256), op(1, 256, 256), 256, 256, 256, None) == fq.FP4_ERR_INVALID_ARG
+    assert f(op(0, 256, 256), op(0, 256, 256), 256, 256, 320, None) == fq.FP4_ERR_SHAPE
+    assert f(op(0, 256, 96), op(0, 256, 96), 256, 256, 96, None) == fq.FP4_ERR_SHAPE
+    assert f(op(0, 128, 256), op(0, 256, 256), 128, 256, 256, None) == fq.FP4_ERR_UNSUPPORTED
+    assert f(op(0, 0, 256), op(0, 256, 256), 0, 256, 256, None) == fq.FP4_OK
+    assert f(op(0, 256, 0), op(0, 256, 0), 256, 256, 0, None) == fq.FP4_OK
+
+
 def test_wrappers_reject_host_tensors_and_wrong_dtypes_before_any_launch(L):
     """A host tensor's pointer never reaches a kernel: every allocating
     wrapper checks device, dtype and layout first (these tensors live on the

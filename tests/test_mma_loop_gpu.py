@@ -1,7 +1,11 @@
-"""The tensor-pipe rate diagnostic (fp4_mma_loop): every kind runs, leaves
-the status word clean, and reports a rate that a device doing the stated
-MMAs can reach -- above a tenth of the nominal dense peak and not above it
-(by more than timing noise), so the timed kernel does the work it claims."""
+"""The roofline diagnostics.  The tensor-pipe rate (fp4_mma_loop): every
+kind runs, leaves the status word clean, and reports a rate that a device
+doing the stated MMAs can reach -- above a tenth of the nominal dense peak
+and not above it (by more than timing noise), so the timed kernel does the
+work it claims.  The GEMM's copies alone (fp4_gemm_copies): they land
+(clean status) and take no longer than the GEMM that makes them, but a
+real share of it; at the rate they imply, an SM's shared memory is filled
+more slowly than its 128-byte-per-cycle port allows."""
 import pytest
 import torch
 
@@ -38,3 +42,48 @@ def test_mma_loop_scales_with_iterations():
     t1, t2 = ms(8000), ms(16000)
     assert 1.6 < t2 / t1 < 2.4, (t1, t2)
     assert fq.fp4_status_sync() == fq.FP4_OK
+
+
+def _median_ms(fn, reps=5):
+    s = torch.cuda.current_stream()
+    fn()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return sorted(times)[len(times) // 2]
+
+
+@pytest.mark.parametrize("fmt", [fq.FP4_FMT_UE5M3_B16, fq.FP4_FMT_MXFP4_B32])
+def test_gemm_copies_bounded_by_the_gemm(fmt):
+    need_gpu()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    M, N, K = 2048, 4096, 8192
+    x = torch.randn(M, K, device="cuda", dtype=torch.bfloat16, generator=g)
+    w = torch.randn(N, K, device="cuda", dtype=torch.bfloat16, generator=g)
+    p = fq.params(format=fmt, T=448.0, sf_layout=fq.FP4_SF_MMA)
+    a = fq.quantize(x, fq.amax(x)[0], p)
+    b = fq.quantize(w, fq.amax(w)[0], p)
+    D = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    t_gemm = _median_ms(lambda: fq.gemm(a, b, out=D))
+    t_copy = _median_ms(lambda: fq.gemm_copies(a, b))
+    assert fq.fp4_status_sync() == fq.FP4_OK
+    assert t_copy < 1.1 * t_gemm, (t_copy, t_gemm)
+    assert t_copy > 0.1 * t_gemm, (t_copy, t_gemm)
+    stage = 2 * 16384 + 3 * (2 if fmt == fq.FP4_FMT_MXFP4_B32 else 4) * 512
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_sm = (M // 256) * (N // 256) * (K // 256) * 2 * stage / sms / (t_copy * 1e-3)
+    assert per_sm < 128 * 2.07e9, per_sm
+
+
+def test_gemm_copies_refuses_one_sm_shapes():
+    need_gpu()
+    x = torch.randn(128, 256, device="cuda", dtype=torch.bfloat16)
+    p = fq.params(format=fq.FP4_FMT_UE5M3_B16, T=448.0, sf_layout=fq.FP4_SF_MMA)
+    a = fq.quantize(x, fq.amax(x)[0], p)
+    with pytest.raises(RuntimeError):
+        fq.gemm_copies(a, a)
